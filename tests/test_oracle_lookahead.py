@@ -1,0 +1,261 @@
+"""Pins of the oracle's lookahead method: the mask against brute force, the
+pages' worked examples and tables, Algorithm 3 cases, the lossless
+invariant, pool replay, KV recompute and the progress bound."""
+import json
+import os
+from fractions import Fraction
+from itertools import product
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import decoder, lookahead as la, philox
+
+from conftest import GOLDEN
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("N,W,G", [(2, 1, 0), (2, 3, 2), (3, 4, 4), (4, 5, 2), (5, 15, 15), (5, 5, 5)])
+def test_mask_closed_form_equals_brute_force(N, W, G):
+    rows = la.step_rows(N, W, G)
+    mask = la.step_mask(N, W, G)
+    for r in range(len(rows)):
+        brute = set(la.ancestors(rows, r)) | {r}
+        assert set(np.nonzero(mask[r])[0]) == brute
+
+
+@pytest.mark.parametrize("N,W,G", [(3, 4, 4), (4, 5, 2), (5, 7, 7)])
+def test_mask_structure(N, W, G):
+    """Causal in position, no edges between the branches or between two
+    candidates, lookahead rows see their column history and the oldest
+    level's left context."""
+    rows = la.step_rows(N, W, G)
+    mask = la.step_mask(N, W, G)
+    for r, s in product(range(len(rows)), repeat=2):
+        if not mask[r, s] or r == s:
+            continue
+        assert rows[s].depth < rows[r].depth
+        if s != 0:
+            assert rows[r].kind == rows[s].kind
+            if rows[r].kind == "cand":
+                assert rows[r].a == rows[s].a
+    for k in range(N - 1):
+        for j in range(W):
+            r = la.look_row(N, W, k, j)
+            seen = {(rows[s].a, rows[s].b) for s in np.nonzero(mask[r])[0] if rows[s].kind == "look"}
+            want = {(kk, j) for kk in range(k + 1)} | {(0, jj) for jj in range(j)}
+            assert seen == want
+
+
+def test_table4_extra_tokens():
+    for case in _load("table4_rows.json")["cases"]:
+        rows = la.step_rows(case["N"], case["W"], case["G"])
+        assert len(rows) - 1 == case["extra"]
+
+
+def test_fig1_ngram_is_a_diagonal():
+    g = _load("fig1_ngram.json")
+    N, W = g["N"], g["W"]
+    rows = la.step_rows(N, W, g["G"])
+    window = np.zeros((N - 1, W), dtype=np.int64)
+    for k in range(N - 1):
+        for j in range(W):
+            depth = rows[la.look_row(N, W, k, j)].depth
+            window[k, j] = 100 * (k + 1) + depth
+    new = [100 * N + rows[la.look_row(N, W, N - 2, j)].depth + 1 for j in range(W)]
+    grams = [(key,) + suf for key, suf in la.harvest(window, new)]
+    assert tuple(g["example_ngram"]) in grams
+
+
+def test_alg3_golden_cases():
+    for case in _load("alg3_cases.json")["cases"]:
+        cands = [tuple(c) for c in case["cands"]]
+        acc, win = la.greedy_verify(cands, case["row0"], lambda c, m: case["cand"][c][m - 1])
+        assert acc == case["accepted"], case["name"]
+        assert win == case["winner"], case["name"]
+        assert 1 <= len(acc) <= case["N"]
+
+
+def test_pool_fifo_and_dedup():
+    p = la.Pool(cap=3)
+    p.insert(7, (1, 2))
+    p.insert(7, (3, 4))
+    p.insert(7, (1, 2))            # present: no-op, order unchanged
+    assert p.lookup(7, 10) == [(1, 2), (3, 4)]
+    p.insert(7, (5, 6))
+    p.insert(7, (8, 9))            # over capacity: oldest (1, 2) leaves
+    assert p.lookup(7, 10) == [(3, 4), (5, 6), (8, 9)]
+    assert p.lookup(7, 2) == [(3, 4), (5, 6)]
+    p.insert(1, (0, 0))
+    assert p.records() == [(1, (0, 0)), (7, (3, 4)), (7, (5, 6)), (7, (8, 9))]
+    assert p.lookup(99, 4) == []
+
+
+@pytest.mark.parametrize("N,W,G,par", [(3, 4, 4, False), (2, 3, 3, False), (4, 2, 5, False),
+                                       (5, 3, 0, False), (3, 1, 2, True), (4, 4, 4, True)])
+def test_lossless_vs_autoregressive(tiny, N, W, G, par):
+    """Greedy lookahead output == greedy autoregressive output (fp64)."""
+    wl, w, p = tiny
+    ar = la.generate_ar(w, p, 48)
+    o = la.Lookahead(w, N, W, G, prompt_as_reference=par)
+    out, steps = o.generate(p, 48)
+    assert out == ar
+    acc_lens = [len(r.accepted) for r in o.history]
+    assert all(1 <= a <= N for a in acc_lens)
+    assert 1 + sum(acc_lens) == len(o.tokens) - len(p)
+    if G == 0:
+        assert steps == 47
+
+
+def test_lossless_repetitive_prompt(tiny):
+    """A repeated prompt with prompt-as-reference: candidates get accepted."""
+    wl, w, _ = tiny
+    chunk = synth.uniform_tokens(8, wl.dims.vocab, seed=9)
+    p = np.tile(chunk, 5)
+    ar = la.generate_ar(w, p, 40)
+    o = la.Lookahead(w, 4, 3, 4, prompt_as_reference=True)
+    out, steps = o.generate(p, 40)
+    assert out == ar
+
+
+def test_pool_replay_from_window_trajectory(tiny):
+    """The pool after each step equals the n-grams read off the logged window
+    trajectory (plus the prompt's, when seeded), replayed in order."""
+    wl, w, p = tiny
+    N, W, G = 4, 3, 3
+    o = la.Lookahead(w, N, W, G, prompt_as_reference=True, pool_cap=2)
+    o.prefill(p)
+    for _ in range(12):
+        o.step()
+    grams = [(int(p[i]), tuple(int(t) for t in p[i + 1:i + N])) for i in range(len(p) - N + 1)]
+    for t, rec in enumerate(o.history):
+        # the window a step starts from is the previous window slid by the previous new tokens
+        if t:
+            prev = o.history[t - 1]
+            np.testing.assert_array_equal(rec.window_before[:-1], prev.window_before[1:])
+            np.testing.assert_array_equal(rec.window_before[-1], prev.new)
+        for j in range(W):
+            grams.append((int(rec.window_before[0, j]),
+                          tuple(int(rec.window_before[k, j]) for k in range(1, N - 1)) + (rec.new[j],)))
+    lists = {}
+    for key, suf in grams:
+        lst = lists.setdefault(key, [])
+        if suf not in lst:
+            lst.append(suf)
+            del lst[:-2]
+    assert sorted((k, s) for k, v in lists.items() for s in v) == sorted(o.pool.records())
+    assert [(k, s) for k in sorted(lists) for s in lists[k]] == o.pool.records()
+
+
+def test_kv_after_steps_equals_fresh_prefill(tiny):
+    wl, w, p = tiny
+    o = la.Lookahead(w, 3, 4, 4)
+    o.prefill(p)
+    for _ in range(6):
+        o.step()
+    P = o.P
+    _, fresh = decoder.forward(w, o.tokens[:P], np.arange(P), decoder.causal_mask(0, P))
+    for (k1, v1), (k2, v2) in zip(o.cache, fresh):
+        np.testing.assert_allclose(k1, k2, atol=1e-12)
+        np.testing.assert_allclose(v1, v2, atol=1e-12)
+
+
+def test_window_init_and_splitmix():
+    g = _load("splitmix64.json")
+    x, outs = g["seed"], []
+    for _ in range(2):
+        outs.append(str(la.splitmix64(x)))
+        x = (x + 0x9E3779B97F4A7C15) % 2 ** 64
+    assert outs == g["outputs"]
+    prompt = list(range(100, 137))
+    V = la.init_window(prompt, 4, 5, seed=3)
+    assert V.shape == (3, 5)
+    for k in range(3):
+        for j in range(5):
+            assert V[k, j] == prompt[la.splitmix64(3 ^ (k * 5 + j)) % len(prompt)]
+
+
+def test_philox_known_answers():
+    for case in _load("philox_kat.json")["cases"]:
+        out = philox.philox4x32_10([int(c, 16) for c in case["ctr"]], [int(c, 16) for c in case["key"]])
+        assert out == [int(c, 16) for c in case["out"]]
+        # and the input generator's C implementation
+        assert synth.philox4x32_10([int(c, 16) for c in case["ctr"]], [int(c, 16) for c in case["key"]]) == out
+
+
+def test_inverse_cdf_exact_frequencies():
+    w = np.array([0.1, 0.0, 0.2, 0.3, 0.4])
+    counts = np.zeros(5, int)
+    for k in range(1000):
+        counts[la.inverse_cdf(w, (k + 0.5) / 1000)] += 1
+    assert counts.tolist() == [100, 0, 200, 300, 400]
+
+
+def _exact_rejection_chain(p, tokens):
+    """Probability of each output token for one depth of Algorithm 4, by
+    exact enumeration over accept/reject outcomes (rational arithmetic)."""
+    out = {x: Fraction(0) for x in range(len(p))}
+
+    def rec(dist, i, prob, rejected):
+        while i < len(tokens) and tokens[i] in rejected:
+            i += 1
+        if i == len(tokens):
+            tot = sum(dist)
+            for x in range(len(dist)):
+                out[x] += prob * dist[x] / tot
+            return
+        x = tokens[i]
+        px = dist[x] / sum(dist)
+        out[x] += prob * px
+        nd = list(dist)
+        nd[x] = Fraction(0)
+        rec(nd, i + 1, prob * (1 - px), rejected | {x})
+
+    rec([Fraction(v) for v in p], 0, Fraction(1), frozenset())
+    return out
+
+
+@pytest.mark.parametrize("tokens", [[0], [3, 1], [2, 2, 5], [1, 4, 6, 7, 0]])
+def test_sampling_rule_preserves_distribution_exactly(tokens):
+    """Appendix B's claim for one depth: with greedy (one-hot) drafts the
+    output token is distributed exactly as the model's distribution."""
+    p = [Fraction(k, 36) for k in (1, 2, 3, 4, 5, 6, 7, 8)]
+    got = _exact_rejection_chain(p, tokens)
+    assert all(got[x] == p[x] for x in range(8))
+
+
+def test_sampling_verify_joint_distribution_monte_carlo():
+    """The oracle's Algorithm 4 over two depths: first two output tokens are
+    distributed as p(x1) q_x1(x2), by a chi-square test over seeds."""
+    V = 4
+    p = np.array([0.1, 0.2, 0.3, 0.4])
+    q = np.array([[0.25, 0.25, 0.25, 0.25], [0.7, 0.1, 0.1, 0.1], [0.05, 0.05, 0.1, 0.8], [0.3, 0.3, 0.2, 0.2]])
+    cands = [(2, 3), (3, 0), (2, 1)]
+    counts = np.zeros((V, V))
+    n = 20000
+    for seed in range(n):
+        acc, _ = la.sampling_verify(cands, p, lambda c, m: q[cands[c][0]], P=5, seed=seed, N=3)
+        if len(acc) >= 2:
+            counts[acc[0], acc[1]] += 1
+        else:
+            # stopped after one token: the next token would come from q[x1] in the following step
+            x1 = acc[0]
+            x2 = la.inverse_cdf(q[x1], philox.uniform(seed + 10 ** 6, 0, 0))
+            counts[x1, x2] += 1
+    expect = n * p[:, None] * q
+    chi2 = np.sum((counts - expect) ** 2 / expect)
+    assert chi2 < 45.0, chi2   # 15 dof: p < 1e-4 false-alarm rate
+
+
+def test_sampling_progress_bounds(tiny):
+    wl, w, p = tiny
+    o = la.Lookahead(w, 3, 4, 4, temperature=1.0, seed=11, prompt_as_reference=True)
+    out, steps = o.generate(np.tile(p[:8], 4), 32)
+    assert len(out) == 32
+    for rec in o.history:
+        assert 1 <= len(rec.accepted) <= 3
