@@ -1,0 +1,262 @@
+// Projection GEMMs of the lookahead step: every weight byte is read once per
+// step and multiplied against all M = 1 + (W+G)(N-1) step rows at once
+// (the "extra tokens per step" of section 4 of the paper-graph-ui page ride
+// on the same weight stream).
+//
+// bf16 path -- tcgen05 tensor cores, swap-AB: the weight matrix [out][K] is
+// the UMMA A operand (128 output features per tile, K-major), the step rows
+// [rows][K] are the B operand (N = rows padded to 16), the fp32 accumulator
+// lives in TMEM (128 lanes x N columns).  One warp issues TMA loads into a
+// shared-memory ring, one thread issues UMMAs, four warps drain TMEM.  Small
+// projections are split along K so that every SM streams weights; partial
+// sums go to a workspace and are added in a fixed order by the consumer
+// kernel, so results are deterministic.
+//
+// fp32 path -- a plain SIMT kernel (fp32 FMA, no tf32) for fp32 models.
+#include <cstdio>
+
+#include "la_kernels.h"
+
+namespace la {
+
+// ------------------------------------------------------------------ tcgen05 kernel
+__global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const int bn = p.bn;
+    const uint32_t a_bytes = kTileM * kBlockK * 2;
+    const uint32_t b_bytes = static_cast<uint32_t>(bn) * kBlockK * 2;
+    const uint32_t stage_bytes = a_bytes + b_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * stage_bytes);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + p.stages;
+    uint64_t *accb = bars + 2 * p.stages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.stages + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+    int seg = 0;
+    while (seg + 1 < p.nseg && tile >= p.seg_tile0[seg + 1]) ++seg;
+    const int row0 = (tile - p.seg_tile0[seg]) * kTileM;
+    const int kb0 = static_cast<int>((static_cast<long long>(split) * p.n_kb) / p.splits);
+    const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * p.n_kb) / p.splits);
+    const int nk = kb1 - kb0;
+    uint32_t ncols = 32;
+    while (ncols < static_cast<uint32_t>(bn)) ncols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), 1);
+        }
+        mbar_init(smem_u32(accb), 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), ncols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // TMA producer: weights stream through L2 once (evict first); the
+            // small row block is re-read by every CTA (evict last).
+            prefetch_tensormap(&p.a[seg]);
+            prefetch_tensormap(&p.b);
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            for (int i = 0; i < nk; ++i) {
+                const int st = i % p.stages;
+                if (i >= p.stages && !mbar_wait(smem_u32(&empty[st]), ((i / p.stages) & 1) ^ 1, p.err, ERR_TIMEOUT_EMPTY))
+                    break;
+                const uint32_t sa = smem_u32(smem + st * stage_bytes);
+                const uint32_t fb = smem_u32(&full[st]);
+                mbar_arrive_expect_tx(fb, stage_bytes);
+                tma_load_2d(sa, &p.a[seg], (kb0 + i) * kBlockK, row0, fb, pol_w);
+                tma_load_2d(sa + a_bytes, &p.b, (kb0 + i) * kBlockK, 0, fb, pol_x);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // UMMA issuer: 4 instructions of K = 16 per 64-wide stage.
+            const uint32_t idesc = umma_idesc_bf16(kTileM, bn);
+            for (int i = 0; i < nk; ++i) {
+                const int st = i % p.stages;
+                if (!mbar_wait(smem_u32(&full[st]), (i / p.stages) & 1, p.err, ERR_TIMEOUT_FULL)) break;
+                tc_fence_after();
+                const uint32_t sa = smem_u32(smem + st * stage_bytes);
+                const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + a_bytes);
+#pragma unroll
+                for (int kk = 0; kk < kBlockK / 16; ++kk)
+                    umma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
+                umma_commit(smem_u32(&empty[st]));
+            }
+            umma_commit(smem_u32(accb));
+        }
+    } else {
+        // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = output features.
+        bool ok = mbar_wait(smem_u32(accb), 0, p.err, ERR_TIMEOUT_ACCUM);
+        ok = __all_sync(0xffffffffu, ok) && nk > 0;
+        __syncwarp();
+        tc_fence_after();
+        if (ok) {
+            const int q = warp & 3;
+            const int f = row0 + 32 * q + lane;
+            const bool fv = f < p.seg_out[seg];
+            float *out = p.out + static_cast<long long>(split) * p.split_stride + p.seg_col0[seg] + f;
+            for (int c0 = 0; c0 < bn; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c0), r);
+                tmem_ld_wait();
+                if (fv) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int row = c0 + j;
+                        if (row < p.nrows) out[static_cast<long long>(row) * p.ldo] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, ncols);
+    }
+}
+
+size_t tc_gemm_smem_bytes(int bn, int stages) {
+    return static_cast<size_t>(stages) * (kTileM * kBlockK * 2 + bn * kBlockK * 2) + 1024 + 256;
+}
+
+int tc_gemm_stages_for(int bn) {
+    // Two CTAs per SM when they fit (about 113 KB each), else one deep ring.
+    const size_t stage = kTileM * kBlockK * 2 + static_cast<size_t>(bn) * kBlockK * 2;
+    int s = static_cast<int>((113 * 1024 - 1280) / stage);
+    if (s >= 3) return s > 6 ? 6 : s;
+    s = static_cast<int>((220 * 1024 - 1280) / stage);
+    return s > 8 ? 8 : (s < 2 ? 2 : s);
+}
+
+int tc_gemm_ctas_per_sm(int bn, int stages) {
+    const size_t sm = tc_gemm_smem_bytes(bn, stages);
+    cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_gemm_tc, 192, sm) != cudaSuccess) n = 1;
+    return n < 1 ? 1 : n;
+}
+
+int choose_splits(int tiles, int n_kb, int slots) {
+    // Minimise waves/split with a small charge per split for the partial
+    // traffic; keep >= 4 k-blocks (256 K) per CTA.
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= 16; ++s) {
+        if (s > 1 && n_kb / s < 4) break;
+        const int ctas = tiles * s;
+        const int waves = (ctas + slots - 1) / slots;
+        const double cost = static_cast<double>(waves) / s * (1.0 + 0.04 * s);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+void tc_gemm_finalize(TcGemm &g) {
+    g.grid = g.p.seg_tile0[g.p.nseg] * g.p.splits;
+    g.smem = tc_gemm_smem_bytes(g.p.bn, g.p.stages);
+}
+
+cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s) {
+    static int configured_smem = 0;
+    if (static_cast<int>(g.smem) > configured_smem) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(g.smem));
+        if (e != cudaSuccess) return e;
+        configured_smem = static_cast<int>(g.smem);
+    }
+    k_gemm_tc<<<g.grid, 192, g.smem, s>>>(g.p);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+int make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                   uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return -1;
+    if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_bytes & 15)) return -2;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -3;
+}
+
+// ------------------------------------------------------------------ fp32 SIMT path
+__global__ void k_gemm_simt(const SimtGemmParams p, int total_f) {
+    const int f = blockIdx.x * 64 + (threadIdx.x & 63);
+    const int r = blockIdx.y * 4 + (threadIdx.x >> 6);
+    if (f >= total_f || r >= p.nrows) return;
+    int seg = 0;
+    while (seg + 1 < p.nseg && f >= p.seg_f0[seg + 1]) ++seg;
+    const int fl = f - p.seg_f0[seg];
+    const float *w = p.a[seg] + static_cast<long long>(fl) * p.K;
+    const float *x = p.x + static_cast<long long>(r) * p.ldx;
+    float acc = 0.f;
+    for (int k = 0; k < p.K; ++k) acc = fmaf(x[k], w[k], acc);
+    p.out[static_cast<long long>(r) * p.ldo + p.seg_col0[seg] + fl] = acc;
+}
+
+cudaError_t simt_gemm_launch(const SimtGemmParams &p, int total_f, cudaStream_t s) {
+    dim3 grid((total_f + 63) / 64, (p.nrows + 3) / 4);
+    k_gemm_simt<<<grid, 256, 0, s>>>(p, total_f);
+    return cudaGetLastError();
+}
+
+__global__ void k_reduce_splits(const float *part, int splits, long long stride, long long n, float *y) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        float acc = part[i];
+        for (int s = 1; s < splits; ++s) acc += part[s * stride + i];
+        y[i] = acc;
+    }
+}
+
+cudaError_t reduce_splits_launch(const float *part, int splits, long long stride, int rows, int cols, float *y,
+                                 cudaStream_t s) {
+    const long long n = static_cast<long long>(rows) * cols;
+    int blocks = static_cast<int>((n + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    k_reduce_splits<<<blocks, 256, 0, s>>>(part, splits, stride, n, y);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -1,0 +1,925 @@
+// Host runtime behind include/la.h: the handle, its device buffers, the GEMM
+// launch plans and the orchestration of prefill and of one lookahead step
+// (paper-graph-ui page, section 3.4: lookahead branch + verification branch
+// + pool update in one forward pass).  Everything that touches step data
+// runs in the kernels of this library on the caller's stream; the host only
+// sequences launches and copies the step's accepted tokens back.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "../../include/la.h"
+#include "la_kernels.h"
+
+using namespace la;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+#define CK(call)                                                                                          \
+    do {                                                                                                  \
+        cudaError_t e_ = (call);                                                                          \
+        if (e_ != cudaSuccess) return fail(LA_ERR_CUDA, "%s: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                                           __FILE__, __LINE__);                                           \
+    } while (0)
+
+constexpr int kPrefillRows = 128;
+
+enum Mode { STEP = 0, PREFILL = 1 };
+enum Kind { QKV = 0, OPROJ = 1, GATEUP = 2, DOWN = 3 };
+
+int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+struct la_handle {
+    la_model_dims dims{};
+    la_opts opts{};
+    cudaStream_t stream = nullptr;
+    bool bf16 = true;
+    int L = 0, d = 0, nh = 0, nkv = 0, hd = 0, F = 0, V = 0, qd = 0, kvd = 0, qkv_out = 0;
+    int N = 0, W = 0, G = 0, M = 0, U = 0, cap = 0, max_seq = 0, R = 0;
+    int bn_step = 0, bn_pf = 0, bn_u = 0;
+    size_t act = 4;   // bytes per activation element
+
+    // caller's weights
+    const void *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
+    std::vector<const void *> attn_norm, wq, wk, wv, wo, ffn_norm, wg, wu, wd;
+
+    // device buffers (owned)
+    std::vector<void *> allocs;
+    float *h = nullptr, *part = nullptr, *q = nullptr, *logits = nullptr, *lmax = nullptr, *lsum = nullptr;
+    float *attn_ws = nullptr;
+    void *xn = nullptr, *ao = nullptr, *fa = nullptr, *xu = nullptr, *cache = nullptr;
+    float2 *rope = nullptr;
+    int *amax = nullptr, *tok = nullptr, *depth = nullptr, *anc = nullptr, *anc_cnt = nullptr, *used = nullptr;
+    int *iota = nullptr;
+    int anc_stride = 0;
+    SpecState *st = nullptr;
+    SpecState *st_host = nullptr;   // pinned
+    int *tokens_log = nullptr, *window = nullptr, *cands = nullptr;
+    int *pkeys = nullptr, *pcnt = nullptr, *phead = nullptr, *pent = nullptr;
+    int nslots_log2 = 0;
+    int *records_dev = nullptr;
+    size_t records_dev_cap = 0;
+
+    // GEMM plans (bf16): [mode][kind][layer]
+    std::vector<TcGemm> plan[2][4];
+    TcGemm plan_lm;
+    int splits[2][4] = {{1, 1, 1, 1}, {1, 1, 1, 1}};
+    size_t part_elems = 0;
+
+    // host-side bookkeeping
+    bool prefilled = false;
+    int P = 0;
+    int64_t steps = 0, generated = 0;
+    int last_A = 0, last_g = 0, logits_rows = 0;
+
+    ~la_handle() {
+        for (void *p : allocs) cudaFree(p);
+        if (st_host) cudaFreeHost(st_host);
+    }
+
+    template <typename T>
+    int alloc(T **p, size_t n) {
+        void *v = nullptr;
+        if (n == 0) n = 1;
+        cudaError_t e = cudaMalloc(&v, n * sizeof(T));
+        if (e != cudaSuccess) return fail(LA_ERR_OOM, "cudaMalloc(%zu bytes): %s", n * sizeof(T), cudaGetErrorString(e));
+        allocs.push_back(v);
+        *p = static_cast<T *>(v);
+        return LA_OK;
+    }
+    int alloc_bytes(void **p, size_t bytes) {
+        void *v = nullptr;
+        cudaError_t e = cudaMalloc(&v, bytes ? bytes : 1);
+        if (e != cudaSuccess) return fail(LA_ERR_OOM, "cudaMalloc(%zu bytes): %s", bytes, cudaGetErrorString(e));
+        allocs.push_back(v);
+        *p = v;
+        return LA_OK;
+    }
+
+    SpecDev spec() const {
+        SpecDev s{};
+        s.st = st;
+        s.tokens_log = tokens_log;
+        s.max_seq = max_seq;
+        s.window = window;
+        s.cands = cands;
+        s.tok = tok;
+        s.amax = amax;
+        s.logits = logits;
+        s.lmax = lmax;
+        s.lsum = lsum;
+        s.V = V;
+        s.pkeys = pkeys;
+        s.pcnt = pcnt;
+        s.phead = phead;
+        s.pent = pent;
+        s.nslots_log2 = nslots_log2;
+        s.cap = cap;
+        s.N = N;
+        s.W = W;
+        s.G = G;
+        s.M = M;
+        s.U = U;
+        s.T = opts.temperature;
+        s.seed = opts.seed;
+        return s;
+    }
+
+    void *kv_layer(int l, int which) const {
+        const size_t plane = static_cast<size_t>(nkv) * max_seq * hd * act;
+        return static_cast<char *>(cache) + (static_cast<size_t>(l) * 2 + which) * plane;
+    }
+};
+
+namespace {
+
+// ------------------------------------------------------------------ step-row structure
+// Parent of each step row (reading of Figure 2b): (0,0) -> row 0, (0,j) ->
+// (0,j-1), (k>=1,j) -> (k-1,j), (c,1) -> row 0, (c,m) -> (c,m-1).
+void step_structure(int N, int W, int G, std::vector<int> &parent, std::vector<int> &depth) {
+    const int L = N - 1, M = 1 + (W + G) * L;
+    parent.assign(M, -1);
+    depth.assign(M, 0);
+    for (int k = 0; k < L; ++k)
+        for (int j = 0; j < W; ++j) {
+            const int r = 1 + k * W + j;
+            parent[r] = k == 0 ? (j == 0 ? 0 : r - 1) : r - W;
+            depth[r] = 1 + j + k;
+        }
+    for (int c = 0; c < G; ++c)
+        for (int m = 1; m <= L; ++m) {
+            const int r = 1 + L * W + c * L + (m - 1);
+            parent[r] = m == 1 ? 0 : r - 1;
+            depth[r] = m;
+        }
+}
+
+uint64_t splitmix64(uint64_t x) {
+    x += 0x9E3779B97F4A7C15ull;
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    return x ^ (x >> 31);
+}
+
+// ------------------------------------------------------------------ GEMM dispatch
+int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
+    const int ldo = kind == QKV ? h->qkv_out : kind == GATEUP ? 2 * h->F : h->d;
+    if (h->bf16) {
+        TcGemm g = h->plan[mode][kind][l];
+        g.p.nrows = nrows;
+        CK(tc_gemm_launch(g, h->stream));
+        return LA_OK;
+    }
+    SimtGemmParams p{};
+    int K = h->d;
+    const void *x = h->xn;
+    if (kind == QKV) {
+        p.nseg = 3;
+        p.a[0] = static_cast<const float *>(h->wq[l]);
+        p.a[1] = static_cast<const float *>(h->wk[l]);
+        p.a[2] = static_cast<const float *>(h->wv[l]);
+        const int outs[3] = {h->qd, h->kvd, h->kvd};
+        int acc = 0;
+        for (int i = 0; i < 3; ++i) {
+            p.seg_f0[i] = acc;
+            p.seg_col0[i] = acc;
+            acc += outs[i];
+        }
+        p.seg_f0[3] = acc;
+    } else if (kind == GATEUP) {
+        p.nseg = 2;
+        p.a[0] = static_cast<const float *>(h->wg[l]);
+        p.a[1] = static_cast<const float *>(h->wu[l]);
+        p.seg_f0[0] = 0;
+        p.seg_col0[0] = 0;
+        p.seg_f0[1] = h->F;
+        p.seg_col0[1] = h->F;
+        p.seg_f0[2] = 2 * h->F;
+    } else {
+        p.nseg = 1;
+        p.a[0] = static_cast<const float *>(kind == OPROJ ? h->wo[l] : h->wd[l]);
+        p.seg_f0[0] = 0;
+        p.seg_col0[0] = 0;
+        p.seg_f0[1] = h->d;
+        K = kind == OPROJ ? h->qd : h->F;
+        x = kind == OPROJ ? h->ao : h->fa;
+    }
+    p.x = static_cast<const float *>(x);
+    p.ldx = K;
+    p.K = K;
+    p.nrows = nrows;
+    p.ldo = ldo;
+    p.out = h->part;
+    CK(simt_gemm_launch(p, p.seg_f0[p.nseg], h->stream));
+    return LA_OK;
+}
+
+int run_lm_head(la_handle *h, int nrows) {
+    if (h->bf16) {
+        TcGemm g = h->plan_lm;
+        g.p.nrows = nrows;
+        CK(tc_gemm_launch(g, h->stream));
+        return LA_OK;
+    }
+    SimtGemmParams p{};
+    p.nseg = 1;
+    p.a[0] = static_cast<const float *>(h->lm_head);
+    p.seg_f0[0] = 0;
+    p.seg_f0[1] = h->V;
+    p.seg_col0[0] = 0;
+    p.x = static_cast<const float *>(h->xu);
+    p.ldx = h->d;
+    p.K = h->d;
+    p.nrows = nrows;
+    p.ldo = h->V;
+    p.out = h->logits;
+    CK(simt_gemm_launch(p, h->V, h->stream));
+    return LA_OK;
+}
+
+// ------------------------------------------------------------------ decoder forward
+// Runs nrows rows (tokens at `tok`) through all layers with prefix length P.
+// Step mode: positions P + depth[r], in-step keys from the ancestor table,
+// final norm of the used rows into xu.  Prefill mode: positions P + r,
+// causal in-step keys, final norm of the last row into xu row 0 when
+// `final_rows` > 0.
+template <typename T>
+int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want_logits) {
+    cudaStream_t s = h->stream;
+    const float eps = h->dims.rms_eps;
+    CK(embed_norm_launch<T>(static_cast<const T *>(h->embed), tok, nrows, h->d,
+                            static_cast<const T *>(h->attn_norm[0]), eps, h->h, static_cast<T *>(h->xn), s));
+    const int nch = (P + kAttnChunk - 1) / kAttnChunk;
+    for (int l = 0; l < h->L; ++l) {
+        int rc;
+        if ((rc = run_gemm(h, mode, QKV, l, nrows)) != LA_OK) return rc;
+        const long long ss_qkv = static_cast<long long>(h->R) * h->qkv_out;
+        CK(qkv_rope_launch<T>(h->part, h->splits[mode][QKV], ss_qkv, h->qkv_out, nrows, h->nh, h->nkv, h->hd,
+                              h->rope, P, mode == STEP ? h->depth : nullptr, h->q,
+                              static_cast<T *>(h->kv_layer(l, 0)), static_cast<T *>(h->kv_layer(l, 1)),
+                              h->max_seq, s));
+        AttnArgs a{};
+        a.q = h->q;
+        a.kc = h->kv_layer(l, 0);
+        a.vc = h->kv_layer(l, 1);
+        a.max_seq = h->max_seq;
+        a.P = P;
+        a.nrows = nrows;
+        a.nh = h->nh;
+        a.nkv = h->nkv;
+        a.hd = h->hd;
+        a.ws = h->attn_ws;
+        a.nch = nch;
+        a.anc = mode == STEP ? h->anc : nullptr;
+        a.anc_cnt = mode == STEP ? h->anc_cnt : nullptr;
+        a.anc_stride = h->anc_stride;
+        a.out = h->ao;
+        CK(attention_launch<T>(a, s));
+        if ((rc = run_gemm(h, mode, OPROJ, l, nrows)) != LA_OK) return rc;
+        const long long ss_d = static_cast<long long>(h->R) * h->d;
+        CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][OPROJ], ss_d, h->d, h->d,
+                                static_cast<const T *>(h->ffn_norm[l]), eps, nullptr, nrows,
+                                static_cast<T *>(h->xn), s));
+        if ((rc = run_gemm(h, mode, GATEUP, l, nrows)) != LA_OK) return rc;
+        const long long ss_gu = static_cast<long long>(h->R) * 2 * h->F;
+        CK(swiglu_launch<T>(h->part, h->splits[mode][GATEUP], ss_gu, 2 * h->F, nrows, h->F,
+                            static_cast<T *>(h->fa), s));
+        if ((rc = run_gemm(h, mode, DOWN, l, nrows)) != LA_OK) return rc;
+        if (l + 1 < h->L) {
+            CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][DOWN], ss_d, h->d, h->d,
+                                    static_cast<const T *>(h->attn_norm[l + 1]), eps, nullptr, nrows,
+                                    static_cast<T *>(h->xn), s));
+        } else if (want_logits) {
+            const int *map = mode == STEP ? h->used : h->iota + (nrows - 1);
+            const int rows = mode == STEP ? h->U : 1;
+            CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][DOWN], ss_d, h->d, h->d,
+                                    static_cast<const T *>(h->final_norm), eps, map, rows,
+                                    static_cast<T *>(h->xu), s));
+        }
+    }
+    return LA_OK;
+}
+
+int forward_any(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want_logits) {
+    return h->bf16 ? forward<__nv_bfloat16>(h, mode, tok, nrows, P, want_logits)
+                   : forward<float>(h, mode, tok, nrows, P, want_logits);
+}
+
+int kv_commit(la_handle *h) {
+    if (h->bf16)
+        CK(kv_commit_launch<__nv_bfloat16>(h->spec(), static_cast<__nv_bfloat16 *>(h->cache), h->L, h->nkv, h->hd,
+                                           h->stream));
+    else
+        CK(kv_commit_launch<float>(h->spec(), static_cast<float *>(h->cache), h->L, h->nkv, h->hd, h->stream));
+    return LA_OK;
+}
+
+int check_device_error(la_handle *h) {
+    if (h->st_host->err) {
+        const unsigned e = h->st_host->err;
+        h->prefilled = false;
+        return fail(LA_ERR_DEVICE_TIMEOUT, "device error bits 0x%x (bounded wait gave up or pool full)", e);
+    }
+    return LA_OK;
+}
+
+// KV of tokens_log[0 .. n) in prefill chunks; logits of the last row if asked.
+int run_prefix(la_handle *h, int n, bool want_logits) {
+    for (int c0 = 0; c0 < n; c0 += kPrefillRows) {
+        const int rows = std::min(kPrefillRows, n - c0);
+        const bool last = c0 + rows >= n;
+        int rc = forward_any(h, PREFILL, h->tokens_log + c0, rows, c0, want_logits && last);
+        if (rc != LA_OK) return rc;
+    }
+    if (want_logits) {
+        int rc = run_lm_head(h, 1);
+        if (rc != LA_OK) return rc;
+        CK(argmax_launch(h->logits, 1, h->V, h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
+                         h->lmax, h->lsum, h->stream));
+    }
+    return LA_OK;
+}
+
+int reset_pool(la_handle *h) {
+    const size_t nslots = static_cast<size_t>(1) << h->nslots_log2;
+    CK(cudaMemsetAsync(h->pkeys, 0xFF, nslots * sizeof(int), h->stream));
+    CK(cudaMemsetAsync(h->pcnt, 0, nslots * sizeof(int), h->stream));
+    CK(cudaMemsetAsync(h->phead, 0, nslots * sizeof(int), h->stream));
+    return LA_OK;
+}
+
+int build_plans(la_handle *h) {
+    int dev = 0;
+    CK(cudaGetDevice(&dev));
+    int nsm = 0;
+    CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+    const int bns[2] = {h->bn_step, h->bn_pf};
+    void *xs[2][4] = {{h->xn, h->ao, h->xn, h->fa}, {h->xn, h->ao, h->xn, h->fa}};
+    const int Ks[4] = {h->d, h->qd, h->d, h->F};
+    const int ldos[4] = {h->qkv_out, h->d, 2 * h->F, h->d};
+    size_t part_max = 0;
+    for (int mode = 0; mode < 2; ++mode) {
+        const int bn = bns[mode];
+        const int rows_map = mode == STEP ? h->M : kPrefillRows;
+        const int stages = tc_gemm_stages_for(bn);
+        const int slots = nsm * tc_gemm_ctas_per_sm(bn, stages);
+        for (int kind = 0; kind < 4; ++kind) {
+            const int K = Ks[kind];
+            CUtensorMap bmap;
+            if (make_tmap_bf16(&bmap, xs[mode][kind], K, rows_map, static_cast<uint64_t>(K) * 2, kBlockK, bn))
+                return fail(LA_ERR_CUDA, "tensor map for activations failed");
+            int outs[3], nseg;
+            if (kind == QKV) {
+                nseg = 3;
+                outs[0] = h->qd;
+                outs[1] = h->kvd;
+                outs[2] = h->kvd;
+            } else if (kind == GATEUP) {
+                nseg = 2;
+                outs[0] = outs[1] = h->F;
+            } else {
+                nseg = 1;
+                outs[0] = h->d;
+            }
+            int tiles = 0;
+            for (int i = 0; i < nseg; ++i) tiles += (outs[i] + kTileM - 1) / kTileM;
+            const int n_kb = (K + kBlockK - 1) / kBlockK;
+            const int S = choose_splits(tiles, n_kb, slots);
+            h->splits[mode][kind] = S;
+            part_max = std::max(part_max, static_cast<size_t>(S) * h->R * ldos[kind]);
+            h->plan[mode][kind].resize(h->L);
+            for (int l = 0; l < h->L; ++l) {
+                TcGemm &g = h->plan[mode][kind][l];
+                std::memset(&g.p, 0, sizeof(g.p));
+                const void *ws[3];
+                if (kind == QKV) {
+                    ws[0] = h->wq[l];
+                    ws[1] = h->wk[l];
+                    ws[2] = h->wv[l];
+                } else if (kind == GATEUP) {
+                    ws[0] = h->wg[l];
+                    ws[1] = h->wu[l];
+                } else {
+                    ws[0] = kind == OPROJ ? h->wo[l] : h->wd[l];
+                }
+                int t0 = 0, col = 0;
+                for (int i = 0; i < nseg; ++i) {
+                    if (make_tmap_bf16(&g.p.a[i], ws[i], K, outs[i], static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
+                        return fail(LA_ERR_INVALID_ARG, "tensor map for a weight failed (16-byte alignment?)");
+                    g.p.seg_tile0[i] = t0;
+                    g.p.seg_out[i] = outs[i];
+                    g.p.seg_col0[i] = col;
+                    t0 += (outs[i] + kTileM - 1) / kTileM;
+                    col += outs[i];
+                }
+                g.p.seg_tile0[nseg] = t0;
+                g.p.b = bmap;
+                g.p.nseg = nseg;
+                g.p.n_kb = n_kb;
+                g.p.splits = S;
+                g.p.nrows = rows_map;
+                g.p.bn = bn;
+                g.p.ldo = ldos[kind];
+                g.p.stages = stages;
+                g.p.split_stride = static_cast<long long>(h->R) * ldos[kind];
+                g.p.out = h->part;
+                g.p.err = &h->st->err;
+                tc_gemm_finalize(g);
+            }
+        }
+    }
+    // lm_head over the used rows (one split: the vocabulary gives enough tiles)
+    {
+        TcGemm &g = h->plan_lm;
+        std::memset(&g.p, 0, sizeof(g.p));
+        const int bn = h->bn_u;
+        if (make_tmap_bf16(&g.p.a[0], h->lm_head, h->d, h->V, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM) ||
+            make_tmap_bf16(&g.p.b, h->xu, h->d, h->U, static_cast<uint64_t>(h->d) * 2, kBlockK, bn))
+            return fail(LA_ERR_INVALID_ARG, "tensor map for lm_head failed");
+        g.p.nseg = 1;
+        g.p.seg_tile0[0] = 0;
+        g.p.seg_tile0[1] = (h->V + kTileM - 1) / kTileM;
+        g.p.seg_out[0] = h->V;
+        g.p.seg_col0[0] = 0;
+        g.p.n_kb = (h->d + kBlockK - 1) / kBlockK;
+        g.p.splits = 1;
+        g.p.nrows = h->U;
+        g.p.bn = bn;
+        g.p.ldo = h->V;
+        g.p.stages = tc_gemm_stages_for(bn);
+        g.p.split_stride = 0;
+        g.p.out = h->logits;
+        g.p.err = &h->st->err;
+        tc_gemm_finalize(g);
+    }
+    h->part_elems = part_max;
+    return LA_OK;
+}
+
+}  // namespace
+
+// ======================================================================== C ABI
+extern "C" {
+
+const char *la_strerror(int code) {
+    switch (code) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument";
+        case LA_ERR_OOM: return "out of memory";
+        case LA_ERR_CAPACITY: return "capacity exceeded";
+        case LA_ERR_CUDA: return "CUDA error";
+        case LA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case LA_ERR_STATE: return "call out of order";
+        case LA_ERR_UNSUPPORTED: return "unsupported configuration";
+        default: return "unknown error";
+    }
+}
+
+const char *la_last_error(void) { return g_last_error.c_str(); }
+
+int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opts, la_handle **out) {
+    if (!dims || !w || !opts || !out) return fail(LA_ERR_INVALID_ARG, "null argument");
+    *out = nullptr;
+    const la_model_dims &D = *dims;
+    if (D.n_layers < 1 || D.d_model < 64 || D.n_heads < 1 || D.n_kv_heads < 1 || D.n_heads % D.n_kv_heads ||
+        D.ffn < 1 || D.vocab < 2 || !(D.rms_eps > 0.f) || !(D.rope_base > 1.f))
+        return fail(LA_ERR_INVALID_ARG, "bad model dims");
+    if (D.head_dim != 64 && D.head_dim != 128) return fail(LA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+    if (D.dtype != LA_F32 && D.dtype != LA_BF16) return fail(LA_ERR_INVALID_ARG, "dtype");
+    if (D.d_model % 8 || D.ffn % 8 || (D.n_heads * D.head_dim) % 8)
+        return fail(LA_ERR_UNSUPPORTED, "d_model, ffn and n_heads*head_dim must be multiples of 8");
+    const la_opts &O = *opts;
+    if (O.N < 2 || O.N > 8 || O.W < 1 || O.G < 0 || O.G > 32 || O.pool_cap < 0 || O.pool_cap > 32 ||
+        !(O.temperature >= 0.f))
+        return fail(LA_ERR_INVALID_ARG, "bad options (N 2..8, W >= 1, G 0..32, pool_cap 0..32, temperature >= 0)");
+    const int M = 1 + (O.W + O.G) * (O.N - 1);
+    if (M > 256) return fail(LA_ERR_UNSUPPORTED, "1 + (W+G)(N-1) must be <= 256");
+    if (O.max_seq < O.N + M + 2) return fail(LA_ERR_INVALID_ARG, "max_seq too small");
+    if (!w->embed || !w->final_norm || !w->lm_head || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
+        !w->ffn_norm || !w->w_gate || !w->w_up || !w->w_down)
+        return fail(LA_ERR_INVALID_ARG, "null weight pointer");
+
+    la_handle *h = new la_handle();
+    h->dims = D;
+    h->opts = O;
+    h->stream = static_cast<cudaStream_t>(O.cuda_stream);
+    h->bf16 = D.dtype == LA_BF16;
+    h->act = h->bf16 ? 2 : 4;
+    h->L = D.n_layers;
+    h->d = D.d_model;
+    h->nh = D.n_heads;
+    h->nkv = D.n_kv_heads;
+    h->hd = D.head_dim;
+    h->F = D.ffn;
+    h->V = D.vocab;
+    h->qd = h->nh * h->hd;
+    h->kvd = h->nkv * h->hd;
+    h->qkv_out = h->qd + 2 * h->kvd;
+    h->N = O.N;
+    h->W = O.W;
+    h->G = O.G;
+    h->M = M;
+    h->U = 1 + O.W + O.G * (O.N - 1);
+    h->cap = O.pool_cap > 0 ? O.pool_cap : std::max(O.G, 1);
+    h->max_seq = O.max_seq;
+    h->R = round_up(std::max(M, kPrefillRows), 16);
+    h->bn_step = round_up(M, 16);
+    h->bn_pf = kPrefillRows;
+    h->bn_u = round_up(h->U, 16);
+    h->embed = w->embed;
+    h->final_norm = w->final_norm;
+    h->lm_head = w->lm_head;
+    auto grab = [&](std::vector<const void *> &v, const void *const *src) {
+        v.assign(src, src + h->L);
+        for (const void *p : v)
+            if (!p || (reinterpret_cast<uintptr_t>(p) & 15)) return false;
+        return true;
+    };
+    if (!grab(h->attn_norm, w->attn_norm) || !grab(h->wq, w->wq) || !grab(h->wk, w->wk) || !grab(h->wv, w->wv) ||
+        !grab(h->wo, w->wo) || !grab(h->ffn_norm, w->ffn_norm) || !grab(h->wg, w->w_gate) || !grab(h->wu, w->w_up) ||
+        !grab(h->wd, w->w_down)) {
+        delete h;
+        return fail(LA_ERR_INVALID_ARG, "null or misaligned per-layer weight pointer");
+    }
+    for (const void *p : {w->embed, w->final_norm, w->lm_head})
+        if (reinterpret_cast<uintptr_t>(p) & 15) {
+            delete h;
+            return fail(LA_ERR_INVALID_ARG, "weights must be 16-byte aligned");
+        }
+
+    int rc = LA_OK;
+    auto A = [&](int r) {
+        if (rc == LA_OK) rc = r;
+    };
+    const size_t act = h->act;
+    const int R = h->R;
+    A(h->alloc(&h->h, static_cast<size_t>(R) * h->d));
+    A(h->alloc_bytes(&h->xn, static_cast<size_t>(R) * h->d * act));
+    A(h->alloc_bytes(&h->ao, static_cast<size_t>(R) * h->qd * act));
+    A(h->alloc_bytes(&h->fa, static_cast<size_t>(R) * h->F * act));
+    A(h->alloc_bytes(&h->xu, static_cast<size_t>(std::max(h->U, 16)) * h->d * act));
+    A(h->alloc(&h->q, static_cast<size_t>(R) * h->qd));
+    A(h->alloc(&h->logits, static_cast<size_t>(std::max(h->U, 1)) * h->V));
+    A(h->alloc(&h->amax, std::max(h->U, 1)));
+    A(h->alloc(&h->lmax, std::max(h->U, 1)));
+    A(h->alloc(&h->lsum, std::max(h->U, 1)));
+    const int nch_max = (h->max_seq + kAttnChunk - 1) / kAttnChunk;
+    A(h->alloc(&h->attn_ws, static_cast<size_t>(nch_max) * R * h->nh * (h->hd + 4)));
+    A(h->alloc_bytes(&h->cache, static_cast<size_t>(h->L) * 2 * h->nkv * h->max_seq * h->hd * act));
+    A(h->alloc(&h->rope, static_cast<size_t>(h->max_seq) * (h->hd / 2)));
+    A(h->alloc(&h->tok, M));
+    A(h->alloc(&h->depth, M));
+    h->anc_stride = h->N + h->W;
+    A(h->alloc(&h->anc, static_cast<size_t>(M) * h->anc_stride));
+    A(h->alloc(&h->anc_cnt, M));
+    A(h->alloc(&h->used, h->U));
+    A(h->alloc(&h->iota, R));
+    A(h->alloc(&h->st, 1));
+    A(h->alloc(&h->tokens_log, h->max_seq));
+    A(h->alloc(&h->window, static_cast<size_t>(h->N - 1) * h->W));
+    A(h->alloc(&h->cands, std::max(h->G * (h->N - 1), 1)));
+    int log2n = 10;
+    while ((1 << log2n) < 2 * h->V) ++log2n;
+    h->nslots_log2 = log2n;
+    const size_t nslots = static_cast<size_t>(1) << log2n;
+    A(h->alloc(&h->pkeys, nslots));
+    A(h->alloc(&h->pcnt, nslots));
+    A(h->alloc(&h->phead, nslots));
+    A(h->alloc(&h->pent, nslots * h->cap * (h->N - 1)));
+    if (rc == LA_OK && cudaMallocHost(&h->st_host, sizeof(SpecState)) != cudaSuccess)
+        rc = fail(LA_ERR_OOM, "pinned host allocation failed");
+    if (rc != LA_OK) {
+        delete h;
+        return rc;
+    }
+    cudaStream_t s = h->stream;
+    // Static tables: rotary angles, step-row depths and in-step key lists.
+    {
+        std::vector<float2> rope(static_cast<size_t>(h->max_seq) * (h->hd / 2));
+        for (int p = 0; p < h->max_seq; ++p)
+            for (int i = 0; i < h->hd / 2; ++i) {
+                const double th = std::pow(static_cast<double>(D.rope_base), -2.0 * i / h->hd);
+                const double a = p * th;
+                rope[static_cast<size_t>(p) * (h->hd / 2) + i] =
+                    make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+            }
+        std::vector<int> parent, depth;
+        step_structure(h->N, h->W, h->G, parent, depth);
+        std::vector<int> anc(static_cast<size_t>(M) * h->anc_stride, 0), cnt(M, 0);
+        for (int r = 0; r < M; ++r) {
+            std::vector<int> chain;
+            for (int x = r; x >= 0; x = parent[x]) chain.push_back(x);
+            std::reverse(chain.begin(), chain.end());
+            cnt[r] = static_cast<int>(chain.size());
+            for (size_t i = 0; i < chain.size(); ++i) anc[static_cast<size_t>(r) * h->anc_stride + i] = chain[i];
+        }
+        std::vector<int> used;
+        used.push_back(0);
+        for (int j = 0; j < h->W; ++j) used.push_back(1 + (h->N - 2) * h->W + j);
+        for (int c = 0; c < h->G; ++c)
+            for (int m = 1; m < h->N; ++m) used.push_back(1 + (h->N - 1) * h->W + c * (h->N - 1) + (m - 1));
+        std::vector<int> iota(R);
+        for (int i = 0; i < R; ++i) iota[i] = i;
+        if (cudaMemcpy(h->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(h->depth, depth.data(), M * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(h->anc, anc.data(), anc.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(h->anc_cnt, cnt.data(), M * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(h->used, used.data(), used.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(h->iota, iota.data(), R * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+            delete h;
+            return fail(LA_ERR_CUDA, "uploading static tables failed");
+        }
+    }
+    // Zero activations once so padded rows never hold NaN bit patterns.
+    if (cudaMemsetAsync(h->xn, 0, static_cast<size_t>(R) * h->d * act, s) != cudaSuccess ||
+        cudaMemsetAsync(h->ao, 0, static_cast<size_t>(R) * h->qd * act, s) != cudaSuccess ||
+        cudaMemsetAsync(h->fa, 0, static_cast<size_t>(R) * h->F * act, s) != cudaSuccess ||
+        cudaMemsetAsync(h->xu, 0, static_cast<size_t>(std::max(h->U, 16)) * h->d * act, s) != cudaSuccess ||
+        cudaMemsetAsync(h->st, 0, sizeof(SpecState), s) != cudaSuccess) {
+        delete h;
+        return fail(LA_ERR_CUDA, "memset failed");
+    }
+    if (h->bf16) {
+        rc = build_plans(h);
+    } else {
+        h->part_elems = static_cast<size_t>(R) * std::max(h->qkv_out, std::max(2 * h->F, h->d));
+    }
+    if (rc == LA_OK) rc = h->alloc(&h->part, h->part_elems);
+    if (rc == LA_OK && h->bf16) {
+        for (int m = 0; m < 2; ++m)
+            for (int k = 0; k < 4; ++k)
+                for (auto &g : h->plan[m][k]) g.p.out = h->part;
+    }
+    if (rc == LA_OK) rc = reset_pool(h);
+    if (rc == LA_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = fail(LA_ERR_CUDA, "create sync failed");
+    if (rc != LA_OK) {
+        delete h;
+        return rc;
+    }
+    *out = h;
+    return LA_OK;
+}
+
+void la_destroy(la_handle *h) {
+    if (!h) return;
+    if (h->stream) cudaStreamSynchronize(h->stream);
+    else cudaDeviceSynchronize();
+    delete h;
+}
+
+int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token) {
+    if (!h || !prompt || !first_token) return fail(LA_ERR_INVALID_ARG, "null argument");
+    if (n < h->N) return fail(LA_ERR_INVALID_ARG, "prompt shorter than N");
+    if (n + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "prompt too long for max_seq");
+    for (int i = 0; i < n; ++i)
+        if (prompt[i] < 0 || prompt[i] >= h->V) return fail(LA_ERR_INVALID_ARG, "token id out of range at %d", i);
+    cudaStream_t s = h->stream;
+    h->prefilled = false;
+    CK(cudaMemsetAsync(h->st, 0, sizeof(SpecState), s));
+    int rc = reset_pool(h);
+    if (rc != LA_OK) return rc;
+    CK(cudaMemcpyAsync(h->tokens_log, prompt, static_cast<size_t>(n) * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    if ((rc = run_prefix(h, n, true)) != LA_OK) return rc;
+    CK(first_token_launch(h->spec(), n, s));
+    // Initial window: prompt tokens picked by splitmix64(seed ^ (k*W + j)).
+    std::vector<int> win(static_cast<size_t>(h->N - 1) * h->W);
+    for (int k = 0; k < h->N - 1; ++k)
+        for (int j = 0; j < h->W; ++j)
+            win[static_cast<size_t>(k) * h->W + j] =
+                prompt[splitmix64(h->opts.seed ^ static_cast<uint64_t>(k * h->W + j)) % static_cast<uint64_t>(n)];
+    CK(cudaMemcpyAsync(h->window, win.data(), win.size() * sizeof(int), cudaMemcpyHostToDevice, s));
+    if (h->opts.prompt_as_reference) CK(pool_seed_prompt_launch(h->spec(), n, s));
+    CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if ((rc = check_device_error(h)) != LA_OK) return rc;
+    *first_token = h->st_host->o;
+    h->P = n;
+    h->prefilled = true;
+    h->steps = 0;
+    h->generated = 1;
+    h->last_A = 0;
+    h->last_g = 0;
+    h->logits_rows = 1;
+    return LA_OK;
+}
+
+int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
+    if (!h || !out_tokens || !out_n) return fail(LA_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled) return fail(LA_ERR_STATE, "la_step before la_prefill");
+    if (h->P + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "max_seq reached");
+    cudaStream_t s = h->stream;
+    CK(build_rows_launch(h->spec(), s));
+    int rc = forward_any(h, STEP, h->tok, h->M, h->P, true);
+    if (rc != LA_OK) return rc;
+    if ((rc = run_lm_head(h, h->U)) != LA_OK) return rc;
+    CK(argmax_launch(h->logits, h->U, h->V, h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
+                     h->lmax, h->lsum, s));
+    CK(finish_step_launch(h->spec(), s));
+    if ((rc = kv_commit(h)) != LA_OK) return rc;
+    CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if ((rc = check_device_error(h)) != LA_OK) return rc;
+    const SpecState &st = *h->st_host;
+    if (st.A < 1 || st.A > h->N) {
+        h->prefilled = false;
+        return fail(LA_ERR_STATE, "device reported A=%d", st.A);
+    }
+    for (int i = 0; i < st.A; ++i) out_tokens[i] = st.acc[i];
+    *out_n = st.A;
+    h->P = st.P;
+    h->steps += 1;
+    h->generated += st.A;
+    h->last_A = st.A;
+    h->last_g = st.g;
+    h->logits_rows = h->U;
+    return LA_OK;
+}
+
+int la_generate(la_handle *h, const int32_t *prompt, int32_t n, int32_t max_new, int32_t *out, int32_t *out_n,
+                int32_t *n_steps) {
+    if (!h || !prompt || !out || max_new < 1) return fail(LA_ERR_INVALID_ARG, "bad argument");
+    int32_t first = 0;
+    int rc = la_prefill(h, prompt, n, &first);
+    if (rc != LA_OK) return rc;
+    int cnt = 0, steps = 0;
+    out[cnt++] = first;
+    int32_t buf[8];
+    while (cnt < max_new) {
+        int32_t a = 0;
+        if ((rc = la_step(h, buf, &a)) != LA_OK) return rc;
+        ++steps;
+        for (int i = 0; i < a && cnt < max_new; ++i) out[cnt++] = buf[i];
+    }
+    if (out_n) *out_n = cnt;
+    if (n_steps) *n_steps = steps;
+    return LA_OK;
+}
+
+int la_stats(const la_handle *h, la_stats_t *o) {
+    if (!h || !o) return fail(LA_ERR_INVALID_ARG, "null argument");
+    o->steps = h->steps;
+    o->generated = h->generated;
+    o->last_accept = h->last_A;
+    o->last_candidates = h->last_g;
+    o->prefix_len = h->P;
+    o->rows = h->M;
+    return LA_OK;
+}
+
+int la_export_state(la_handle *h, la_state_t *stt) {
+    if (!h || !stt || !stt->tokens || !stt->window || (!stt->records && stt->records_cap > 0))
+        return fail(LA_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled) return fail(LA_ERR_STATE, "no state before la_prefill");
+    cudaStream_t s = h->stream;
+    const int n = h->P + 1;
+    const size_t nslots = static_cast<size_t>(1) << h->nslots_log2;
+    const int L = h->N - 1;
+    std::vector<int> keys(nslots), cnt(nslots), head(nslots), ent(nslots * h->cap * L);
+    std::vector<int> toks(n);
+    CK(cudaMemcpyAsync(toks.data(), h->tokens_log, n * sizeof(int), cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(stt->window, h->window, static_cast<size_t>(L) * h->W * sizeof(int), cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(keys.data(), h->pkeys, nslots * sizeof(int), cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(cnt.data(), h->pcnt, nslots * sizeof(int), cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(head.data(), h->phead, nslots * sizeof(int), cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(ent.data(), h->pent, ent.size() * sizeof(int), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    std::map<int, size_t> order;
+    for (size_t i = 0; i < nslots; ++i)
+        if (keys[i] >= 0) order[keys[i]] = i;
+    int nrec = 0;
+    for (auto &kv : order) nrec += cnt[kv.second];
+    stt->n_tokens = n;
+    stt->n_records = nrec;
+    if (n > stt->tokens_cap || nrec > stt->records_cap)
+        return fail(LA_ERR_CAPACITY, "state buffers too small (tokens %d, records %d)", n, nrec);
+    std::memcpy(stt->tokens, toks.data(), n * sizeof(int));
+    int r = 0;
+    for (auto &kv : order) {
+        const size_t sl = kv.second;
+        for (int e = 0; e < cnt[sl]; ++e) {
+            int *rec = stt->records + static_cast<size_t>(r) * h->N;
+            rec[0] = kv.first;
+            const int *src = ent.data() + (sl * h->cap + (head[sl] + e) % h->cap) * L;
+            for (int m = 0; m < L; ++m) rec[1 + m] = src[m];
+            ++r;
+        }
+    }
+    return LA_OK;
+}
+
+int la_import_state(la_handle *h, const la_state_t *stt) {
+    if (!h || !stt || !stt->tokens || !stt->window || (stt->n_records > 0 && !stt->records))
+        return fail(LA_ERR_INVALID_ARG, "null argument");
+    const int n = stt->n_tokens;
+    if (n < 2) return fail(LA_ERR_INVALID_ARG, "state needs at least two tokens");
+    if (n - 1 + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "state too long for max_seq");
+    for (int i = 0; i < n; ++i)
+        if (stt->tokens[i] < 0 || stt->tokens[i] >= h->V) return fail(LA_ERR_INVALID_ARG, "token out of range");
+    const int L = h->N - 1;
+    for (int i = 0; i < L * h->W; ++i)
+        if (stt->window[i] < 0 || stt->window[i] >= h->V) return fail(LA_ERR_INVALID_ARG, "window token out of range");
+    for (int i = 0; i < stt->n_records * h->N; ++i)
+        if (stt->records[i] < 0 || stt->records[i] >= h->V) return fail(LA_ERR_INVALID_ARG, "pool token out of range");
+    cudaStream_t s = h->stream;
+    h->prefilled = false;
+    CK(cudaMemsetAsync(h->st, 0, sizeof(SpecState), s));
+    int rc = reset_pool(h);
+    if (rc != LA_OK) return rc;
+    CK(cudaMemcpyAsync(h->tokens_log, stt->tokens, static_cast<size_t>(n) * sizeof(int), cudaMemcpyHostToDevice, s));
+    if ((rc = run_prefix(h, n - 1, false)) != LA_OK) return rc;
+    SpecState init{};
+    init.P = n - 1;
+    init.o = stt->tokens[n - 1];
+    init.n_tokens = n;
+    init.cstar = -1;
+    *h->st_host = init;
+    CK(cudaMemcpyAsync(h->st, h->st_host, sizeof(SpecState), cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(h->window, stt->window, static_cast<size_t>(L) * h->W * sizeof(int), cudaMemcpyHostToDevice, s));
+    if (stt->n_records > 0) {
+        const size_t need = static_cast<size_t>(stt->n_records) * h->N;
+        if (need > h->records_dev_cap) {
+            int *p = nullptr;
+            if ((rc = h->alloc(&p, need)) != LA_OK) return rc;
+            h->records_dev = p;
+            h->records_dev_cap = need;
+        }
+        CK(cudaMemcpyAsync(h->records_dev, stt->records, need * sizeof(int), cudaMemcpyHostToDevice, s));
+        CK(pool_insert_launch(h->spec(), h->records_dev, stt->n_records, s));
+    }
+    CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if ((rc = check_device_error(h)) != LA_OK) return rc;
+    h->P = n - 1;
+    h->prefilled = true;
+    h->logits_rows = 0;
+    return LA_OK;
+}
+
+int la_debug_logits(la_handle *h, float *host, int32_t *rows, int32_t *vocab) {
+    if (!h || !rows || !vocab) return fail(LA_ERR_INVALID_ARG, "null argument");
+    *rows = h->logits_rows;
+    *vocab = h->V;
+    if (host && h->logits_rows > 0) {
+        CK(cudaMemcpyAsync(host, h->logits, static_cast<size_t>(h->logits_rows) * h->V * sizeof(float),
+                           cudaMemcpyDeviceToHost, h->stream));
+        CK(cudaStreamSynchronize(h->stream));
+    }
+    return LA_OK;
+}
+
+int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k, int32_t splits,
+                 float *workspace, void *stream) {
+    if (!x || !w || !y || rows < 1 || rows > 256 || out < 1 || k < 8 || k % 8 || splits < 1)
+        return fail(LA_ERR_INVALID_ARG, "bad GEMM arguments");
+    const int n_kb = (k + kBlockK - 1) / kBlockK;
+    if (splits > n_kb) return fail(LA_ERR_INVALID_ARG, "splits > k / 64");
+    if (splits > 1 && !workspace) return fail(LA_ERR_INVALID_ARG, "workspace required when splits > 1");
+    static unsigned *err = nullptr;
+    if (!err) CK(cudaMalloc(&err, sizeof(unsigned)));
+    TcGemm g;
+    std::memset(&g.p, 0, sizeof(g.p));
+    const int bn = round_up(rows, 16);
+    if (make_tmap_bf16(&g.p.a[0], w, k, out, static_cast<uint64_t>(k) * 2, kBlockK, kTileM) ||
+        make_tmap_bf16(&g.p.b, x, k, rows, static_cast<uint64_t>(k) * 2, kBlockK, bn))
+        return fail(LA_ERR_INVALID_ARG, "tensor map creation failed (16-byte alignment?)");
+    g.p.nseg = 1;
+    g.p.seg_tile0[0] = 0;
+    g.p.seg_tile0[1] = (out + kTileM - 1) / kTileM;
+    g.p.seg_out[0] = out;
+    g.p.seg_col0[0] = 0;
+    g.p.n_kb = n_kb;
+    g.p.splits = splits;
+    g.p.nrows = rows;
+    g.p.bn = bn;
+    g.p.ldo = out;
+    g.p.stages = tc_gemm_stages_for(bn);
+    g.p.split_stride = static_cast<long long>(rows) * out;
+    g.p.out = splits > 1 ? workspace : y;
+    g.p.err = err;
+    tc_gemm_finalize(g);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    CK(tc_gemm_launch(g, s));
+    if (splits > 1) CK(reduce_splits_launch(workspace, splits, g.p.split_stride, rows, out, y, s));
+    return LA_OK;
+}
+
+}  // extern "C"

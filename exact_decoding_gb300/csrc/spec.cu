@@ -1,0 +1,446 @@
+// Speculation state of lookahead decoding on the device: candidate lookup
+// and step-row build, verification (Algorithm 3 greedy / Algorithm 4
+// sampling), n-gram harvest into the pool, window slide, bookkeeping and the
+// KV commit of accepted rows.  Source: paper-graph-ui page, section 3.4,
+// "The Lookahead Branch", "The Verification Branch", "Integrated Forward
+// Pass".
+//
+// Step-row layout: row 0 is the last committed token o (position P);
+// lookahead row (k, j) is 1 + k*W + j (window level k, column j, position
+// P+1+j+k); candidate row (c, m), m = 1..N-1, is 1 + (N-1)*W + c*(N-1) + m-1
+// (suffix token m of candidate c, position P+m).  "Used" rows (the ones
+// whose logits are computed) are row 0, the top level's W rows and all
+// candidate rows, in that order.
+//
+// n-gram pool: open-addressed hash table keyed by the n-gram's first token
+// (Fibonacci hashing, linear probing, >= 2x as many slots as the vocabulary
+// so it never fills).  Each slot keeps a FIFO ring of up to `cap` distinct
+// (N-1)-token suffixes, oldest first; inserting a suffix that is present
+// does nothing, inserting into a full ring drops the oldest.  All pool
+// operations run in one warp: lanes probe 32 slots, or compare 32 ring
+// entries, at once; inserts keep their sequential order.
+#include <climits>
+
+#include "la_kernels.h"
+
+namespace la {
+
+constexpr unsigned FULL = 0xffffffffu;
+
+// ------------------------------------------------------------------ Philox4x32-10
+// Counter-based generator of Salmon, Moraes, Dror and Shaw (SC'11): ten
+// rounds of two 32x32->64 multiplies, key bumped by the Weyl constants.
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+        const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+        const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = lo1;
+        c[2] = n2;
+        c[3] = lo0;
+    }
+}
+// Sampling draw for (position, draw index): 24 high bits of the first word.
+__device__ __forceinline__ float draw_uniform(unsigned long long seed, int position, int draw) {
+    uint32_t c[4] = {static_cast<uint32_t>(position), static_cast<uint32_t>(draw), 0u, 0u};
+    philox4x32_10(c, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+    return static_cast<float>(c[0] >> 8) * (1.0f / 16777216.0f);
+}
+
+// ------------------------------------------------------------------ pool (one warp)
+__device__ __forceinline__ int hash_slot(int key, int log2n) {
+    return static_cast<int>((static_cast<uint32_t>(key) * 2654435761u) >> (32 - log2n));
+}
+
+// Slot holding `key` (>= 0), or -(first empty slot + 1) if absent, INT_MIN if full.
+__device__ int pool_find(const SpecDev &d, int key, int lane) {
+    const int n = 1 << d.nslots_log2, mask = n - 1;
+    const int base = hash_slot(key, d.nslots_log2);
+    for (int probe = 0; probe < n; probe += 32) {
+        const int s = (base + probe + lane) & mask;
+        const int k = d.pkeys[s];
+        const unsigned hit = __ballot_sync(FULL, k == key);
+        const unsigned emp = __ballot_sync(FULL, k == -1);
+        const unsigned any = hit | emp;
+        if (any) {
+            const int i = __ffs(any) - 1;
+            const int slot = (base + probe + i) & mask;
+            return ((hit >> i) & 1u) ? slot : -(slot + 1);
+        }
+    }
+    return INT_MIN;
+}
+
+// suf: N-1 tokens, identical in every lane.
+__device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int lane) {
+    const int L = d.N - 1, cap = d.cap;
+    const int f = pool_find(d, key, lane);
+    if (f == INT_MIN) {
+        if (lane == 0) atomicOr(&d.st->err, ERR_POOL);
+        return;
+    }
+    int slot = f;
+    if (f < 0) {
+        slot = -f - 1;
+        if (lane == 0) {
+            d.pkeys[slot] = key;
+            d.pcnt[slot] = 0;
+            d.phead[slot] = 0;
+        }
+        __syncwarp();
+    }
+    const int cnt = d.pcnt[slot], head = d.phead[slot];
+    bool same = false;
+    if (lane < cnt) {
+        const int *e = d.pent + (static_cast<long long>(slot) * cap + (head + lane) % cap) * L;
+        same = true;
+        for (int m = 0; m < L; ++m) same = same && (e[m] == suf[m]);
+    }
+    if (__any_sync(FULL, same)) return;
+    if (lane == 0) {
+        int pos;
+        if (cnt < cap) {
+            pos = (head + cnt) % cap;
+            d.pcnt[slot] = cnt + 1;
+        } else {
+            pos = head;
+            d.phead[slot] = (head + 1) % cap;
+        }
+        int *e = d.pent + (static_cast<long long>(slot) * cap + pos) * L;
+        for (int m = 0; m < L; ++m) e[m] = suf[m];
+    }
+    __syncwarp();
+}
+
+// ------------------------------------------------------------------ candidate lookup + step rows
+__global__ void __launch_bounds__(256) k_build_rows(SpecDev d) {
+    __shared__ int s_g;
+    __shared__ int s_c[32 * 8];
+    const int L = d.N - 1;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int o = d.st->o;
+    if (tid < 32) {
+        int g = 0;
+        if (d.G > 0) {
+            const int f = pool_find(d, o, lane);
+            if (f >= 0) {
+                const int cnt = d.pcnt[f], head = d.phead[f];
+                g = min(cnt, d.G);
+                for (int t = lane; t < g * L; t += 32) {
+                    const int c = t / L, m = t % L;
+                    s_c[t] = d.pent[(static_cast<long long>(f) * d.cap + (head + c) % d.cap) * L + m];
+                }
+            }
+        }
+        if (lane == 0) s_g = g;
+    }
+    __syncthreads();
+    const int g = s_g;
+    const int look_end = 1 + L * d.W;
+    for (int r = tid; r < d.M; r += blockDim.x) {
+        int t;
+        if (r == 0) {
+            t = o;
+        } else if (r < look_end) {
+            t = d.window[r - 1];   // level-major: (k, j) -> k*W + j = r - 1
+        } else {
+            const int idx = r - look_end, c = idx / L;
+            t = c < g ? s_c[idx] : 0;
+        }
+        d.tok[r] = t;
+    }
+    for (int t = tid; t < d.G * L; t += blockDim.x) d.cands[t] = (t / L) < g ? s_c[t] : -1;
+    if (tid == 0) d.st->g = g;
+}
+
+// ------------------------------------------------------------------ inverse CDF (one block)
+// Smallest id whose ascending cumulative weight exceeds u * total, with
+// weight exp((l_v - mx) * invT) and the ids in rej[0..nrej) removed.
+template <int NT>
+__device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, const int *rej, int nrej, float u) {
+    __shared__ float s_part[NT];
+    __shared__ float s_warp[NT / 32];
+    __shared__ int s_ans;
+    const int tid = threadIdx.x;
+    const int per = (V + NT - 1) / NT;
+    const int a = min(V, tid * per), b = min(V, a + per);
+    float part = 0.f;
+    for (int v = a; v < b; ++v) {
+        bool r = false;
+        for (int i = 0; i < nrej; ++i) r = r || (rej[i] == v);
+        part += r ? 0.f : expf((l[v] - mx) * invT);
+    }
+    // inclusive warp scan, then across warps (fixed order)
+    float incl = part;
+    const int lane = tid & 31, w = tid >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_warp[w] = incl;
+    if (tid == 0) s_ans = -1;
+    __syncthreads();
+    if (w == 0) {
+        float x = lane < NT / 32 ? s_warp[lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(FULL, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane < NT / 32) s_warp[lane] = x;
+    }
+    __syncthreads();
+    const float excl = (w > 0 ? s_warp[w - 1] : 0.f) + (incl - part);
+    const float total = s_warp[NT / 32 - 1];
+    const float t = u * total;
+    s_part[tid] = part;
+    if (part > 0.f && excl <= t && t < excl + part) {
+        float s = 0.f;
+        int ans = b - 1;
+        for (int v = a; v < b; ++v) {
+            bool r = false;
+            for (int i = 0; i < nrej; ++i) r = r || (rej[i] == v);
+            s += r ? 0.f : expf((l[v] - mx) * invT);
+            if (excl + s > t) {
+                ans = v;
+                break;
+            }
+        }
+        s_ans = ans;
+    }
+    __syncthreads();
+    if (tid == 0 && s_ans < 0) {
+        // t rounded up to the total: take the last id with weight
+        for (int i = NT - 1; i >= 0; --i)
+            if (s_part[i] > 0.f) {
+                const int aa = min(V, i * per), bb = min(V, aa + per);
+                for (int v = bb - 1; v >= aa; --v) {
+                    bool r = false;
+                    for (int k = 0; k < nrej; ++k) r = r || (rej[k] == v);
+                    if (!r && expf((l[v] - mx) * invT) > 0.f) {
+                        s_ans = v;
+                        break;
+                    }
+                }
+                break;
+            }
+    }
+    __syncthreads();
+    return s_ans;
+}
+
+// ------------------------------------------------------------------ verify + harvest + slide
+constexpr int kFinishThreads = 1024;
+
+__global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
+    __shared__ int s_acc[8];
+    __shared__ int s_A, s_win, s_need_draw, s_dist_u, s_nrej, s_pos;
+    __shared__ int s_rej[32];
+    __shared__ float s_u;
+    const int L = d.N - 1;
+    const int tid = threadIdx.x;
+    const int P = d.st->P;
+    const int g = d.st->g;
+    const int cand_u0 = 1 + d.W;   // used index of candidate 0, depth 1
+    if (tid == 0) {
+        int A = 0, win = -1;
+        unsigned surv = g >= 32 ? FULL : ((1u << g) - 1u);
+        if (d.T <= 0.f) {
+            // Algorithm 3: progressive filter against the argmax chain.
+            int tau = d.amax[0];
+            for (int depth = 1;; ++depth) {
+                unsigned nxt = 0;
+                for (int c = 0; c < g; ++c)
+                    if (((surv >> c) & 1u) && d.cands[c * L + depth - 1] == tau) nxt |= 1u << c;
+                s_acc[A++] = tau;
+                if (!nxt) break;
+                surv = nxt;
+                const int c0 = __ffs(surv) - 1;
+                const int nt = d.amax[cand_u0 + c0 * L + depth - 1];
+                if (depth == L) {
+                    s_acc[A++] = nt;
+                    break;
+                }
+                tau = nt;
+            }
+            if (A > 1) win = __ffs(surv) - 1;
+            s_need_draw = 0;
+        } else {
+            // Algorithm 4 with greedy drafts: accept x with probability
+            // dist(x); on rejection remove x from dist; draw from dist at the end.
+            const float invT = 1.f / d.T;
+            int dist_u = 0, depth = 1;
+            for (;;) {
+                const int pos = P + depth;
+                int nd = 0, accepted = -1, nrej = 0;
+                float rej_mass = 0.f;
+                const float *lr = d.logits + static_cast<long long>(dist_u) * d.V;
+                const float mx = d.lmax[dist_u], Z = d.lsum[dist_u];
+                if (depth <= L && surv) {
+                    for (int c = 0; c < g; ++c) {
+                        if (!((surv >> c) & 1u)) continue;
+                        const int x = d.cands[c * L + depth - 1];
+                        bool seen = false;
+                        for (int i = 0; i < nrej; ++i) seen = seen || (s_rej[i] == x);
+                        if (seen) continue;
+                        const float r = draw_uniform(d.seed, pos, nd++);
+                        const float ex = expf((lr[x] - mx) * invT);
+                        const float px = ex / (Z - rej_mass);
+                        if (r <= px) {
+                            accepted = x;
+                            break;
+                        }
+                        s_rej[nrej++] = x;
+                        rej_mass += ex;
+                    }
+                }
+                if (accepted >= 0) {
+                    s_acc[A++] = accepted;
+                    unsigned nxt = 0;
+                    for (int c = 0; c < g; ++c)
+                        if (((surv >> c) & 1u) && d.cands[c * L + depth - 1] == accepted) nxt |= 1u << c;
+                    surv = nxt;
+                    dist_u = cand_u0 + (__ffs(surv) - 1) * L + depth - 1;
+                    ++depth;
+                    continue;
+                }
+                s_dist_u = dist_u;
+                s_nrej = nrej;
+                s_u = draw_uniform(d.seed, pos, nd);
+                s_pos = pos;
+                break;
+            }
+            if (A > 0) win = __ffs(surv) - 1;
+            s_need_draw = 1;
+        }
+        s_A = A;
+        s_win = win;
+    }
+    __syncthreads();
+    if (s_need_draw) {
+        const int u = s_dist_u;
+        const int x = block_inverse_cdf<kFinishThreads>(d.logits + static_cast<long long>(u) * d.V, d.V, d.lmax[u],
+                                                        1.f / d.T, s_rej, s_nrej, s_u);
+        if (tid == 0) {
+            s_acc[s_A] = x;
+            s_A = s_A + 1;
+        }
+        __syncthreads();
+    }
+    // Harvest the window's n-grams (column order), then slide it.
+    if (tid < 32) {
+        int suf[8];
+        for (int j = 0; j < d.W; ++j) {
+            for (int k = 1; k < L; ++k) suf[k - 1] = d.window[k * d.W + j];
+            suf[L - 1] = d.amax[1 + j];
+            pool_insert_warp(d, d.window[j], suf, tid);
+        }
+    }
+    __syncthreads();
+    for (int j = tid; j < d.W; j += blockDim.x) {
+        for (int k = 0; k + 1 < L; ++k) d.window[k * d.W + j] = d.window[(k + 1) * d.W + j];
+        d.window[(L - 1) * d.W + j] = d.amax[1 + j];
+    }
+    if (tid == 0) {
+        const int A = s_A;
+        SpecState *st = d.st;
+        st->P_old = P;
+        st->A = A;
+        st->cstar = s_win;
+        for (int i = 0; i < A; ++i) {
+            st->acc[i] = s_acc[i];
+            d.tokens_log[P + 1 + i] = s_acc[i];
+        }
+        st->P = P + A;
+        st->o = s_acc[A - 1];
+        st->n_tokens = P + A + 1;
+    }
+}
+
+// Copy K/V of the winning candidate's rows m = 1..A-1 (slot P_old + its row)
+// to slots P_old + m.  Row 0 already sits at P_old.
+template <typename T>
+__global__ void k_kv_commit(SpecDev d, T *cache, int nkv, int hd) {
+    const int A = d.st->A, cs = d.st->cstar, P0 = d.st->P_old;
+    if (A <= 1 || cs < 0) return;
+    const int L = d.N - 1;
+    const long long plane = static_cast<long long>(blockIdx.x);   // (layer, k|v, kv head)
+    T *base = cache + plane * d.max_seq * hd;
+    for (int t = threadIdx.x; t < (A - 1) * hd; t += blockDim.x) {
+        const int m = 1 + t / hd, i = t % hd;
+        const int src = P0 + 1 + L * d.W + cs * L + (m - 1);
+        base[static_cast<long long>(P0 + m) * hd + i] = base[static_cast<long long>(src) * hd + i];
+    }
+}
+
+// ------------------------------------------------------------------ pool seeding / import
+__global__ void k_pool_insert(SpecDev d, const int *records, int n) {
+    const int lane = threadIdx.x;
+    const int N = d.N;
+    for (int i = 0; i < n; ++i) pool_insert_warp(d, records[i * N], records + i * N + 1, lane);
+}
+
+__global__ void k_pool_seed_prompt(SpecDev d, int n) {
+    const int lane = threadIdx.x;
+    const int N = d.N;
+    for (int i = 0; i + N <= n; ++i) pool_insert_warp(d, d.tokens_log[i], d.tokens_log + i + 1, lane);
+}
+
+__global__ void __launch_bounds__(kFinishThreads) k_first_token(SpecDev d, int n) {
+    int y;
+    if (d.T <= 0.f) {
+        y = d.amax[0];
+    } else {
+        const float u = draw_uniform(d.seed, n, 0);
+        y = block_inverse_cdf<kFinishThreads>(d.logits, d.V, d.lmax[0], 1.f / d.T, nullptr, 0, u);
+    }
+    if (threadIdx.x == 0) {
+        d.tokens_log[n] = y;
+        d.st->o = y;
+        d.st->P = n;
+        d.st->n_tokens = n + 1;
+        d.st->A = 0;
+        d.st->g = 0;
+        d.st->cstar = -1;
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+cudaError_t build_rows_launch(const SpecDev &d, cudaStream_t s) {
+    k_build_rows<<<1, 256, 0, s>>>(d);
+    return cudaGetLastError();
+}
+cudaError_t finish_step_launch(const SpecDev &d, cudaStream_t s) {
+    k_finish_step<<<1, kFinishThreads, 0, s>>>(d);
+    return cudaGetLastError();
+}
+template <typename T>
+cudaError_t kv_commit_launch(const SpecDev &d, T *cache, int L, int nkv, int hd, cudaStream_t s) {
+    k_kv_commit<T><<<L * 2 * nkv, 128, 0, s>>>(d, cache, nkv, hd);
+    return cudaGetLastError();
+}
+template cudaError_t kv_commit_launch<float>(const SpecDev &, float *, int, int, int, cudaStream_t);
+template cudaError_t kv_commit_launch<__nv_bfloat16>(const SpecDev &, __nv_bfloat16 *, int, int, int, cudaStream_t);
+
+cudaError_t pool_insert_launch(const SpecDev &d, const int *records, int n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    k_pool_insert<<<1, 32, 0, s>>>(d, records, n);
+    return cudaGetLastError();
+}
+cudaError_t pool_seed_prompt_launch(const SpecDev &d, int n, cudaStream_t s) {
+    k_pool_seed_prompt<<<1, 32, 0, s>>>(d, n);
+    return cudaGetLastError();
+}
+cudaError_t first_token_launch(const SpecDev &d, int n, cudaStream_t s) {
+    k_first_token<<<1, kFinishThreads, 0, s>>>(d, n);
+    return cudaGetLastError();
+}
+
+}  // namespace la

@@ -1,0 +1,195 @@
+/*
+ * la.h -- C ABI of the GB300 lookahead-decoding library (libla.so).
+ *
+ * The method: lookahead decoding ("Break the Sequential Dependency of LLM
+ * Inference Using Lookahead Decoding", arXiv 2402.02057; paper-graph-ui
+ * summary, section 3.4).  One step runs a single forward pass of a
+ * LLaMA-style decoder over the cached prefix plus
+ *   - the lookahead branch: a window of W columns x (N-1) past Jacobi levels
+ *     ("The Lookahead Branch"),
+ *   - the verification branch: up to G candidate (N-1)-token suffixes taken
+ *     from the n-gram pool by first token ("The Verification Branch"),
+ * under the lookahead attention mask ("Integrated Forward Pass", Figure 2b),
+ * then verifies the candidates (Algorithm 3 greedy, Algorithm 4 sampling),
+ * accepts the longest matching prefix, harvests the window's new n-grams into
+ * the pool, slides the window and commits the accepted tokens' KV.
+ *
+ * Conventions (all entry points):
+ *   - Return LA_OK (0) or a negative LA_ERR_* code; no exception or abort
+ *     crosses the ABI.  la_strerror() names a code; la_last_error() gives the
+ *     message of the last failure on the calling thread.
+ *   - Device pointers are CUDA device addresses on the current device; host
+ *     pointers are ordinary host memory.  Each argument says which it is.
+ *   - All work runs on the stream given in la_opts.cuda_stream (NULL: the
+ *     legacy default stream).  Calls that return host results synchronise
+ *     that stream before they return.
+ *   - A handle is not thread-safe: one thread at a time per handle.
+ *   - Matrices are row-major [out][in]; a token id is int32 in [0, vocab).
+ */
+#ifndef LA_H
+#define LA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Error codes. */
+#define LA_OK                   0
+#define LA_ERR_INVALID_ARG     -1  /* bad pointer, size, alignment or option */
+#define LA_ERR_OOM             -2  /* device or pinned host allocation failed */
+#define LA_ERR_CAPACITY        -3  /* max_seq (or a caller buffer) too small for the request */
+#define LA_ERR_CUDA            -4  /* a CUDA runtime or driver call failed */
+#define LA_ERR_DEVICE_TIMEOUT  -5  /* a kernel's bounded wait gave up; the step's results are void */
+#define LA_ERR_STATE           -6  /* call out of order (e.g. la_step before la_prefill) */
+#define LA_ERR_UNSUPPORTED     -7  /* valid request this build does not handle (e.g. head_dim 96) */
+
+/* Weight / activation element types. */
+#define LA_F32   0   /* fp32 weights, fp32 activations and KV cache (SIMT GEMMs) */
+#define LA_BF16  1   /* bf16 weights, bf16 GEMM inputs and KV cache, fp32 accumulation
+                        and fp32 residual stream (tcgen05 tensor-core GEMMs) */
+
+/* Model shape of a LLaMA-style decoder (the pages run LLaMA-2 / CodeLlama,
+ * paper-graph-ui page, section 5 "Experimental setup"). */
+typedef struct la_model_dims {
+    int32_t n_layers;
+    int32_t d_model;
+    int32_t n_heads;      /* query heads */
+    int32_t n_kv_heads;   /* key/value heads; n_heads % n_kv_heads == 0 (GQA) */
+    int32_t head_dim;     /* 64 or 128 */
+    int32_t ffn;          /* SwiGLU hidden width */
+    int32_t vocab;
+    float   rms_eps;      /* RMSNorm epsilon */
+    float   rope_base;    /* rotary base; rotate-half pairing (i, i + head_dim/2) */
+    int32_t dtype;        /* LA_F32 or LA_BF16, for every weight tensor */
+} la_model_dims;
+
+/* Device pointers to the weights, owned by the caller, which must keep them
+ * alive and unchanged until la_destroy.  Each is 16-byte aligned.
+ * Per-layer entries are host arrays of n_layers device pointers; the library
+ * copies those arrays at la_create.
+ *   embed      [vocab][d_model]          lm_head  [vocab][d_model]
+ *   final_norm, attn_norm[l], ffn_norm[l]  [d_model]
+ *   wq [n_heads*head_dim][d_model]       wk, wv [n_kv_heads*head_dim][d_model]
+ *   wo [d_model][n_heads*head_dim]
+ *   w_gate, w_up [ffn][d_model]          w_down [d_model][ffn]              */
+typedef struct la_weights {
+    const void *embed;
+    const void *final_norm;
+    const void *lm_head;
+    const void *const *attn_norm;
+    const void *const *wq;
+    const void *const *wk;
+    const void *const *wv;
+    const void *const *wo;
+    const void *const *ffn_norm;
+    const void *const *w_gate;
+    const void *const *w_up;
+    const void *const *w_down;
+} la_weights;
+
+/* Decoding options (section 3.4: W lookahead width, N n-gram size / window
+ * depth N-1, G verification cap; Table 3 prompt-as-reference; Table 2
+ * temperature-1 sampling). */
+typedef struct la_opts {
+    int32_t N;                    /* n-gram length, 2..8 */
+    int32_t W;                    /* window columns, >= 1 */
+    int32_t G;                    /* candidates per step, 0..32 */
+    int32_t max_seq;              /* KV capacity in tokens: prompt + generated + step rows */
+    int32_t prompt_as_reference;  /* 1: seed the pool with the prompt's n-grams after prefill */
+    int32_t pool_cap;             /* suffixes kept per first token (FIFO); 0 -> G (min 1); <= 32 */
+    float   temperature;          /* 0: greedy (Algorithm 3); > 0: sampling (Algorithm 4) */
+    uint64_t seed;                /* window initialisation and sampling draws */
+    void   *cuda_stream;          /* cudaStream_t or NULL */
+} la_opts;
+
+typedef struct la_handle la_handle;
+
+typedef struct la_stats_t {
+    int64_t steps;            /* la_step calls since la_prefill */
+    int64_t generated;        /* tokens produced: the prefill's first token + every accepted token */
+    int32_t last_accept;      /* A of the last step, 1..N */
+    int32_t last_candidates;  /* g of the last step, 0..G */
+    int32_t prefix_len;       /* P: tokens whose KV is committed */
+    int32_t rows;             /* M = 1 + (W + G)(N - 1) rows per step */
+} la_stats_t;
+
+/* Host-side snapshot of the decoding state, for resume and for checking a
+ * step against an independent implementation.  The caller allocates the
+ * arrays; *_cap fields give their capacities (elements). */
+typedef struct la_state_t {
+    int32_t  n_tokens;      /* committed tokens: prompt, then outputs; the last one (o) has no KV yet */
+    int32_t  tokens_cap;
+    int32_t *tokens;        /* [tokens_cap] */
+    int32_t *window;        /* [(N-1) * W], level-major: window[k*W + j] = level k, column j (level 0 oldest) */
+    int32_t  n_records;     /* pool entries */
+    int32_t  records_cap;
+    int32_t *records;       /* [records_cap][N]: first token, then the N-1 suffix tokens;
+                               keys ascending, each key's suffixes oldest first */
+} la_state_t;
+
+/* Create a decoder for the given weights.  Allocates the KV cache
+ * ([n_layers][2][n_kv_heads][max_seq][head_dim]), activations, the n-gram pool
+ * and the window on the current device; no weight is copied.
+ * Errors: INVALID_ARG (shapes, alignment, options), UNSUPPORTED, OOM, CUDA. */
+int la_create(const la_model_dims *dims, const la_weights *weights, const la_opts *opts,
+              la_handle **out);
+
+/* Prefill: run the prompt (host int32[n], n >= N and n + generated + M <= max_seq)
+ * causally, commit its KV, produce the first token (argmax, or a draw at
+ * temperature > 0) into *first_token (host), initialise the window from the
+ * prompt and, if asked, seed the pool.  Resets any previous state.
+ * Errors: INVALID_ARG, CAPACITY, CUDA, DEVICE_TIMEOUT. */
+int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token);
+
+/* One lookahead step.  Writes the A accepted tokens (1 <= A <= N) to host
+ * out_tokens (capacity >= N) and A to *out_n.  Synchronous.
+ * Errors: STATE (no prefill), CAPACITY (max_seq reached), CUDA, DEVICE_TIMEOUT. */
+int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n);
+
+/* Prefill, then steps until max_new tokens are produced (the prefill's first
+ * token counts; the last step is truncated).  Host out[max_new]; *out_n =
+ * tokens written; *n_steps = la_step calls.  Any of out_n / n_steps may be NULL. */
+int la_generate(la_handle *h, const int32_t *prompt, int32_t n, int32_t max_new,
+                int32_t *out, int32_t *out_n, int32_t *n_steps);
+
+/* Counters since the last prefill (host struct). */
+int la_stats(const la_handle *h, la_stats_t *out);
+
+/* Copy the committed tokens, window and pool to host buffers in *st.
+ * Errors: STATE, CAPACITY (a cap too small; n_tokens / n_records still report
+ * the sizes needed), CUDA. */
+int la_export_state(la_handle *h, la_state_t *st);
+
+/* Replace the state with *st (same N, W): recomputes the prefix KV from the
+ * tokens, loads window and pool.  Errors: INVALID_ARG, CAPACITY, CUDA. */
+int la_import_state(la_handle *h, const la_state_t *st);
+
+/* Logits of the last step's used rows, fp32, to host[rows * vocab]: row 0,
+ * then the top lookahead level's W rows, then G*(N-1) candidate rows
+ * (candidate c, depth m at 1 + W + c*(N-1) + m-1).  After la_prefill it
+ * holds the prompt's last row only (rows = 1).  *rows, *vocab receive the
+ * sizes; host may be NULL to query them. */
+int la_debug_logits(la_handle *h, float *host, int32_t *rows, int32_t *vocab);
+
+/* Plain bf16 GEMM on the library's tcgen05 kernel:
+ *   y[r][f] = sum_k x[r][k] * w[f][k]   (fp32 accumulation, fp32 out)
+ * x device bf16 [rows][k], w device bf16 [out][k], y device fp32 [rows][out];
+ * all 16-byte aligned, k % 8 == 0, 1 <= rows <= 256.  splits > 1 splits k
+ * across CTAs: partial sums go to `workspace` (device fp32, at least
+ * splits*rows*out elements, owned by the caller) and are added in a fixed
+ * order, so results are deterministic.  splits == 1 needs no workspace
+ * (NULL allowed).  stream: cudaStream_t or NULL.  Asynchronous.
+ * Errors: INVALID_ARG, CUDA. */
+int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
+                 int32_t splits, float *workspace, void *stream);
+
+void la_destroy(la_handle *h);
+const char *la_strerror(int code);
+const char *la_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LA_H */

@@ -1,0 +1,185 @@
+"""Lookahead step on the GPU vs the oracle, tiny fp32 decoder (2 layers,
+d 256, 4 heads x 64, FFN 688, vocab 1024): end-to-end streams, step-level
+teacher-forced parity (accepted tokens, new window, pool, logits <= 1e-4),
+edge configurations and error paths."""
+import numpy as np
+import pytest
+
+import synth
+from helpers import MARGIN_F32 as MARGIN, ar_with_margins, compare_stream, ensure_built, top2_margin
+from oracle import lookahead as la
+
+pytestmark = pytest.mark.gpu
+
+LOGIT_TOL_F32 = 1e-4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ensure_built()
+    import exact_decoding_gb300 as e
+    return e
+
+
+@pytest.fixture(scope="module")
+def tiny_model():
+    wl = synth.WORKLOADS["tiny-fp32-greedy"]
+    return wl, synth.model_weights(wl.dims, wl.seed), synth.prompt(wl)
+
+
+def make(lib, w, N, W, G, max_seq=256, **kw):
+    return lib.Decoder(w, N, W, G, max_seq, **kw)
+
+
+def test_prefill_first_token_and_logits(lib, tiny_model):
+    from oracle import decoder
+    wl, w, p = tiny_model
+    dec = make(lib, w, 3, 4, 4)
+    y1 = dec.prefill(p)
+    ref, _ = decoder.forward(w, list(p), np.arange(len(p)), decoder.causal_mask(0, len(p)), logit_rows=[len(p) - 1])
+    g = dec.debug_logits()
+    assert g.shape == (1, wl.dims.vocab)
+    assert np.max(np.abs(g[0] - ref[0])) <= LOGIT_TOL_F32
+    assert y1 == la.argmax_lowest(ref[0]) or top2_margin(ref[0]) <= MARGIN
+    dec.close()
+
+
+@pytest.mark.parametrize("N,W,G,par", [(3, 4, 4, False), (2, 3, 2, False), (5, 3, 0, False), (4, 2, 5, True),
+                                       (3, 1, 1, False), (8, 2, 3, False)])
+def test_generate_equals_autoregressive(lib, tiny_model, N, W, G, par):
+    wl, w, p = tiny_model
+    ar, margins = ar_with_margins(w, p, wl.new_tokens)
+    dec = make(lib, w, N, W, G, prompt_as_reference=par)
+    out, steps = dec.generate(p, wl.new_tokens)
+    assert len(out) == wl.new_tokens
+    upto = compare_stream(out, ar, margins, MARGIN)
+    assert upto >= 16, f"first low-margin decision at {upto}"
+    st = dec.stats()
+    assert st["steps"] == steps and st["generated"] >= wl.new_tokens
+    dec.close()
+
+
+def _teacher_forced(lib, w, p, N, W, G, steps, temperature=0.0, seed=0, par=False, tol=LOGIT_TOL_F32):
+    dec = make(lib, w, N, W, G, temperature=temperature, seed=seed, prompt_as_reference=par)
+    dec.prefill(p)
+    orc = la.Lookahead(w, N, W, G, temperature=temperature, seed=seed, prompt_as_reference=par, keep_logits=True)
+    checked = 0
+    for t in range(steps):
+        s0 = dec.export_state()
+        orc.load_state(s0["tokens"], s0["window"], s0["records"])
+        acc_ref = orc.step()
+        rec = orc.history[-1]
+        acc = dec.step()
+        logits = dec.debug_logits()
+        assert logits.shape == rec.logits.shape
+        err = np.max(np.abs(logits - rec.logits))
+        assert err <= tol, f"step {t}: logits max-abs {err}"
+        s1 = dec.export_state()
+        used = la.used_rows(N, W, G)
+        decisive = [0] + [1 + W + i for i in range(G * (N - 1))]
+        low = any(top2_margin(rec.logits[i]) <= MARGIN for i in decisive)
+        if temperature == 0.0 and not low:
+            assert acc == acc_ref, f"step {t}"
+        # new lookahead tokens: exact where the oracle's margin is clear
+        for j in range(W):
+            lr = rec.logits[1 + j]
+            gnew = int(s1["window"][N - 2, j])
+            if top2_margin(lr) > MARGIN:
+                assert gnew == rec.new[j], f"step {t} column {j}"
+            else:
+                assert lr[gnew] >= lr.max() - MARGIN
+        # pool: the oracle replays the GPU's own new tokens from the same start
+        pool = la.Pool.from_records(orc.pool.cap, s0["records"])
+        for key, suf in la.harvest(np.asarray(s0["window"]), [int(x) for x in s1["window"][N - 2]]):
+            pool.insert(key, suf)
+        assert pool.records() == s1["records"], f"step {t}: pool"
+        assert s1["tokens"] == s0["tokens"] + acc
+        checked += 1
+    dec.close()
+    return checked
+
+
+def test_step_teacher_forced_greedy(lib, tiny_model):
+    wl, w, p = tiny_model
+    assert _teacher_forced(lib, w, p, 3, 4, 4, steps=12) == 12
+
+
+def test_step_teacher_forced_repetitive_prompt(lib, tiny_model):
+    """A repeated prompt with prompt-as-reference makes candidates hit (A > 1)."""
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(8, wl.dims.vocab, seed=9), 5)
+    assert _teacher_forced(lib, w, p, 4, 3, 4, steps=10, par=True) == 10
+
+
+def test_step_teacher_forced_sampling(lib, tiny_model):
+    """Algorithm 4: same Philox draws on both sides; decisions within 1e-3 of
+    a threshold may differ (fp32 vs fp64), everything else must match."""
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(8, wl.dims.vocab, seed=9), 5)
+    N, W, G = 4, 3, 4
+    dec = make(lib, w, N, W, G, temperature=1.0, seed=1234, prompt_as_reference=True)
+    dec.prefill(p)
+    orc = la.Lookahead(w, N, W, G, temperature=1.0, seed=1234, prompt_as_reference=True, keep_logits=True)
+    exact = 0
+    for t in range(10):
+        s0 = dec.export_state()
+        orc.load_state(s0["tokens"], s0["window"], s0["records"])
+        acc_ref = orc.step()
+        trace = orc.history[-1].trace
+        acc = dec.step()
+        if acc == acc_ref:
+            exact += 1
+            continue
+        # find the first differing decision: it must be a near-tie
+        k = next(i for i in range(min(len(acc), len(acc_ref))) if acc[i] != acc_ref[i]) \
+            if any(a != b for a, b in zip(acc, acc_ref)) else min(len(acc), len(acc_ref))
+        near = [d for d in trace if abs(d.value) <= 1e-3]
+        assert near, f"step {t}: gpu {acc} vs oracle {acc_ref} with no near-threshold decision"
+    assert exact >= 8
+    dec.close()
+
+
+def test_import_state_resumes_identically(lib, tiny_model):
+    wl, w, p = tiny_model
+    a = make(lib, w, 3, 4, 4)
+    a.prefill(p)
+    for _ in range(5):
+        a.step()
+    s = a.export_state()
+    b = make(lib, w, 3, 4, 4)
+    b.import_state(s["tokens"], s["window"], s["records"])
+    for _ in range(6):
+        assert a.step() == b.step()
+    assert a.export_state()["records"] == b.export_state()["records"]
+    a.close()
+    b.close()
+
+
+def test_runs_are_bitwise_deterministic(lib, tiny_model):
+    wl, w, p = tiny_model
+    outs = []
+    for _ in range(2):
+        dec = make(lib, w, 4, 4, 4, prompt_as_reference=True)
+        outs.append((dec.generate(p, 40), dec.debug_logits().tobytes()))
+        dec.close()
+    assert outs[0] == outs[1]
+
+
+def test_error_paths(lib, tiny_model):
+    wl, w, p = tiny_model
+    dec = make(lib, w, 3, 4, 4, max_seq=64)
+    with pytest.raises(lib.LaError) as e:
+        dec.step()
+    assert e.value.code == -6            # step before prefill
+    with pytest.raises(lib.LaError) as e:
+        dec.prefill([1, 2])              # shorter than N
+    assert e.value.code == -1
+    with pytest.raises(lib.LaError) as e:
+        dec.prefill(list(p) + [5000])    # token out of range
+    assert e.value.code == -1
+    dec.prefill(p)
+    with pytest.raises(lib.LaError) as e:
+        for _ in range(64):
+            dec.step()
+    assert e.value.code == -3            # max_seq reached, reported before any launch
+    dec.close()
