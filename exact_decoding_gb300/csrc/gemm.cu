@@ -144,9 +144,22 @@ int tc_gemm_stages_for(int bn) {
     return s > 8 ? 8 : (s < 2 ? 2 : s);
 }
 
+// Raise the kernel's dynamic shared-memory limit once to the device's opt-in
+// maximum; every plan then launches under it.
+static cudaError_t gemm_smem_attr() {
+    static int done = 0;
+    if (done) return cudaSuccess;
+    int dev = 0, mx = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) done = 1;
+    return e;
+}
+
 int tc_gemm_ctas_per_sm(int bn, int stages) {
     const size_t sm = tc_gemm_smem_bytes(bn, stages);
-    cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
+    gemm_smem_attr();
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_gemm_tc, 192, sm) != cudaSuccess) n = 1;
     return n < 1 ? 1 : n;
@@ -176,13 +189,8 @@ void tc_gemm_finalize(TcGemm &g) {
 }
 
 cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s) {
-    static int configured_smem = 0;
-    if (static_cast<int>(g.smem) > configured_smem) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(g.smem));
-        if (e != cudaSuccess) return e;
-        configured_smem = static_cast<int>(g.smem);
-    }
+    cudaError_t e = gemm_smem_attr();
+    if (e != cudaSuccess) return e;
     k_gemm_tc<<<g.grid, 192, g.smem, s>>>(g.p);
     return cudaGetLastError();
 }

@@ -85,6 +85,16 @@ struct la_handle {
     int splits[2][4] = {{1, 1, 1, 1}, {1, 1, 1, 1}};
     size_t part_elems = 0;
 
+    // profiling (la_opts.profile): event pairs around GEMM / attention launches
+    bool prof_on = false;
+    std::vector<cudaEvent_t> ev;
+    std::vector<int> ev_cls;
+    std::vector<double> ev_bytes;
+    int ev_used = 0;
+    double prof_ms[2] = {0, 0}, prof_bytes[2] = {0, 0};
+    int64_t prof_launches[2] = {0, 0};
+    int64_t launches = 0;
+
     // host-side bookkeeping
     bool prefilled = false;
     int P = 0;
@@ -92,6 +102,7 @@ struct la_handle {
     int last_A = 0, last_g = 0, logits_rows = 0;
 
     ~la_handle() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
         for (void *p : allocs) cudaFree(p);
         if (st_host) cudaFreeHost(st_host);
     }
@@ -144,6 +155,41 @@ struct la_handle {
         return s;
     }
 
+    // Start a profiled launch: returns the event-pair slot, or -1 when off.
+    int prof_begin() {
+        if (!prof_on) return -1;
+        if (ev_used * 2 + 2 > static_cast<int>(ev.size())) {
+            for (int i = 0; i < 64; ++i) {
+                cudaEvent_t e;
+                if (cudaEventCreate(&e) != cudaSuccess) return -1;
+                ev.push_back(e);
+            }
+            ev_cls.resize(ev.size() / 2);
+            ev_bytes.resize(ev.size() / 2);
+        }
+        const int i = ev_used++;
+        cudaEventRecord(ev[2 * i], stream);
+        return i;
+    }
+    void prof_end(int i, int cls, double bytes) {
+        if (i < 0) return;
+        cudaEventRecord(ev[2 * i + 1], stream);
+        ev_cls[i] = cls;
+        ev_bytes[i] = bytes;
+    }
+    // After the stream is synchronised: fold the recorded pairs into the totals.
+    void prof_collect() {
+        for (int i = 0; i < ev_used; ++i) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, ev[2 * i], ev[2 * i + 1]) == cudaSuccess) {
+                prof_ms[ev_cls[i]] += ms;
+                prof_bytes[ev_cls[i]] += ev_bytes[i];
+                prof_launches[ev_cls[i]] += 1;
+            }
+        }
+        ev_used = 0;
+    }
+
     void *kv_layer(int l, int which) const {
         const size_t plane = static_cast<size_t>(nkv) * max_seq * hd * act;
         return static_cast<char *>(cache) + (static_cast<size_t>(l) * 2 + which) * plane;
@@ -181,12 +227,21 @@ uint64_t splitmix64(uint64_t x) {
 }
 
 // ------------------------------------------------------------------ GEMM dispatch
+double gemm_bytes(const la_handle *h, Kind kind, int nrows) {
+    const int K = kind == OPROJ ? h->qd : kind == DOWN ? h->F : h->d;
+    const int out = kind == QKV ? h->qkv_out : kind == GATEUP ? 2 * h->F : h->d;
+    return (static_cast<double>(out) * K + static_cast<double>(nrows) * K) * h->act + 4.0 * nrows * out;
+}
+
 int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
     const int ldo = kind == QKV ? h->qkv_out : kind == GATEUP ? 2 * h->F : h->d;
+    h->launches += 1;
+    const int pe = mode == STEP ? h->prof_begin() : -1;
     if (h->bf16) {
         TcGemm g = h->plan[mode][kind][l];
         g.p.nrows = nrows;
         CK(tc_gemm_launch(g, h->stream));
+        h->prof_end(pe, 0, gemm_bytes(h, kind, nrows));
         return LA_OK;
     }
     SimtGemmParams p{};
@@ -230,14 +285,20 @@ int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
     p.ldo = ldo;
     p.out = h->part;
     CK(simt_gemm_launch(p, p.seg_f0[p.nseg], h->stream));
+    h->prof_end(pe, 0, gemm_bytes(h, kind, nrows));
     return LA_OK;
 }
 
-int run_lm_head(la_handle *h, int nrows) {
+int run_lm_head(la_handle *h, int nrows, bool step) {
+    h->launches += 1;
+    const int pe = step ? h->prof_begin() : -1;
+    const double bytes = (static_cast<double>(h->V) * h->d + static_cast<double>(nrows) * h->d) * h->act +
+                         4.0 * nrows * h->V;
     if (h->bf16) {
         TcGemm g = h->plan_lm;
         g.p.nrows = nrows;
         CK(tc_gemm_launch(g, h->stream));
+        h->prof_end(pe, 0, bytes);
         return LA_OK;
     }
     SimtGemmParams p{};
@@ -253,6 +314,7 @@ int run_lm_head(la_handle *h, int nrows) {
     p.ldo = h->V;
     p.out = h->logits;
     CK(simt_gemm_launch(p, h->V, h->stream));
+    h->prof_end(pe, 0, bytes);
     return LA_OK;
 }
 
@@ -266,6 +328,7 @@ template <typename T>
 int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want_logits) {
     cudaStream_t s = h->stream;
     const float eps = h->dims.rms_eps;
+    h->launches += 1;
     CK(embed_norm_launch<T>(static_cast<const T *>(h->embed), tok, nrows, h->d,
                             static_cast<const T *>(h->attn_norm[0]), eps, h->h, static_cast<T *>(h->xn), s));
     const int nch = (P + kAttnChunk - 1) / kAttnChunk;
@@ -293,7 +356,12 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         a.anc_cnt = mode == STEP ? h->anc_cnt : nullptr;
         a.anc_stride = h->anc_stride;
         a.out = h->ao;
+        const int pe = mode == STEP ? h->prof_begin() : -1;
         CK(attention_launch<T>(a, s));
+        h->prof_end(pe, 1,
+                    (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * h->act + 4.0 * nrows * h->qd +
+                        static_cast<double>(nrows) * h->qd * h->act);
+        h->launches += 2 + (nch > 0 ? 1 : 0);   // qkv_rope, attention passes
         if ((rc = run_gemm(h, mode, OPROJ, l, nrows)) != LA_OK) return rc;
         const long long ss_d = static_cast<long long>(h->R) * h->d;
         CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][OPROJ], ss_d, h->d, h->d,
@@ -303,6 +371,7 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         const long long ss_gu = static_cast<long long>(h->R) * 2 * h->F;
         CK(swiglu_launch<T>(h->part, h->splits[mode][GATEUP], ss_gu, 2 * h->F, nrows, h->F,
                             static_cast<T *>(h->fa), s));
+        h->launches += 3;   // resid_norm after O, swiglu, resid_norm after down
         if ((rc = run_gemm(h, mode, DOWN, l, nrows)) != LA_OK) return rc;
         if (l + 1 < h->L) {
             CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][DOWN], ss_d, h->d, h->d,
@@ -351,7 +420,7 @@ int run_prefix(la_handle *h, int n, bool want_logits) {
         if (rc != LA_OK) return rc;
     }
     if (want_logits) {
-        int rc = run_lm_head(h, 1);
+        int rc = run_lm_head(h, 1, false);
         if (rc != LA_OK) return rc;
         CK(argmax_launch(h->logits, 1, h->V, h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
                          h->lmax, h->lsum, h->stream));
@@ -522,6 +591,7 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     h->dims = D;
     h->opts = O;
     h->stream = static_cast<cudaStream_t>(O.cuda_stream);
+    h->prof_on = O.profile != 0;
     h->bf16 = D.dtype == LA_BF16;
     h->act = h->bf16 ? 2 : 4;
     h->L = D.n_layers;
@@ -719,6 +789,9 @@ int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_to
     h->last_A = 0;
     h->last_g = 0;
     h->logits_rows = 1;
+    h->launches = 0;
+    h->ev_used = 0;
+    for (int c = 0; c < 2; ++c) h->prof_ms[c] = h->prof_bytes[c] = 0, h->prof_launches[c] = 0;
     return LA_OK;
 }
 
@@ -730,14 +803,16 @@ int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     CK(build_rows_launch(h->spec(), s));
     int rc = forward_any(h, STEP, h->tok, h->M, h->P, true);
     if (rc != LA_OK) return rc;
-    if ((rc = run_lm_head(h, h->U)) != LA_OK) return rc;
+    if ((rc = run_lm_head(h, h->U, true)) != LA_OK) return rc;
     CK(argmax_launch(h->logits, h->U, h->V, h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
                      h->lmax, h->lsum, s));
     CK(finish_step_launch(h->spec(), s));
     if ((rc = kv_commit(h)) != LA_OK) return rc;
+    h->launches += 4;   // build_rows, argmax, finish_step, kv_commit
     CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));
     if ((rc = check_device_error(h)) != LA_OK) return rc;
+    h->prof_collect();
     const SpecState &st = *h->st_host;
     if (st.A < 1 || st.A > h->N) {
         h->prefilled = false;
@@ -782,6 +857,13 @@ int la_stats(const la_handle *h, la_stats_t *o) {
     o->last_candidates = h->last_g;
     o->prefix_len = h->P;
     o->rows = h->M;
+    o->gemm_ms = h->prof_ms[0];
+    o->gemm_bytes = h->prof_bytes[0];
+    o->gemm_launches = h->prof_launches[0];
+    o->attn_ms = h->prof_ms[1];
+    o->attn_bytes = h->prof_bytes[1];
+    o->attn_launches = h->prof_launches[1];
+    o->kernel_launches = h->launches;
     return LA_OK;
 }
 

@@ -185,7 +185,7 @@ __device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, co
         if (lane >= o) incl += y;
     }
     if (lane == 31) s_warp[w] = incl;
-    if (tid == 0) s_ans = -1;
+    if (tid == 0) s_ans = INT_MAX;
     __syncthreads();
     if (w == 0) {
         float x = lane < NT / 32 ? s_warp[lane] : 0.f;
@@ -213,10 +213,10 @@ __device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, co
                 break;
             }
         }
-        s_ans = ans;
+        atomicMin(&s_ans, ans);   // rounding can make two ranges claim t: lowest id wins
     }
     __syncthreads();
-    if (tid == 0 && s_ans < 0) {
+    if (tid == 0 && s_ans == INT_MAX) {
         // t rounded up to the total: take the last id with weight
         for (int i = NT - 1; i >= 0; --i)
             if (s_part[i] > 0.f) {
@@ -241,7 +241,7 @@ constexpr int kFinishThreads = 1024;
 
 __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
     __shared__ int s_acc[8];
-    __shared__ int s_A, s_win, s_need_draw, s_dist_u, s_nrej, s_pos;
+    __shared__ int s_A, s_win, s_need_draw, s_dist_u, s_nrej;
     __shared__ int s_rej[32];
     __shared__ float s_u;
     const int L = d.N - 1;
@@ -314,7 +314,6 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
                 s_dist_u = dist_u;
                 s_nrej = nrej;
                 s_u = draw_uniform(d.seed, pos, nd);
-                s_pos = pos;
                 break;
             }
             if (A > 0) win = __ffs(surv) - 1;

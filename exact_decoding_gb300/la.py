@@ -45,12 +45,16 @@ class la_weights(ctypes.Structure):
 class la_opts(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int32), ("W", ctypes.c_int32), ("G", ctypes.c_int32), ("max_seq", ctypes.c_int32),
                 ("prompt_as_reference", ctypes.c_int32), ("pool_cap", ctypes.c_int32),
-                ("temperature", ctypes.c_float), ("seed", ctypes.c_uint64), ("cuda_stream", ctypes.c_void_p)]
+                ("temperature", ctypes.c_float), ("seed", ctypes.c_uint64), ("cuda_stream", ctypes.c_void_p),
+                ("profile", ctypes.c_int32)]
 
 
 class la_stats_t(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int64), ("generated", ctypes.c_int64), ("last_accept", ctypes.c_int32),
-                ("last_candidates", ctypes.c_int32), ("prefix_len", ctypes.c_int32), ("rows", ctypes.c_int32)]
+                ("last_candidates", ctypes.c_int32), ("prefix_len", ctypes.c_int32), ("rows", ctypes.c_int32),
+                ("gemm_ms", ctypes.c_double), ("gemm_bytes", ctypes.c_double), ("gemm_launches", ctypes.c_int64),
+                ("attn_ms", ctypes.c_double), ("attn_bytes", ctypes.c_double), ("attn_launches", ctypes.c_int64),
+                ("kernel_launches", ctypes.c_int64)]
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -187,15 +191,15 @@ def la_destroy(h) -> None:
         load_library().la_destroy(h)
 
 
-# ---------------------------------------------------------------------------- owner
-class Decoder:
-    """Owns device copies of a weight dict (synth.model_weights layout) and a handle."""
+# ---------------------------------------------------------------------------- owners
+class DeviceWeights:
+    """Device copies (torch tensors) of a weight dict in the synth.model_weights
+    layout, and the la_weights / la_model_dims structs that point at them."""
 
-    def __init__(self, weights: dict, N: int, W: int, G: int, max_seq: int, temperature: float = 0.0,
-                 seed: int = 0, prompt_as_reference: bool = False, pool_cap: int = 0, stream=None, device="cuda"):
+    def __init__(self, weights: dict, device="cuda"):
         import torch
         dims = weights["dims"]
-        self.dims, self.N, self.W, self.G = dims, N, W, G
+        self.dims = dims
         self._keep = []
 
         def up(a):
@@ -211,20 +215,33 @@ class Decoder:
             self._keep.append(a)
             return ctypes.cast(a, _PP)
 
-        layers = weights["layers"]
-        per = {k: [] for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")}
-        for lw in layers:
-            for k in per:
+        names = ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down")
+        per = {k: [] for k in names}
+        for lw in weights["layers"]:
+            for k in names:
                 per[k].append(up(lw[k]))
-        w = la_weights(up(weights["embed"]), up(weights["final_norm"]), up(weights["lm_head"]),
-                       *[arr(per[k]) for k in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
-                                               "w_down")])
-        d = la_model_dims(dims.n_layers, dims.d_model, dims.n_heads, dims.n_kv_heads, dims.head_dim, dims.ffn,
-                          dims.vocab, dims.rms_eps, dims.rope_base, LA_BF16 if dims.dtype == "bf16" else LA_F32)
+        self.struct = la_weights(up(weights["embed"]), up(weights["final_norm"]), up(weights["lm_head"]),
+                                 *[arr(per[k]) for k in names])
+        self.dims_struct = la_model_dims(dims.n_layers, dims.d_model, dims.n_heads, dims.n_kv_heads, dims.head_dim,
+                                         dims.ffn, dims.vocab, dims.rms_eps, dims.rope_base,
+                                         LA_BF16 if dims.dtype == "bf16" else LA_F32)
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self._keep if hasattr(t, "numel"))
+
+
+class Decoder:
+    """A la_handle over DeviceWeights (or a host weight dict, uploaded here)."""
+
+    def __init__(self, weights, N: int, W: int, G: int, max_seq: int, temperature: float = 0.0,
+                 seed: int = 0, prompt_as_reference: bool = False, pool_cap: int = 0, stream=None, device="cuda",
+                 profile: bool = False):
+        self.weights = weights if isinstance(weights, DeviceWeights) else DeviceWeights(weights, device)
+        self.dims, self.N, self.W, self.G = self.weights.dims, N, W, G
         self.stream = stream
         sp = stream.cuda_stream if stream is not None else None
-        o = la_opts(N, W, G, max_seq, int(prompt_as_reference), pool_cap, temperature, seed, sp)
-        self.h = la_create(d, w, o)
+        o = la_opts(N, W, G, max_seq, int(prompt_as_reference), pool_cap, temperature, seed, sp, int(profile))
+        self.h = la_create(self.weights.dims_struct, self.weights.struct, o)
 
     def prefill(self, prompt) -> int:
         return la_prefill(self.h, prompt)
@@ -251,7 +268,6 @@ class Decoder:
         if getattr(self, "h", None):
             la_destroy(self.h)
             self.h = None
-        self._keep = []
 
     def __del__(self):
         try:

@@ -102,6 +102,9 @@ typedef struct la_opts {
     float   temperature;          /* 0: greedy (Algorithm 3); > 0: sampling (Algorithm 4) */
     uint64_t seed;                /* window initialisation and sampling draws */
     void   *cuda_stream;          /* cudaStream_t or NULL */
+    int32_t profile;              /* 1: bracket every GEMM and attention launch of la_step with CUDA
+                                     events and accumulate their device time in la_stats (adds two
+                                     event records per launch) */
 } la_opts;
 
 typedef struct la_handle la_handle;
@@ -113,6 +116,17 @@ typedef struct la_stats_t {
     int32_t last_candidates;  /* g of the last step, 0..G */
     int32_t prefix_len;       /* P: tokens whose KV is committed */
     int32_t rows;             /* M = 1 + (W + G)(N - 1) rows per step */
+    /* With la_opts.profile = 1, summed over la_step calls since la_prefill:
+     * device time (CUDA events on the handle's stream), launch count and
+     * algorithmic bytes of the projection GEMMs (weights + input rows + fp32
+     * output) and of attention (prefix K/V + queries + outputs). */
+    double  gemm_ms;
+    double  gemm_bytes;
+    int64_t gemm_launches;
+    double  attn_ms;
+    double  attn_bytes;
+    int64_t attn_launches;
+    int64_t kernel_launches;  /* kernels launched by la_step calls since la_prefill */
 } la_stats_t;
 
 /* Host-side snapshot of the decoding state, for resume and for checking a

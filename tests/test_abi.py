@@ -47,7 +47,7 @@ def test_create_rejects_bad_options_without_touching_the_gpu():
     lib = L.load_library()
     d = L.la_model_dims(2, 256, 4, 4, 96, 688, 1024, 1e-5, 1e4, L.LA_F32)   # head_dim 96: unsupported
     w = L.la_weights()
-    o = L.la_opts(3, 4, 4, 256, 0, 0, 0.0, 0, None)
+    o = L.la_opts(3, 4, 4, 256, 0, 0, 0.0, 0, None, 0)
     h = ctypes.c_void_p()
     assert lib.la_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(o), ctypes.byref(h)) == -7
     d.head_dim = 64
