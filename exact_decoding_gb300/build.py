@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libla.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["gemm.cu", "elementwise.cu", "attention.cu", "spec.cu", "la_api.cu"]
+SOURCES = ["gemm.cu", "elementwise.cu", "attention.cu", "spec.cu", "la_api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 

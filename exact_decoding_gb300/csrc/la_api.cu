@@ -48,6 +48,8 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 }  // namespace
 
+int la::set_last_error(int code, const char *msg) { return fail(code, "%s", msg); }
+
 struct la_handle {
     la_model_dims dims{};
     la_opts opts{};

@@ -50,6 +50,9 @@ struct SimtGemmParams {
     float *out;
 };
 
+// Record `msg` as the calling thread's last error (la_last_error) and return `code`.
+int set_last_error(int code, const char *msg);
+
 // Tensor-map construction (driver entry point fetched through the runtime).
 int make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                    uint32_t box_inner, uint32_t box_outer);

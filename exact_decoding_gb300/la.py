@@ -86,6 +86,8 @@ def load_library():
     lib.la_debug_logits.argtypes = [H, ctypes.c_void_p, _I32P, _I32P]
     lib.la_gemm_bf16.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+    lib.la_gemm_bf16_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
     lib.la_destroy.argtypes = [H]
     lib.la_destroy.restype = None
     lib.la_strerror.argtypes = [ctypes.c_int]
@@ -93,7 +95,7 @@ def load_library():
     lib.la_last_error.argtypes = []
     lib.la_last_error.restype = ctypes.c_char_p
     for name in ("la_create", "la_prefill", "la_step", "la_generate", "la_stats", "la_export_state",
-                 "la_import_state", "la_debug_logits", "la_gemm_bf16"):
+                 "la_import_state", "la_debug_logits", "la_gemm_bf16", "la_gemm_bf16_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -184,6 +186,19 @@ def la_gemm_bf16(x_ptr: int, w_ptr: int, y_ptr: int, rows: int, out: int, k: int
                  workspace_ptr: Optional[int] = None, stream: Optional[int] = None) -> None:
     _check(load_library().la_gemm_bf16(x_ptr, w_ptr, y_ptr, rows, out, k, splits, workspace_ptr, stream),
            "la_gemm_bf16")
+
+
+def la_gemm_bf16_noalloc(x_ptr: int, w_ptr: int, y_ptr: int, rows: int, out: int, k: int, splits: int = 1,
+                         stream: Optional[int] = None) -> None:
+    """la_gemm_bf16 without a caller workspace: for callers that cannot allocate
+    device memory at call time.  The split-K partials live in a fixed device
+    array inside the library (LA_NOALLOC_SCRATCH_FLOATS floats); overlapping
+    calls race on it."""
+    _check(load_library().la_gemm_bf16_noalloc(x_ptr, w_ptr, y_ptr, rows, out, k, splits, stream),
+           "la_gemm_bf16_noalloc")
+
+
+NOALLOC_SCRATCH_FLOATS = 4 * 1024 * 1024
 
 
 def la_destroy(h) -> None:

@@ -199,6 +199,26 @@ int la_debug_logits(la_handle *h, float *host, int32_t *rows, int32_t *vocab);
 int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
                  int32_t splits, float *workspace, void *stream);
 
+/* Same GEMM as la_gemm_bf16, for callers that cannot allocate device memory
+ * at call time (for example a plugin inside a host framework that owns every
+ * device allocation, or a latency-critical loop that must not call cudaMalloc
+ * and its implied synchronisation), and so cannot pass a split-K workspace.
+ * The paper has no counterpart; this is a library convenience.
+ *
+ * The partial sums live in a fixed device array inside the library of
+ * LA_NOALLOC_SCRATCH_FLOATS floats (16 MiB), which every GPU that loads the
+ * library holds until the process exits.  The call allocates nothing.
+ * Requires splits * rows * out <= LA_NOALLOC_SCRATCH_FLOATS, else it returns
+ * LA_ERR_CAPACITY with nothing launched; other limits as la_gemm_bf16.
+ * The first call on each device looks up that array's device address (with
+ * the device current); make that first call before any stream capture.
+ * All calls share the array: calls whose kernels overlap on the GPU (other
+ * streams, other threads on the same device) race and must be serialised by
+ * the caller.  Asynchronous on `stream`.  Errors: INVALID_ARG, CAPACITY, CUDA. */
+#define LA_NOALLOC_SCRATCH_FLOATS (4 * 1024 * 1024)
+int la_gemm_bf16_noalloc(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
+                         int32_t splits, void *stream);
+
 void la_destroy(la_handle *h);
 const char *la_strerror(int code);
 const char *la_last_error(void);
