@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama7b-bf16-greedy")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu", action="store_true",
+                    help="profiling run: prefill + warm-up + timed steps only (no e2e, profiled pass or CPU baseline)")
     return ap.parse_args()
 
 
@@ -232,13 +234,15 @@ def run_ours(args, wl, rank, world, local_rank):
         torch.cuda.synchronize()
 
     # ---- end to end: la_generate, host prompt -> host tokens (one warm call first)
-    dec.generate(prompt, min(wl.new_tokens, 16))
-    sync()
-    t0 = time.perf_counter()
-    toks, gen_steps = dec.generate(prompt, wl.new_tokens)
-    sync()
-    e2e_s = time.perf_counter() - t0
-    e2e_tps = len(toks) / e2e_s
+    toks, gen_steps, e2e_s, e2e_tps = [], 0, 0.0, None
+    if not args.ncu:
+        dec.generate(prompt, min(wl.new_tokens, 16))
+        sync()
+        t0 = time.perf_counter()
+        toks, gen_steps = dec.generate(prompt, wl.new_tokens)
+        sync()
+        e2e_s = time.perf_counter() - t0
+        e2e_tps = len(toks) / e2e_s
     log(f"e2e: {len(toks)} tokens in {gen_steps} steps, {e2e_s:.3f} s")
 
     # ---- device-timed steps
@@ -274,11 +278,12 @@ def run_ours(args, wl, rank, world, local_rank):
 
     # ---- profiled pass (events around every GEMM / attention launch)
     pdec = e.Decoder(dw, wl.N, wl.W, wl.G, max_seq, stream=stream, profile=True, **kw)
-    pdec.prefill(prompt)
-    for _ in range(min(args.steps, 16)):
-        if pdec.stats()["generated"] + wl.N > wl.new_tokens:
-            break
-        pdec.step()
+    if not args.ncu:
+        pdec.prefill(prompt)
+        for _ in range(min(args.steps, 16)):
+            if pdec.stats()["generated"] + wl.N > wl.new_tokens:
+                break
+            pdec.step()
     pst = pdec.stats()
     pdec.close()
     log(f"profile: gemm {pst['gemm_ms']:.2f} ms / {pst['gemm_launches']} launches, "
@@ -300,7 +305,7 @@ def run_ours(args, wl, rank, world, local_rank):
     d = wl.dims
     act = 2 if d.dtype == "bf16" else 4
     weight_bytes = sum(t.numel() * t.element_size() for t in dw._keep if hasattr(t, "numel")) - d.vocab * d.d_model * act
-    kv_per_tok = 2 * d.n_layers * d.n_kv_heads * d.head_dim * act
+    kv_per_tok = 2 * d.n_layers * d.n_kv_heads * d.head_dim * 4   # fp32 KV cache
     mean_P = statistics.mean(prefixes)
     step_bytes = weight_bytes + mean_P * kv_per_tok + wl.M * d.d_model * act + wl.N * kv_per_tok
     peak, peak_kind = peaks()
@@ -338,7 +343,7 @@ def run_ours(args, wl, rank, world, local_rank):
                       "ms_per_step": pst["attn_ms"] / max(pst["steps"], 1)},
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline and world == 1:
+    if not args.no_cpu_baseline and not args.ncu and world == 1:
         t1, t0 = oracle_step_sample(weights, wl, prompt, 0)
         step_s = extrapolated_step_seconds(t1, t0, d.n_layers)
         a = accepted / args.steps

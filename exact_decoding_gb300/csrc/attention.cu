@@ -209,14 +209,13 @@ static cudaError_t attention_launch_hd(const AttnArgs &a, cudaStream_t s) {
             configured = true;
         }
         dim3 grid(a.nkv, a.nch);
-        k_attn_prefix<T, HD><<<grid, 256, smem, s>>>(a.q, static_cast<const T *>(a.kc), static_cast<const T *>(a.vc),
+        k_attn_prefix<T, HD><<<grid, 256, smem, s>>>(a.q, a.kc, a.vc,
                                                      a.max_seq, a.P, a.nrows, a.nh, a.nkv, a.ws);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     const int warps = a.nrows * a.nh;
-    k_attn_final<T, HD><<<(warps + 7) / 8, 256, 0, s>>>(a.q, static_cast<const T *>(a.kc),
-                                                         static_cast<const T *>(a.vc), a.max_seq, a.P, a.nrows, a.nh,
+    k_attn_final<T, HD><<<(warps + 7) / 8, 256, 0, s>>>(a.q, a.kc, a.vc, a.max_seq, a.P, a.nrows, a.nh,
                                                          a.nkv, a.ws, a.nch, a.anc, a.anc_cnt, a.anc_stride,
                                                          static_cast<T *>(a.out));
     return cudaGetLastError();
@@ -230,6 +229,300 @@ cudaError_t attention_launch(const AttnArgs &a, cudaStream_t s) {
 }
 
 template cudaError_t attention_launch<float>(const AttnArgs &, cudaStream_t);
-template cudaError_t attention_launch<__nv_bfloat16>(const AttnArgs &, cudaStream_t);
+
+// ========================================================================== tensor-core path (bf16 models)
+// One CTA = (KV head, 64-key chunk, 64 query vectors); 4 warps x 16 queries.
+// Chunks [0, nch_prefix) cover the cached prefix [0, P), visible to every
+// row.  Chunks from nch_prefix on cover this step's own rows (slots P + s):
+// row r sees step key s iff bit s of vis_bits[r] is set (tree mode) or s <= r
+// (causal mode).
+//
+// Precision: K, V and q are fp32.  Each is split into bf16 planes hi + lo in
+// shared memory and every product runs as three bf16 MMAs (hi*hi + hi*lo +
+// lo*hi, fp32 accumulate) on mma.sync m16n8k16, which keeps about 16
+// mantissa bits; the softmax is fp32 in registers and P is split the same
+// way for P V.  Each CTA writes the chunk's (unnormalised O, max, sum) per
+// query; k_attn_merge combines the chunks in order.
+namespace {
+
+constexpr int kTcChunk = 64;
+constexpr int kTcQ = 64;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// bf16 pair (lo element first) for hi and for the remainder lo.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(128) k_attn_tc(const float *q, const float *kc, const float *vc, int max_seq, int P,
+                                                 int nrows, int nh, int nkv, int nch_prefix, const uint32_t *vis_bits,
+                                                 float *ws) {
+    constexpr int LD = HD + 8;   // smem row stride (bf16): 16-byte aligned rows, conflict-free ldmatrix
+    extern __shared__ __align__(16) __nv_bfloat16 smb[];
+    __nv_bfloat16 *Kh = smb;                     // [kTcChunk][LD] each
+    __nv_bfloat16 *Kl = Kh + kTcChunk * LD;
+    __nv_bfloat16 *Vh = Kl + kTcChunk * LD;
+    __nv_bfloat16 *Vl = Vh + kTcChunk * LD;
+    __nv_bfloat16 *Qh = Vl + kTcChunk * LD;      // [kTcQ][LD] each
+    __nv_bfloat16 *Ql = Qh + kTcQ * LD;
+
+    const int kvh = blockIdx.x, chunk = blockIdx.y, qb = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = nh / nkv;
+    const int QV = nrows * gq;
+    const bool step_chunk = chunk >= nch_prefix;
+    const int key0 = step_chunk ? (chunk - nch_prefix) * kTcChunk : chunk * kTcChunk;   // step index or position
+    const int slot0 = step_chunk ? P + key0 : key0;
+    const int nkeys = step_chunk ? min(kTcChunk, nrows - key0) : min(kTcChunk, P - key0);
+
+    // K / V chunk -> shared hi/lo planes (keys past the chunk are zero)
+    const float *kb = kc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
+    const float *vb = vc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
+    for (int t = tid; t < kTcChunk * (HD / 4); t += 128) {
+        const int key = t / (HD / 4), c = (t % (HD / 4)) * 4;
+        float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
+        if (key < nkeys) {
+            kx = *reinterpret_cast<const float4 *>(kb + static_cast<long long>(key) * HD + c);
+            vx = *reinterpret_cast<const float4 *>(vb + static_cast<long long>(key) * HD + c);
+        }
+        uint2 h, l;
+        split2(kx.x, kx.y, h.x, l.x);
+        split2(kx.z, kx.w, h.y, l.y);
+        *reinterpret_cast<uint2 *>(Kh + key * LD + c) = h;
+        *reinterpret_cast<uint2 *>(Kl + key * LD + c) = l;
+        split2(vx.x, vx.y, h.x, l.x);
+        split2(vx.z, vx.w, h.y, l.y);
+        *reinterpret_cast<uint2 *>(Vh + key * LD + c) = h;
+        *reinterpret_cast<uint2 *>(Vl + key * LD + c) = l;
+    }
+    // Q block -> shared hi/lo planes (scaled by 1/sqrt(hd))
+    const float scale = rsqrtf(static_cast<float>(HD));
+    for (int t = tid; t < kTcQ * (HD / 4); t += 128) {
+        const int i = t / (HD / 4), c = (t % (HD / 4)) * 4;
+        const int qv = qb * kTcQ + i;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qv < QV) {
+            const int r = qv / gq, hq = kvh * gq + qv % gq;
+            x = *reinterpret_cast<const float4 *>(q + (static_cast<long long>(r) * nh + hq) * HD + c);
+        }
+        uint2 h, l;
+        split2(x.x * scale, x.y * scale, h.x, l.x);
+        split2(x.z * scale, x.w * scale, h.y, l.y);
+        *reinterpret_cast<uint2 *>(Qh + i * LD + c) = h;
+        *reinterpret_cast<uint2 *>(Ql + i * LD + c) = l;
+    }
+    __syncthreads();
+
+    const int qv0 = qb * kTcQ + warp * 16;
+    if (qv0 >= QV) return;   // whole warp past the last query (no later block-wide sync)
+
+    // S = Q K^T : 16 queries x 64 keys (8 n-tiles of 8 keys), three passes
+    float sacc[kTcChunk / 8][4];
+#pragma unroll
+    for (int j = 0; j < kTcChunk / 8; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
+    {
+        const int qrow = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int qcol = 8 * (lane >> 4);
+        const int krow = (lane & 7) + 8 * (lane >> 4);
+        const int kcol = 8 * ((lane >> 3) & 1);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+            uint32_t ah[4], al[4];
+            ldsm_x4(smem_u32(Qh + qrow * LD + ks * 16 + qcol), ah[0], ah[1], ah[2], ah[3]);
+            ldsm_x4(smem_u32(Ql + qrow * LD + ks * 16 + qcol), al[0], al[1], al[2], al[3]);
+#pragma unroll
+            for (int np = 0; np < kTcChunk / 16; ++np) {
+                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                ldsm_x4(smem_u32(Kh + (np * 16 + krow) * LD + ks * 16 + kcol), h0, h1, h2, h3);
+                ldsm_x4(smem_u32(Kl + (np * 16 + krow) * LD + ks * 16 + kcol), l0, l1, l2, l3);
+                mma_bf16(sacc[2 * np], ah, h0, h1);
+                mma_bf16(sacc[2 * np], ah, l0, l1);
+                mma_bf16(sacc[2 * np], al, h0, h1);
+                mma_bf16(sacc[2 * np + 1], ah, h2, h3);
+                mma_bf16(sacc[2 * np + 1], ah, l2, l3);
+                mma_bf16(sacc[2 * np + 1], al, h2, h3);
+            }
+        }
+    }
+    // mask + softmax (rows ra = lane/4 and rb = ra + 8 of this warp's 16)
+    const int qa_v = qv0 + (lane >> 2), qb_v = qa_v + 8;
+    const int ra = qa_v < QV ? qa_v / gq : -1, rb = qb_v < QV ? qb_v / gq : -1;
+    float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kTcChunk / 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int kk = j * 8 + 2 * (lane & 3) + e;
+            bool va = kk < nkeys && ra >= 0, vb2 = kk < nkeys && rb >= 0;
+            if (step_chunk) {
+                const int sidx = key0 + kk;
+                if (vis_bits) {
+                    va = va && ((vis_bits[ra * 8 + (sidx >> 5)] >> (sidx & 31)) & 1u);
+                    vb2 = vb2 && ((vis_bits[rb * 8 + (sidx >> 5)] >> (sidx & 31)) & 1u);
+                } else {
+                    va = va && sidx <= ra;
+                    vb2 = vb2 && sidx <= rb;
+                }
+            }
+            if (!va) sacc[j][e] = -INFINITY;
+            if (!vb2) sacc[j][2 + e] = -INFINITY;
+            ma = fmaxf(ma, sacc[j][e]);
+            mb = fmaxf(mb, sacc[j][2 + e]);
+        }
+    }
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    float la_ = 0.f, lb = 0.f;
+#pragma unroll
+    for (int j = 0; j < kTcChunk / 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float pa = ma == -INFINITY ? 0.f : expf(sacc[j][e] - ma);
+            const float pb = mb == -INFINITY ? 0.f : expf(sacc[j][2 + e] - mb);
+            sacc[j][e] = pa;
+            sacc[j][2 + e] = pb;
+            la_ += pa;
+            lb += pb;
+        }
+    }
+    la_ += __shfl_xor_sync(0xffffffffu, la_, 1);
+    la_ += __shfl_xor_sync(0xffffffffu, la_, 2);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+    // O = P V : 16 queries x HD dims, three passes
+    float oacc[HD / 8][4];
+#pragma unroll
+    for (int j = 0; j < HD / 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
+    {
+        const int vrow = (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int vcol = 8 * (lane >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kTcChunk / 16; ++kk) {
+            uint32_t ph[4], pl[4];
+            split2(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
+            split2(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
+            split2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ph[2], pl[2]);
+            split2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+            for (int dp = 0; dp < HD / 16; ++dp) {
+                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
+                ldsm_x4_t(smem_u32(Vh + (kk * 16 + vrow) * LD + dp * 16 + vcol), h0, h1, h2, h3);
+                ldsm_x4_t(smem_u32(Vl + (kk * 16 + vrow) * LD + dp * 16 + vcol), l0, l1, l2, l3);
+                mma_bf16(oacc[2 * dp], ph, h0, h1);
+                mma_bf16(oacc[2 * dp], ph, l0, l1);
+                mma_bf16(oacc[2 * dp], pl, h0, h1);
+                mma_bf16(oacc[2 * dp + 1], ph, h2, h3);
+                mma_bf16(oacc[2 * dp + 1], ph, l2, l3);
+                mma_bf16(oacc[2 * dp + 1], pl, h2, h3);
+            }
+        }
+    }
+    // partials: ws[chunk][r][h][HD + 4] = (O, max, sum)
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int qvv = half ? qb_v : qa_v;
+        if (qvv >= QV) continue;
+        const int r = qvv / gq, hq = kvh * gq + qvv % gq;
+        float *w = ws + ((static_cast<long long>(chunk) * nrows + r) * nh + hq) * (HD + 4);
+#pragma unroll
+        for (int j = 0; j < HD / 8; ++j)
+            *reinterpret_cast<float2 *>(w + j * 8 + 2 * (lane & 3)) =
+                make_float2(oacc[j][2 * half], oacc[j][2 * half + 1]);
+        if ((lane & 3) == 0) {
+            w[HD] = half ? mb : ma;
+            w[HD + 1] = half ? lb : la_;
+        }
+    }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(256) k_attn_merge(const float *ws, int nch, int nrows, int nh, __nv_bfloat16 *out,
+                                                    long long lo_off) {
+    constexpr int DPL = HD / 32;
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= nrows * nh) return;
+    const int r = gw / nh, h = gw % nh;
+    float m = -INFINITY, l = 0.f, o[DPL];
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) o[j] = 0.f;
+    for (int c = 0; c < nch; ++c) {
+        const float *w = ws + ((static_cast<long long>(c) * nrows + r) * nh + h) * (HD + 4);
+        const float pm = w[HD];
+        if (pm == -INFINITY) continue;
+        const float pl = w[HD + 1];
+        const float nm = fmaxf(m, pm);
+        const float a = (m == -INFINITY) ? 0.f : expf(m - nm);
+        const float b = expf(pm - nm);
+        l = l * a + pl * b;
+#pragma unroll
+        for (int j = 0; j < DPL; ++j) o[j] = o[j] * a + w[lane * DPL + j] * b;
+        m = nm;
+    }
+    const float inv = 1.f / l;
+    const long long base = static_cast<long long>(r) * nh * HD + h * HD + lane * DPL;
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) store_act(out, base + j, o[j] * inv, lo_off);
+}
+
+template <int HD>
+cudaError_t attention_tc_hd(const AttnArgs &a, cudaStream_t s) {
+    const int nch_prefix = (a.P + kTcChunk - 1) / kTcChunk;
+    const int nch = nch_prefix + (a.nrows + kTcChunk - 1) / kTcChunk;
+    const int gq = a.nh / a.nkv;
+    const size_t smem = static_cast<size_t>(4 * kTcChunk + 2 * kTcQ) * (HD + 8) * sizeof(__nv_bfloat16);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    dim3 grid(a.nkv, nch, (a.nrows * gq + kTcQ - 1) / kTcQ);
+    k_attn_tc<HD><<<grid, 128, smem, s>>>(a.q, a.kc, a.vc, a.max_seq, a.P, a.nrows, a.nh, a.nkv, nch_prefix,
+                                          a.vis_bits, a.ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int warps = a.nrows * a.nh;
+    k_attn_merge<HD><<<(warps + 7) / 8, 256, 0, s>>>(a.ws, nch, a.nrows, a.nh, static_cast<__nv_bfloat16 *>(a.out),
+                                                     a.out_lo_off);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int attention_tc_chunks(int P, int nrows) {
+    return (P + kTcChunk - 1) / kTcChunk + (nrows + kTcChunk - 1) / kTcChunk;
+}
+
+template <>
+cudaError_t attention_launch<__nv_bfloat16>(const AttnArgs &a, cudaStream_t s) {
+    if (a.hd == 128) return attention_tc_hd<128>(a, s);
+    if (a.hd == 64) return attention_tc_hd<64>(a, s);
+    return cudaErrorInvalidValue;
+}
 
 }  // namespace la

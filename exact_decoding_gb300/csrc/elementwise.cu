@@ -28,7 +28,7 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 // ------------------------------------------------------------------ embed + norm
 template <typename T>
 __global__ void __launch_bounds__(256) k_embed_norm(const T *embed, const int *tok, int d, const T *gain, float eps,
-                                                    float *h, T *xn) {
+                                                    float *h, T *xn, long long lo_off) {
     __shared__ float red[32];
     const int r = blockIdx.x;
     const T *e = embed + static_cast<long long>(tok[r]) * d;
@@ -40,31 +40,31 @@ __global__ void __launch_bounds__(256) k_embed_norm(const T *embed, const int *t
         ss += v * v;
     }
     const float inv = rsqrtf(block_sum<256>(ss, red) / d + eps);
-    for (int i = threadIdx.x; i < d; i += 256) xn[static_cast<long long>(r) * d + i] = from_f32<T>(hr[i] * inv * to_f32(gain[i]));
+    for (int i = threadIdx.x; i < d; i += 256)
+        store_act(xn, static_cast<long long>(r) * d + i, hr[i] * inv * to_f32(gain[i]), lo_off);
 }
 
 template <typename T>
 cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, const T *gain, float eps, float *h,
-                              T *xn, cudaStream_t s) {
-    k_embed_norm<T><<<nrows, 256, 0, s>>>(embed, tok, d, gain, eps, h, xn);
+                              T *xn, long long lo_off, cudaStream_t s) {
+    k_embed_norm<T><<<nrows, 256, 0, s>>>(embed, tok, d, gain, eps, h, xn, lo_off);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ qkv + rope + KV write
 // part: [S][nrows][ldp] with q | k | v columns.  Row r sits at position
 // P + depth[r] (P + r when depth is null) and its K/V go to cache slot P + r.
-template <typename T>
-__global__ void __launch_bounds__(128) k_qkv_rope(const float *part, int S, long long sstride, int ldp, int nh,
+// One thread per work item: a rotated (q or k) pair, or one v element.
+__global__ void __launch_bounds__(256) k_qkv_rope(const float *part, int S, long long sstride, int ldp, int nh,
                                                   int nkv, int hd, const float2 *rope, int P, const int *depth,
-                                                  float *q, T *kc, T *vc, int max_seq) {
-    const int r = blockIdx.x;
-    const int pos = P + (depth ? depth[r] : r);
+                                                  float *q, float *kc, float *vc, int max_seq) {
+    const int r = blockIdx.y;
+    const int t = blockIdx.x * 256 + threadIdx.x;
     const int half = hd / 2;
-    const float *pr = part + static_cast<long long>(r) * ldp;
-    const float2 *cs = rope + static_cast<long long>(pos) * half;
-    // q and k: rotate pairs (i, i + hd/2)
     const int nq_pairs = nh * half, nk_pairs = nkv * half;
-    for (int t = threadIdx.x; t < nq_pairs + nk_pairs; t += blockDim.x) {
+    const float *pr = part + static_cast<long long>(r) * ldp;
+    if (t < nq_pairs + nk_pairs) {
+        const int pos = P + (depth ? depth[r] : r);
         const bool isq = t < nq_pairs;
         const int tt = isq ? t : t - nq_pairs;
         const int head = tt / half, i = tt % half;
@@ -74,69 +74,98 @@ __global__ void __launch_bounds__(128) k_qkv_rope(const float *part, int S, long
             x1 += pr[sp * sstride + col];
             x2 += pr[sp * sstride + col + half];
         }
-        const float2 c = cs[i];
+        const float2 c = rope[static_cast<long long>(pos) * half + i];
         const float y1 = x1 * c.x - x2 * c.y, y2 = x1 * c.y + x2 * c.x;
         if (isq) {
             float *qr = q + (static_cast<long long>(r) * nh + head) * hd;
             qr[i] = y1;
             qr[i + half] = y2;
         } else {
-            T *kr = kc + (static_cast<long long>(head) * max_seq + P + r) * hd;
-            kr[i] = from_f32<T>(y1);
-            kr[i + half] = from_f32<T>(y2);
+            float *kr = kc + (static_cast<long long>(head) * max_seq + P + r) * hd;
+            kr[i] = y1;
+            kr[i + half] = y2;
         }
-    }
-    const int vcol0 = (nh + nkv) * hd;
-    for (int t = threadIdx.x; t < nkv * hd; t += blockDim.x) {
-        const int head = t / hd, i = t % hd;
+    } else if (t < nq_pairs + nk_pairs + nkv * hd) {
+        const int tv = t - nq_pairs - nk_pairs;
+        const int head = tv / hd, i = tv % hd;
+        const int col = (nh + nkv) * hd + tv;
         float v = 0.f;
-        for (int sp = 0; sp < S; ++sp) v += pr[sp * sstride + vcol0 + t];
-        vc[(static_cast<long long>(head) * max_seq + P + r) * hd + i] = from_f32<T>(v);
+        for (int sp = 0; sp < S; ++sp) v += pr[sp * sstride + col];
+        vc[(static_cast<long long>(head) * max_seq + P + r) * hd + i] = v;
     }
 }
 
-template <typename T>
 cudaError_t qkv_rope_launch(const float *part, int S, long long sstride, int ldp, int nrows, int nh, int nkv, int hd,
-                            const float2 *rope, int P, const int *depth, float *q, T *kc, T *vc, int max_seq,
+                            const float2 *rope, int P, const int *depth, float *q, float *kc, float *vc, int max_seq,
                             cudaStream_t s) {
-    k_qkv_rope<T><<<nrows, 128, 0, s>>>(part, S, sstride, ldp, nh, nkv, hd, rope, P, depth, q, kc, vc, max_seq);
+    const int items = (nh + nkv) * (hd / 2) + nkv * hd;
+    dim3 grid((items + 255) / 256, nrows);
+    k_qkv_rope<<<grid, 256, 0, s>>>(part, S, sstride, ldp, nh, nkv, hd, rope, P, depth, q, kc, vc, max_seq);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ residual + norm
 // Output row i reads residual row r = row_map[i] (or i): h[r] += sum_s part[s][r];
-// xout[i] = rmsnorm(h[r]) * gain.
+// xout[i] = rmsnorm(h[r]) * gain.  d % 4 == 0; float4 accesses, all loads of
+// a thread issued before the reduction.
 template <typename T>
-__global__ void __launch_bounds__(256) k_resid_norm(float *h, const float *part, int S, long long sstride, int ldp,
-                                                    int d, const T *gain, float eps, const int *row_map, T *xout) {
+__global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part, int S, long long sstride, int ldp,
+                                                     int d, const T *gain, float eps, const int *row_map, T *xout,
+                                                     long long lo_off) {
     __shared__ float red[32];
     const int i = blockIdx.x;
     const int r = row_map ? row_map[i] : i;
-    float *hr = h + static_cast<long long>(r) * d;
+    float4 *hr = reinterpret_cast<float4 *>(h + static_cast<long long>(r) * d);
     const float *pr = part + static_cast<long long>(r) * ldp;
+    const int d4 = d / 4;
+    constexpr int kMaxPer = 4;   // d <= 16384
+    float4 v[kMaxPer];
     float ss = 0.f;
-    for (int c = threadIdx.x; c < d; c += 256) {
-        float v = hr[c];
-        for (int sp = 0; sp < S; ++sp) v += pr[sp * sstride + c];
-        hr[c] = v;
-        ss += v * v;
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j) {
+        const int c = threadIdx.x + j * 1024;
+        if (c < d4) {
+            float4 a = hr[c];
+            for (int sp = 0; sp < S; ++sp) {
+                const float4 b = *reinterpret_cast<const float4 *>(pr + sp * sstride + 4 * c);
+                a.x += b.x;
+                a.y += b.y;
+                a.z += b.z;
+                a.w += b.w;
+            }
+            v[j] = a;
+            if (S > 0) hr[c] = a;
+            ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+        }
     }
-    const float inv = rsqrtf(block_sum<256>(ss, red) / d + eps);
-    T *xo = xout + static_cast<long long>(i) * d;
-    for (int c = threadIdx.x; c < d; c += 256) xo[c] = from_f32<T>(hr[c] * inv * to_f32(gain[c]));
+    const float inv = rsqrtf(block_sum<1024>(ss, red) / d + eps);
+    const long long o = static_cast<long long>(i) * d;
+#pragma unroll
+    for (int j = 0; j < kMaxPer; ++j) {
+        const int c = threadIdx.x + j * 1024;
+        if (c < d4) {
+            const float4 a = v[j];
+            store_act(xout, o + 4 * c + 0, a.x * inv * to_f32(gain[4 * c + 0]), lo_off);
+            store_act(xout, o + 4 * c + 1, a.y * inv * to_f32(gain[4 * c + 1]), lo_off);
+            store_act(xout, o + 4 * c + 2, a.z * inv * to_f32(gain[4 * c + 2]), lo_off);
+            store_act(xout, o + 4 * c + 3, a.w * inv * to_f32(gain[4 * c + 3]), lo_off);
+        }
+    }
 }
 
 template <typename T>
 cudaError_t resid_norm_launch(float *h, const float *part, int S, long long sstride, int ldp, int d, const T *gain,
-                              float eps, const int *row_map, int nrows, T *xout, cudaStream_t s) {
-    k_resid_norm<T><<<nrows, 256, 0, s>>>(h, part, S, sstride, ldp, d, gain, eps, row_map, xout);
+                              float eps, const int *row_map, int nrows, T *xout, long long lo_off, cudaStream_t s) {
+    if (d % 4 || d > 16384) return cudaErrorInvalidValue;
+    k_resid_norm<T><<<nrows, 1024, 0, s>>>(h, part, S, sstride, ldp, d, gain, eps, row_map, xout, lo_off);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ SwiGLU
 // part columns: gate [0, F) | up [F, 2F).  out[r][f] = silu(gate) * up.
 template <typename T>
-__global__ void k_swiglu(const float *part, int S, long long sstride, int ldp, int nrows, int F, T *out) {
+__global__ void k_swiglu(const float *part, int S, long long sstride, int ldp, int nrows, int F, T *out,
+                         long long lo_off) {
     const long long n = static_cast<long long>(nrows) * F;
     for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
          t += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -147,17 +176,17 @@ __global__ void k_swiglu(const float *part, int S, long long sstride, int ldp, i
             g += pr[sp * sstride + f];
             u += pr[sp * sstride + F + f];
         }
-        out[t] = from_f32<T>(g / (1.f + expf(-g)) * u);
+        store_act(out, t, g / (1.f + expf(-g)) * u, lo_off);
     }
 }
 
 template <typename T>
 cudaError_t swiglu_launch(const float *part, int S, long long sstride, int ldp, int nrows, int F, T *out,
-                          cudaStream_t s) {
+                          long long lo_off, cudaStream_t s) {
     const long long n = static_cast<long long>(nrows) * F;
     int blocks = static_cast<int>((n + 255) / 256);
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    k_swiglu<T><<<blocks, 256, 0, s>>>(part, S, sstride, ldp, nrows, F, out);
+    if (blocks > 152 * 64) blocks = 152 * 64;
+    k_swiglu<T><<<blocks, 256, 0, s>>>(part, S, sstride, ldp, nrows, F, out, lo_off);
     return cudaGetLastError();
 }
 
@@ -234,12 +263,10 @@ cudaError_t argmax_launch(const float *logits, int rows, int V, float invT, int 
 
 #define LA_INST(T)                                                                                                   \
     template cudaError_t embed_norm_launch<T>(const T *, const int *, int, int, const T *, float, float *, T *,       \
-                                              cudaStream_t);                                                         \
-    template cudaError_t qkv_rope_launch<T>(const float *, int, long long, int, int, int, int, int, const float2 *,   \
-                                            int, const int *, float *, T *, T *, int, cudaStream_t);                 \
+                                              long long, cudaStream_t);                                              \
     template cudaError_t resid_norm_launch<T>(float *, const float *, int, long long, int, int, const T *, float,    \
-                                              const int *, int, T *, cudaStream_t);                                  \
-    template cudaError_t swiglu_launch<T>(const float *, int, long long, int, int, int, T *, cudaStream_t);
+                                              const int *, int, T *, long long, cudaStream_t);                       \
+    template cudaError_t swiglu_launch<T>(const float *, int, long long, int, int, int, T *, long long, cudaStream_t);
 LA_INST(float)
 LA_INST(__nv_bfloat16)
 #undef LA_INST

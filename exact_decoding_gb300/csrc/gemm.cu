@@ -108,15 +108,34 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
             const int f = row0 + 32 * q + lane;
             const bool fv = f < p.seg_out[seg];
             float *out = p.out + static_cast<long long>(split) * p.split_stride + p.seg_col0[seg] + f;
-            for (int c0 = 0; c0 < bn; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c0), r);
-                tmem_ld_wait();
-                if (fv) {
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+            if (p.bh > 0) {
+                // columns c (hi rows) + columns c + bh (lo rows) = one output row
+                for (int c0 = 0; c0 < p.bh; c0 += 32) {
+                    uint32_t r[32], s2[32];
+                    tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0), r);
+                    tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0 + p.bh), s2);
+                    tmem_ld_wait();
+                    if (fv) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int row = c0 + j;
-                        if (row < p.nrows) out[static_cast<long long>(row) * p.ldo] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 32; ++j) {
+                            const int row = c0 + j;
+                            if (row < p.nrows)
+                                out[static_cast<long long>(row) * p.ldo] = __uint_as_float(r[j]) + __uint_as_float(s2[j]);
+                        }
+                    }
+                }
+            } else {
+                for (int c0 = 0; c0 < bn; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0), r);
+                    tmem_ld_wait();
+                    if (fv) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int row = c0 + j;
+                            if (row < p.nrows) out[static_cast<long long>(row) * p.ldo] = __uint_as_float(r[j]);
+                        }
                     }
                 }
             }
@@ -166,21 +185,18 @@ int tc_gemm_ctas_per_sm(int bn, int stages) {
 }
 
 int choose_splits(int tiles, int n_kb, int slots) {
-    // Minimise waves/split with a small charge per split for the partial
-    // traffic; keep >= 4 k-blocks (256 K) per CTA.
-    int best = 1;
-    double best_cost = 1e30;
-    for (int s = 1; s <= 16; ++s) {
-        if (s > 1 && n_kb / s < 4) break;
-        const int ctas = tiles * s;
-        const int waves = (ctas + slots - 1) / slots;
-        const double cost = static_cast<double>(waves) / s * (1.0 + 0.04 * s);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = s;
-        }
-    }
-    return best;
+    // The GEMM is bound by HBM, not by waves: it needs every SM streaming,
+    // not every CTA slot filled.  Take the fewest K-splits that put at least
+    // one CTA on (nearly) every SM, since each split adds S x rows x out fp32
+    // partials that the consumer kernel must read back.  Keep >= 4 k-blocks
+    // (256 K) per CTA.
+    int nsm = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        nsm = 148;
+    (void)slots;
+    int s = 1;
+    while (tiles * s < (nsm * 9) / 10 && n_kb / (s + 1) >= 4 && s < 16) ++s;
+    return s;
 }
 
 void tc_gemm_finalize(TcGemm &g) {

@@ -13,6 +13,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/la.h"
 #include "la_kernels.h"
 
@@ -58,7 +60,10 @@ struct la_handle {
     int L = 0, d = 0, nh = 0, nkv = 0, hd = 0, F = 0, V = 0, qd = 0, kvd = 0, qkv_out = 0;
     int N = 0, W = 0, G = 0, M = 0, U = 0, cap = 0, max_seq = 0, R = 0;
     int bn_step = 0, bn_pf = 0, bn_u = 0;
-    size_t act = 4;   // bytes per activation element
+    // bf16 models: GEMM inputs are bf16 hi/lo planes, hi rows [0, bh), lo rows [bh, 2 bh)
+    int bh_step = 0, bh_pf = 0, bh_u = 0;
+    int act_rows = 0;   // rows of each activation buffer
+    size_t act = 4;     // bytes per activation element
 
     // caller's weights
     const void *embed = nullptr, *final_norm = nullptr, *lm_head = nullptr;
@@ -72,6 +77,7 @@ struct la_handle {
     float2 *rope = nullptr;
     int *amax = nullptr, *tok = nullptr, *depth = nullptr, *anc = nullptr, *anc_cnt = nullptr, *used = nullptr;
     int *iota = nullptr;
+    uint32_t *vis_bits = nullptr;   // [M][8] in-step visibility bits
     int anc_stride = 0;
     SpecState *st = nullptr;
     SpecState *st_host = nullptr;   // pinned
@@ -192,10 +198,12 @@ struct la_handle {
         ev_used = 0;
     }
 
-    void *kv_layer(int l, int which) const {
-        const size_t plane = static_cast<size_t>(nkv) * max_seq * hd * act;
-        return static_cast<char *>(cache) + (static_cast<size_t>(l) * 2 + which) * plane;
+    // K (which = 0) or V (1) cache of layer l: fp32 [nkv][max_seq][hd].
+    float *kv_layer(int l, int which) const {
+        const size_t plane = static_cast<size_t>(nkv) * max_seq * hd;
+        return static_cast<float *>(cache) + (static_cast<size_t>(l) * 2 + which) * plane;
     }
+    int bh(int mode) const { return mode == 0 ? bh_step : bh_pf; }
 };
 
 namespace {
@@ -232,7 +240,8 @@ uint64_t splitmix64(uint64_t x) {
 double gemm_bytes(const la_handle *h, Kind kind, int nrows) {
     const int K = kind == OPROJ ? h->qd : kind == DOWN ? h->F : h->d;
     const int out = kind == QKV ? h->qkv_out : kind == GATEUP ? 2 * h->F : h->d;
-    return (static_cast<double>(out) * K + static_cast<double>(nrows) * K) * h->act + 4.0 * nrows * out;
+    // weights once + input rows (fp32, or its bf16 hi/lo pair) + fp32 output
+    return static_cast<double>(out) * K * h->act + 4.0 * nrows * K + 4.0 * nrows * out;
 }
 
 int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
@@ -294,8 +303,7 @@ int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
 int run_lm_head(la_handle *h, int nrows, bool step) {
     h->launches += 1;
     const int pe = step ? h->prof_begin() : -1;
-    const double bytes = (static_cast<double>(h->V) * h->d + static_cast<double>(nrows) * h->d) * h->act +
-                         4.0 * nrows * h->V;
+    const double bytes = static_cast<double>(h->V) * h->d * h->act + 4.0 * nrows * h->d + 4.0 * nrows * h->V;
     if (h->bf16) {
         TcGemm g = h->plan_lm;
         g.p.nrows = nrows;
@@ -331,17 +339,18 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
     cudaStream_t s = h->stream;
     const float eps = h->dims.rms_eps;
     h->launches += 1;
+    const long long bh = h->bh(mode);
     CK(embed_norm_launch<T>(static_cast<const T *>(h->embed), tok, nrows, h->d,
-                            static_cast<const T *>(h->attn_norm[0]), eps, h->h, static_cast<T *>(h->xn), s));
+                            static_cast<const T *>(h->attn_norm[0]), eps, h->h, static_cast<T *>(h->xn), bh * h->d,
+                            s));
     const int nch = (P + kAttnChunk - 1) / kAttnChunk;
     for (int l = 0; l < h->L; ++l) {
         int rc;
         if ((rc = run_gemm(h, mode, QKV, l, nrows)) != LA_OK) return rc;
         const long long ss_qkv = static_cast<long long>(h->R) * h->qkv_out;
-        CK(qkv_rope_launch<T>(h->part, h->splits[mode][QKV], ss_qkv, h->qkv_out, nrows, h->nh, h->nkv, h->hd,
-                              h->rope, P, mode == STEP ? h->depth : nullptr, h->q,
-                              static_cast<T *>(h->kv_layer(l, 0)), static_cast<T *>(h->kv_layer(l, 1)),
-                              h->max_seq, s));
+        CK(qkv_rope_launch(h->part, h->splits[mode][QKV], ss_qkv, h->qkv_out, nrows, h->nh, h->nkv, h->hd, h->rope,
+                           P, mode == STEP ? h->depth : nullptr, h->q, h->kv_layer(l, 0), h->kv_layer(l, 1),
+                           h->max_seq, s));
         AttnArgs a{};
         a.q = h->q;
         a.kc = h->kv_layer(l, 0);
@@ -357,34 +366,35 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         a.anc = mode == STEP ? h->anc : nullptr;
         a.anc_cnt = mode == STEP ? h->anc_cnt : nullptr;
         a.anc_stride = h->anc_stride;
+        a.vis_bits = mode == STEP ? h->vis_bits : nullptr;
         a.out = h->ao;
+        a.out_lo_off = bh * h->qd;
         const int pe = mode == STEP ? h->prof_begin() : -1;
         CK(attention_launch<T>(a, s));
         h->prof_end(pe, 1,
-                    (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * h->act + 4.0 * nrows * h->qd +
-                        static_cast<double>(nrows) * h->qd * h->act);
-        h->launches += 2 + (nch > 0 ? 1 : 0);   // qkv_rope, attention passes
+                    (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * 4.0 + 4.0 * nrows * h->qd + 4.0 * nrows * h->qd);
+        h->launches += 1 + (h->bf16 ? 2 : 1 + (nch > 0 ? 1 : 0));   // qkv_rope, attention passes
         if ((rc = run_gemm(h, mode, OPROJ, l, nrows)) != LA_OK) return rc;
         const long long ss_d = static_cast<long long>(h->R) * h->d;
         CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][OPROJ], ss_d, h->d, h->d,
                                 static_cast<const T *>(h->ffn_norm[l]), eps, nullptr, nrows,
-                                static_cast<T *>(h->xn), s));
+                                static_cast<T *>(h->xn), bh * h->d, s));
         if ((rc = run_gemm(h, mode, GATEUP, l, nrows)) != LA_OK) return rc;
         const long long ss_gu = static_cast<long long>(h->R) * 2 * h->F;
         CK(swiglu_launch<T>(h->part, h->splits[mode][GATEUP], ss_gu, 2 * h->F, nrows, h->F,
-                            static_cast<T *>(h->fa), s));
+                            static_cast<T *>(h->fa), bh * h->F, s));
         h->launches += 3;   // resid_norm after O, swiglu, resid_norm after down
         if ((rc = run_gemm(h, mode, DOWN, l, nrows)) != LA_OK) return rc;
         if (l + 1 < h->L) {
             CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][DOWN], ss_d, h->d, h->d,
                                     static_cast<const T *>(h->attn_norm[l + 1]), eps, nullptr, nrows,
-                                    static_cast<T *>(h->xn), s));
+                                    static_cast<T *>(h->xn), bh * h->d, s));
         } else if (want_logits) {
             const int *map = mode == STEP ? h->used : h->iota + (nrows - 1);
             const int rows = mode == STEP ? h->U : 1;
             CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][DOWN], ss_d, h->d, h->d,
                                     static_cast<const T *>(h->final_norm), eps, map, rows,
-                                    static_cast<T *>(h->xu), s));
+                                    static_cast<T *>(h->xu), static_cast<long long>(h->bh_u) * h->d, s));
         }
     }
     return LA_OK;
@@ -396,11 +406,7 @@ int forward_any(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool 
 }
 
 int kv_commit(la_handle *h) {
-    if (h->bf16)
-        CK(kv_commit_launch<__nv_bfloat16>(h->spec(), static_cast<__nv_bfloat16 *>(h->cache), h->L, h->nkv, h->hd,
-                                           h->stream));
-    else
-        CK(kv_commit_launch<float>(h->spec(), static_cast<float *>(h->cache), h->L, h->nkv, h->hd, h->stream));
+    CK(kv_commit_launch(h->spec(), static_cast<float *>(h->cache), h->L, h->nkv, h->hd, h->stream));
     return LA_OK;
 }
 
@@ -443,14 +449,15 @@ int build_plans(la_handle *h) {
     CK(cudaGetDevice(&dev));
     int nsm = 0;
     CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-    const int bns[2] = {h->bn_step, h->bn_pf};
+    const int bhs[2] = {h->bh_step, h->bh_pf};
     void *xs[2][4] = {{h->xn, h->ao, h->xn, h->fa}, {h->xn, h->ao, h->xn, h->fa}};
     const int Ks[4] = {h->d, h->qd, h->d, h->F};
     const int ldos[4] = {h->qkv_out, h->d, 2 * h->F, h->d};
     size_t part_max = 0;
     for (int mode = 0; mode < 2; ++mode) {
-        const int bn = bns[mode];
-        const int rows_map = mode == STEP ? h->M : kPrefillRows;
+        const int bhm = bhs[mode];
+        const int bn = 2 * bhm;             // hi rows + lo rows
+        const int rows_map = bn;
         const int stages = tc_gemm_stages_for(bn);
         const int slots = nsm * tc_gemm_ctas_per_sm(bn, stages);
         for (int kind = 0; kind < 4; ++kind) {
@@ -507,8 +514,9 @@ int build_plans(la_handle *h) {
                 g.p.nseg = nseg;
                 g.p.n_kb = n_kb;
                 g.p.splits = S;
-                g.p.nrows = rows_map;
+                g.p.nrows = mode == STEP ? h->M : kPrefillRows;
                 g.p.bn = bn;
+                g.p.bh = bhm;
                 g.p.ldo = ldos[kind];
                 g.p.stages = stages;
                 g.p.split_stride = static_cast<long long>(h->R) * ldos[kind];
@@ -522,9 +530,9 @@ int build_plans(la_handle *h) {
     {
         TcGemm &g = h->plan_lm;
         std::memset(&g.p, 0, sizeof(g.p));
-        const int bn = h->bn_u;
+        const int bn = 2 * h->bh_u;
         if (make_tmap_bf16(&g.p.a[0], h->lm_head, h->d, h->V, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM) ||
-            make_tmap_bf16(&g.p.b, h->xu, h->d, h->U, static_cast<uint64_t>(h->d) * 2, kBlockK, bn))
+            make_tmap_bf16(&g.p.b, h->xu, h->d, bn, static_cast<uint64_t>(h->d) * 2, kBlockK, bn))
             return fail(LA_ERR_INVALID_ARG, "tensor map for lm_head failed");
         g.p.nseg = 1;
         g.p.seg_tile0[0] = 0;
@@ -535,6 +543,7 @@ int build_plans(la_handle *h) {
         g.p.splits = 1;
         g.p.nrows = h->U;
         g.p.bn = bn;
+        g.p.bh = h->bh_u;
         g.p.ldo = h->V;
         g.p.stages = tc_gemm_stages_for(bn);
         g.p.split_stride = 0;
@@ -566,6 +575,8 @@ const char *la_strerror(int code) {
 }
 
 const char *la_last_error(void) { return g_last_error.c_str(); }
+
+static int la_prefill_impl(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token);
 
 int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opts, la_handle **out) {
     if (!dims || !w || !opts || !out) return fail(LA_ERR_INVALID_ARG, "null argument");
@@ -617,6 +628,14 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     h->bn_step = round_up(M, 16);
     h->bn_pf = kPrefillRows;
     h->bn_u = round_up(h->U, 16);
+    h->bh_step = round_up(M, 32);
+    h->bh_pf = kPrefillRows;
+    h->bh_u = round_up(h->U, 32);
+    h->act_rows = h->bf16 ? 2 * kPrefillRows : h->R;
+    if (h->bf16 && M > kPrefillRows) {
+        delete h;
+        return fail(LA_ERR_UNSUPPORTED, "bf16 models need 1 + (W+G)(N-1) <= 128");
+    }
     h->embed = w->embed;
     h->final_norm = w->final_norm;
     h->lm_head = w->lm_head;
@@ -645,24 +664,26 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     const size_t act = h->act;
     const int R = h->R;
     A(h->alloc(&h->h, static_cast<size_t>(R) * h->d));
-    A(h->alloc_bytes(&h->xn, static_cast<size_t>(R) * h->d * act));
-    A(h->alloc_bytes(&h->ao, static_cast<size_t>(R) * h->qd * act));
-    A(h->alloc_bytes(&h->fa, static_cast<size_t>(R) * h->F * act));
-    A(h->alloc_bytes(&h->xu, static_cast<size_t>(std::max(h->U, 16)) * h->d * act));
+    const size_t ar = static_cast<size_t>(h->act_rows);
+    A(h->alloc_bytes(&h->xn, ar * h->d * act));
+    A(h->alloc_bytes(&h->ao, ar * h->qd * act));
+    A(h->alloc_bytes(&h->fa, ar * h->F * act));
+    A(h->alloc_bytes(&h->xu, ar * h->d * act));
     A(h->alloc(&h->q, static_cast<size_t>(R) * h->qd));
     A(h->alloc(&h->logits, static_cast<size_t>(std::max(h->U, 1)) * h->V));
     A(h->alloc(&h->amax, std::max(h->U, 1)));
     A(h->alloc(&h->lmax, std::max(h->U, 1)));
     A(h->alloc(&h->lsum, std::max(h->U, 1)));
-    const int nch_max = (h->max_seq + kAttnChunk - 1) / kAttnChunk;
+    const int nch_max = std::max((h->max_seq + kAttnChunk - 1) / kAttnChunk, attention_tc_chunks(h->max_seq, R));
     A(h->alloc(&h->attn_ws, static_cast<size_t>(nch_max) * R * h->nh * (h->hd + 4)));
-    A(h->alloc_bytes(&h->cache, static_cast<size_t>(h->L) * 2 * h->nkv * h->max_seq * h->hd * act));
+    A(h->alloc_bytes(&h->cache, static_cast<size_t>(h->L) * 2 * h->nkv * h->max_seq * h->hd * sizeof(float)));
     A(h->alloc(&h->rope, static_cast<size_t>(h->max_seq) * (h->hd / 2)));
     A(h->alloc(&h->tok, M));
     A(h->alloc(&h->depth, M));
     h->anc_stride = h->N + h->W;
     A(h->alloc(&h->anc, static_cast<size_t>(M) * h->anc_stride));
     A(h->alloc(&h->anc_cnt, M));
+    A(h->alloc(&h->vis_bits, static_cast<size_t>(M) * 8));
     A(h->alloc(&h->used, h->U));
     A(h->alloc(&h->iota, R));
     A(h->alloc(&h->st, 1));
@@ -704,6 +725,12 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
             cnt[r] = static_cast<int>(chain.size());
             for (size_t i = 0; i < chain.size(); ++i) anc[static_cast<size_t>(r) * h->anc_stride + i] = chain[i];
         }
+        std::vector<uint32_t> bits(static_cast<size_t>(M) * 8, 0u);
+        for (int r = 0; r < M; ++r)
+            for (int i = 0; i < cnt[r]; ++i) {
+                const int a = anc[static_cast<size_t>(r) * h->anc_stride + i];
+                bits[static_cast<size_t>(r) * 8 + a / 32] |= 1u << (a % 32);
+            }
         std::vector<int> used;
         used.push_back(0);
         for (int j = 0; j < h->W; ++j) used.push_back(1 + (h->N - 2) * h->W + j);
@@ -715,6 +742,7 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
             cudaMemcpy(h->depth, depth.data(), M * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
             cudaMemcpy(h->anc, anc.data(), anc.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
             cudaMemcpy(h->anc_cnt, cnt.data(), M * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+            cudaMemcpy(h->vis_bits, bits.data(), bits.size() * sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
             cudaMemcpy(h->used, used.data(), used.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
             cudaMemcpy(h->iota, iota.data(), R * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
             delete h;
@@ -722,10 +750,10 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         }
     }
     // Zero activations once so padded rows never hold NaN bit patterns.
-    if (cudaMemsetAsync(h->xn, 0, static_cast<size_t>(R) * h->d * act, s) != cudaSuccess ||
-        cudaMemsetAsync(h->ao, 0, static_cast<size_t>(R) * h->qd * act, s) != cudaSuccess ||
-        cudaMemsetAsync(h->fa, 0, static_cast<size_t>(R) * h->F * act, s) != cudaSuccess ||
-        cudaMemsetAsync(h->xu, 0, static_cast<size_t>(std::max(h->U, 16)) * h->d * act, s) != cudaSuccess ||
+    if (cudaMemsetAsync(h->xn, 0, ar * h->d * act, s) != cudaSuccess ||
+        cudaMemsetAsync(h->ao, 0, ar * h->qd * act, s) != cudaSuccess ||
+        cudaMemsetAsync(h->fa, 0, ar * h->F * act, s) != cudaSuccess ||
+        cudaMemsetAsync(h->xu, 0, ar * h->d * act, s) != cudaSuccess ||
         cudaMemsetAsync(h->st, 0, sizeof(SpecState), s) != cudaSuccess) {
         delete h;
         return fail(LA_ERR_CUDA, "memset failed");
@@ -759,6 +787,13 @@ void la_destroy(la_handle *h) {
 }
 
 int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token) {
+    nvtxRangePushA("la_prefill");
+    const int rc = la_prefill_impl(h, prompt, n, first_token);
+    nvtxRangePop();
+    return rc;
+}
+
+static int la_prefill_impl(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token) {
     if (!h || !prompt || !first_token) return fail(LA_ERR_INVALID_ARG, "null argument");
     if (n < h->N) return fail(LA_ERR_INVALID_ARG, "prompt shorter than N");
     if (n + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "prompt too long for max_seq");
@@ -797,7 +832,15 @@ int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_to
     return LA_OK;
 }
 
+namespace {
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
+
 int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
+    NvtxRange range("la_step");
     if (!h || !out_tokens || !out_n) return fail(LA_ERR_INVALID_ARG, "null argument");
     if (!h->prefilled) return fail(LA_ERR_STATE, "la_step before la_prefill");
     if (h->P + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "max_seq reached");

@@ -34,6 +34,16 @@ template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
+// Activation stores.  fp32 models keep fp32 activations.  bf16 models feed
+// the tensor cores a pair of bf16 planes (hi, lo) with x = hi + lo to about
+// 16 mantissa bits; the lo plane sits `lo_off` elements after the hi plane.
+__device__ __forceinline__ void store_act(float *p, long long i, float v, long long) { p[i] = v; }
+__device__ __forceinline__ void store_act(__nv_bfloat16 *p, long long i, float v, long long lo_off) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    p[i] = hi;
+    p[i + lo_off] = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -22,8 +22,10 @@ struct TcGemmParams {
     int seg_col0[kMaxSeg];       // column of the segment's first feature in the output row
     int n_kb;                    // K / 64 rounded up
     int splits;                  // k-splits (CTAs per tile)
-    int nrows;                   // rows stored (<= bn)
+    int nrows;                   // rows stored (<= bn, <= bh when bh > 0)
     int bn;                      // UMMA N: padded rows, multiple of 16, <= 256
+    int bh;                      // > 0: B holds hi rows [0, bh) and lo rows [bh, 2bh) = bn; the
+                                 //      epilogue adds columns c and c + bh.  0: plain bf16 rows
     int ldo;                     // output row stride (floats)
     int stages;                  // shared-memory pipeline depth
     long long split_stride;      // floats between split partials
@@ -72,19 +74,21 @@ cudaError_t reduce_splits_launch(const float *part, int splits, long long stride
                                  cudaStream_t s);
 
 // ------------------------------------------------------------------ elementwise
+// T is the weight type; activations written as T go through store_act
+// (fp32, or a bf16 hi/lo pair whose lo plane is lo_off elements later).
 template <typename T>
 cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, const T *gain, float eps, float *h,
-                              T *xn, cudaStream_t s);
-template <typename T>
+                              T *xn, long long lo_off, cudaStream_t s);
+// Rotated q (fp32) and the rows' K/V into the fp32 cache at slots P + r.
 cudaError_t qkv_rope_launch(const float *part, int S, long long sstride, int ldp, int nrows, int nh, int nkv, int hd,
-                            const float2 *rope, int P, const int *depth, float *q, T *kc, T *vc, int max_seq,
+                            const float2 *rope, int P, const int *depth, float *q, float *kc, float *vc, int max_seq,
                             cudaStream_t s);
 template <typename T>
 cudaError_t resid_norm_launch(float *h, const float *part, int S, long long sstride, int ldp, int d, const T *gain,
-                              float eps, const int *row_map, int nrows, T *xout, cudaStream_t s);
+                              float eps, const int *row_map, int nrows, T *xout, long long lo_off, cudaStream_t s);
 template <typename T>
 cudaError_t swiglu_launch(const float *part, int S, long long sstride, int ldp, int nrows, int F, T *out,
-                          cudaStream_t s);
+                          long long lo_off, cudaStream_t s);
 cudaError_t argmax_launch(const float *logits, int rows, int V, float invT, int *amax, float *lmax, float *lsum,
                           cudaStream_t s);
 
@@ -94,19 +98,27 @@ cudaError_t argmax_launch(const float *logits, int rows, int V, float invT, int 
 // in causal mode (anc == nullptr) they are rows 0..r.
 struct AttnArgs {
     const float *q;        // [nrows][nh][hd] fp32 (rotated)
-    const void *kc;        // this layer's K cache [nkv][max_seq][hd]
-    const void *vc;        // V cache, same layout
+    const float *kc;       // this layer's K cache [nkv][max_seq][hd], fp32
+    const float *vc;       // V cache, same layout
     int max_seq, P, nrows, nh, nkv, hd;
     float *ws;             // prefix partials [nch][nrows][nh][hd + 4] (out, max, sum, pad)
     int nch;               // prefix chunks = ceil(P / kAttnChunk)
     const int *anc;        // [nrows][anc_stride] or nullptr
     const int *anc_cnt;
     int anc_stride;
-    void *out;             // [nrows][nh * hd] activations
+    const uint32_t *vis_bits;  // [nrows][8] in-step visibility bits (tree mode) or nullptr (causal)
+    void *out;             // [nrows][nh * hd] activations (store_act form)
+    long long out_lo_off;  // lo plane offset of `out` (bf16 models)
 };
 constexpr int kAttnChunk = 64;
+// fp32 models: SIMT split-KV (64-key chunks) + per-row in-step pass.
+// bf16 models: tensor-core chunks of 128 keys (prefix and in-step) + merge.
 template <typename T>
 cudaError_t attention_launch(const AttnArgs &a, cudaStream_t s);
+template <>
+cudaError_t attention_launch<__nv_bfloat16>(const AttnArgs &a, cudaStream_t s);
+// Partial records the bf16 path writes for prefix length P and nrows rows.
+int attention_tc_chunks(int P, int nrows);
 
 // ------------------------------------------------------------------ speculation state
 struct SpecState {
@@ -143,8 +155,7 @@ struct SpecDev {
 
 cudaError_t build_rows_launch(const SpecDev &d, cudaStream_t s);
 cudaError_t finish_step_launch(const SpecDev &d, cudaStream_t s);
-template <typename T>
-cudaError_t kv_commit_launch(const SpecDev &d, T *cache, int L, int nkv, int hd, cudaStream_t s);
+cudaError_t kv_commit_launch(const SpecDev &d, float *cache, int L, int nkv, int hd, cudaStream_t s);
 // Insert n records [n][N] (key, suffix) in order, one warp, sequential semantics.
 cudaError_t pool_insert_launch(const SpecDev &d, const int *records, int n, cudaStream_t s);
 // Insert the prompt's n-grams (tokens_log[0..n)) in ascending start position.

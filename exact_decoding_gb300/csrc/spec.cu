@@ -365,13 +365,12 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
 
 // Copy K/V of the winning candidate's rows m = 1..A-1 (slot P_old + its row)
 // to slots P_old + m.  Row 0 already sits at P_old.
-template <typename T>
-__global__ void k_kv_commit(SpecDev d, T *cache, int nkv, int hd) {
+__global__ void k_kv_commit(SpecDev d, float *cache, int nkv, int hd) {
     const int A = d.st->A, cs = d.st->cstar, P0 = d.st->P_old;
     if (A <= 1 || cs < 0) return;
     const int L = d.N - 1;
     const long long plane = static_cast<long long>(blockIdx.x);   // (layer, k|v, kv head)
-    T *base = cache + plane * d.max_seq * hd;
+    float *base = cache + plane * d.max_seq * hd;
     for (int t = threadIdx.x; t < (A - 1) * hd; t += blockDim.x) {
         const int m = 1 + t / hd, i = t % hd;
         const int src = P0 + 1 + L * d.W + cs * L + (m - 1);
@@ -420,13 +419,10 @@ cudaError_t finish_step_launch(const SpecDev &d, cudaStream_t s) {
     k_finish_step<<<1, kFinishThreads, 0, s>>>(d);
     return cudaGetLastError();
 }
-template <typename T>
-cudaError_t kv_commit_launch(const SpecDev &d, T *cache, int L, int nkv, int hd, cudaStream_t s) {
-    k_kv_commit<T><<<L * 2 * nkv, 128, 0, s>>>(d, cache, nkv, hd);
+cudaError_t kv_commit_launch(const SpecDev &d, float *cache, int L, int nkv, int hd, cudaStream_t s) {
+    k_kv_commit<<<L * 2 * nkv, 128, 0, s>>>(d, cache, nkv, hd);
     return cudaGetLastError();
 }
-template cudaError_t kv_commit_launch<float>(const SpecDev &, float *, int, int, int, cudaStream_t);
-template cudaError_t kv_commit_launch<__nv_bfloat16>(const SpecDev &, __nv_bfloat16 *, int, int, int, cudaStream_t);
 
 cudaError_t pool_insert_launch(const SpecDev &d, const int *records, int n, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
