@@ -21,6 +21,8 @@ namespace la {
 template <typename T, int HD>
 __global__ void __launch_bounds__(256) k_attn_prefix(const float *q, const T *kc, const T *vc, int max_seq, int P,
                                                      int nrows, int nh, int nkv, float *ws) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int CH = kAttnChunk;
     constexpr int KT = CH + 4;      // Kt row stride (floats), keeps float4 alignment
     constexpr int QS = HD + 1;      // Qs row stride
@@ -145,6 +147,8 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(256) k_attn_final(const float *q, const T *kc, const T *vc, int max_seq, int P,
                                                     int nrows, int nh, int nkv, const float *ws, int nch,
                                                     const int *anc, const int *anc_cnt, int anc_stride, T *out) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int DPL = HD / 32;   // dims per lane
     const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -209,13 +213,13 @@ static cudaError_t attention_launch_hd(const AttnArgs &a, cudaStream_t s) {
             configured = true;
         }
         dim3 grid(a.nkv, a.nch);
-        k_attn_prefix<T, HD><<<grid, 256, smem, s>>>(a.q, a.kc, a.vc,
+        launch_k(k_attn_prefix<T, HD>, dim3(grid), dim3(256), smem, s, a.q, a.kc, a.vc,
                                                      a.max_seq, a.P, a.nrows, a.nh, a.nkv, a.ws);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     const int warps = a.nrows * a.nh;
-    k_attn_final<T, HD><<<(warps + 7) / 8, 256, 0, s>>>(a.q, a.kc, a.vc, a.max_seq, a.P, a.nrows, a.nh,
+    launch_k(k_attn_final<T, HD>, dim3((warps + 7) / 8), dim3(256), 0, s, a.q, a.kc, a.vc, a.max_seq, a.P, a.nrows, a.nh,
                                                          a.nkv, a.ws, a.nch, a.anc, a.anc_cnt, a.anc_stride,
                                                          static_cast<T *>(a.out));
     return cudaGetLastError();
@@ -278,6 +282,8 @@ template <int HD>
 __global__ void __launch_bounds__(128) k_attn_tc(const float *q, const float *kc, const float *vc, int max_seq, int P,
                                                  int nrows, int nh, int nkv, int nch_prefix, const uint32_t *vis_bits,
                                                  float *ws) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int LD = HD + 8;   // smem row stride (bf16): 16-byte aligned rows, conflict-free ldmatrix
     extern __shared__ __align__(16) __nv_bfloat16 smb[];
     __nv_bfloat16 *Kh = smb;                     // [kTcChunk][LD] each
@@ -461,6 +467,8 @@ __global__ void __launch_bounds__(128) k_attn_tc(const float *q, const float *kc
 template <int HD>
 __global__ void __launch_bounds__(256) k_attn_merge(const float *ws, int nch, int nrows, int nh, __nv_bfloat16 *out,
                                                     long long lo_off) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int DPL = HD / 32;
     const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -502,12 +510,12 @@ cudaError_t attention_tc_hd(const AttnArgs &a, cudaStream_t s) {
         configured = true;
     }
     dim3 grid(a.nkv, nch, (a.nrows * gq + kTcQ - 1) / kTcQ);
-    k_attn_tc<HD><<<grid, 128, smem, s>>>(a.q, a.kc, a.vc, a.max_seq, a.P, a.nrows, a.nh, a.nkv, nch_prefix,
+    launch_k(k_attn_tc<HD>, dim3(grid), dim3(128), smem, s, a.q, a.kc, a.vc, a.max_seq, a.P, a.nrows, a.nh, a.nkv, nch_prefix,
                                           a.vis_bits, a.ws);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int warps = a.nrows * a.nh;
-    k_attn_merge<HD><<<(warps + 7) / 8, 256, 0, s>>>(a.ws, nch, a.nrows, a.nh, static_cast<__nv_bfloat16 *>(a.out),
+    launch_k(k_attn_merge<HD>, dim3((warps + 7) / 8), dim3(256), 0, s, a.ws, nch, a.nrows, a.nh, static_cast<__nv_bfloat16 *>(a.out),
                                                      a.out_lo_off);
     return cudaGetLastError();
 }

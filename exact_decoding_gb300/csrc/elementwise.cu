@@ -29,6 +29,8 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 template <typename T>
 __global__ void __launch_bounds__(256) k_embed_norm(const T *embed, const int *tok, int d, const T *gain, float eps,
                                                     float *h, T *xn, long long lo_off) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[32];
     const int r = blockIdx.x;
     const T *e = embed + static_cast<long long>(tok[r]) * d;
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(256) k_embed_norm(const T *embed, const int *t
 template <typename T>
 cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, const T *gain, float eps, float *h,
                               T *xn, long long lo_off, cudaStream_t s) {
-    k_embed_norm<T><<<nrows, 256, 0, s>>>(embed, tok, d, gain, eps, h, xn, lo_off);
+    launch_k(k_embed_norm<T>, dim3(nrows), dim3(256), 0, s, embed, tok, d, gain, eps, h, xn, lo_off);
     return cudaGetLastError();
 }
 
@@ -55,9 +57,19 @@ cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, 
 // part: [S][nrows][ldp] with q | k | v columns.  Row r sits at position
 // P + depth[r] (P + r when depth is null) and its K/V go to cache slot P + r.
 // One thread per work item: a rotated (q or k) pair, or one v element.
-__global__ void __launch_bounds__(256) k_qkv_rope(const float *part, int S, long long sstride, int ldp, int nh,
-                                                  int nkv, int hd, const float2 *rope, int P, const int *depth,
-                                                  float *q, float *kc, float *vc, int max_seq) {
+__device__ __forceinline__ float sum_planes(const float *pr, const int *planes, long long sstride, int col) {
+    const int n = planes ? planes[col >> 7] : 1;
+    float v = pr[col];
+    for (int sp = 1; sp < n; ++sp) v += pr[sp * sstride + col];
+    return v;
+}
+
+__global__ void __launch_bounds__(256) k_qkv_rope(const float *part, const int *planes, long long sstride, int ldp,
+                                                  int nh, int nkv, int hd, int k_off, int v_off, const float2 *rope,
+                                                  int P, const int *depth, float *q, float *kc, float *vc,
+                                                  int max_seq) {
+    pdl_trigger();
+    pdl_wait();
     const int r = blockIdx.y;
     const int t = blockIdx.x * 256 + threadIdx.x;
     const int half = hd / 2;
@@ -68,12 +80,9 @@ __global__ void __launch_bounds__(256) k_qkv_rope(const float *part, int S, long
         const bool isq = t < nq_pairs;
         const int tt = isq ? t : t - nq_pairs;
         const int head = tt / half, i = tt % half;
-        const int col = (isq ? 0 : nh * hd) + head * hd + i;
-        float x1 = 0.f, x2 = 0.f;
-        for (int sp = 0; sp < S; ++sp) {
-            x1 += pr[sp * sstride + col];
-            x2 += pr[sp * sstride + col + half];
-        }
+        const int col = (isq ? 0 : k_off) + head * hd + i;
+        const float x1 = sum_planes(pr, planes, sstride, col);
+        const float x2 = sum_planes(pr, planes, sstride, col + half);
         const float2 c = rope[static_cast<long long>(pos) * half + i];
         const float y1 = x1 * c.x - x2 * c.y, y2 = x1 * c.y + x2 * c.x;
         if (isq) {
@@ -88,19 +97,18 @@ __global__ void __launch_bounds__(256) k_qkv_rope(const float *part, int S, long
     } else if (t < nq_pairs + nk_pairs + nkv * hd) {
         const int tv = t - nq_pairs - nk_pairs;
         const int head = tv / hd, i = tv % hd;
-        const int col = (nh + nkv) * hd + tv;
-        float v = 0.f;
-        for (int sp = 0; sp < S; ++sp) v += pr[sp * sstride + col];
+        const float v = sum_planes(pr, planes, sstride, v_off + tv);
         vc[(static_cast<long long>(head) * max_seq + P + r) * hd + i] = v;
     }
 }
 
-cudaError_t qkv_rope_launch(const float *part, int S, long long sstride, int ldp, int nrows, int nh, int nkv, int hd,
-                            const float2 *rope, int P, const int *depth, float *q, float *kc, float *vc, int max_seq,
-                            cudaStream_t s) {
+cudaError_t qkv_rope_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows, int nh,
+                            int nkv, int hd, int k_off, int v_off, const float2 *rope, int P, const int *depth,
+                            float *q, float *kc, float *vc, int max_seq, cudaStream_t s) {
     const int items = (nh + nkv) * (hd / 2) + nkv * hd;
     dim3 grid((items + 255) / 256, nrows);
-    k_qkv_rope<<<grid, 256, 0, s>>>(part, S, sstride, ldp, nh, nkv, hd, rope, P, depth, q, kc, vc, max_seq);
+    launch_k(k_qkv_rope, dim3(grid), dim3(256), 0, s, part, planes, sstride, ldp, nh, nkv, hd, k_off, v_off, rope, P, depth, q, kc, vc,
+                                    max_seq);
     return cudaGetLastError();
 }
 
@@ -109,9 +117,12 @@ cudaError_t qkv_rope_launch(const float *part, int S, long long sstride, int ldp
 // xout[i] = rmsnorm(h[r]) * gain.  d % 4 == 0; float4 accesses, all loads of
 // a thread issued before the reduction.
 template <typename T>
-__global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part, int S, long long sstride, int ldp,
+__global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part, const int *planes,
+                                                     long long sstride, int ldp,
                                                      int d, const T *gain, float eps, const int *row_map, T *xout,
                                                      long long lo_off) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[32];
     const int i = blockIdx.x;
     const int r = row_map ? row_map[i] : i;
@@ -126,7 +137,8 @@ __global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part
         const int c = threadIdx.x + j * 1024;
         if (c < d4) {
             float4 a = hr[c];
-            for (int sp = 0; sp < S; ++sp) {
+            const int np = planes ? planes[(4 * c) >> 7] : 1;
+            for (int sp = 0; sp < np; ++sp) {
                 const float4 b = *reinterpret_cast<const float4 *>(pr + sp * sstride + 4 * c);
                 a.x += b.x;
                 a.y += b.y;
@@ -134,7 +146,7 @@ __global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part
                 a.w += b.w;
             }
             v[j] = a;
-            if (S > 0) hr[c] = a;
+            hr[c] = a;
             ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
         }
     }
@@ -154,56 +166,61 @@ __global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part
 }
 
 template <typename T>
-cudaError_t resid_norm_launch(float *h, const float *part, int S, long long sstride, int ldp, int d, const T *gain,
-                              float eps, const int *row_map, int nrows, T *xout, long long lo_off, cudaStream_t s) {
+cudaError_t resid_norm_launch(float *h, const float *part, const int *planes, long long sstride, int ldp, int d,
+                              const T *gain, float eps, const int *row_map, int nrows, T *xout, long long lo_off,
+                              cudaStream_t s) {
     if (d % 4 || d > 16384) return cudaErrorInvalidValue;
-    k_resid_norm<T><<<nrows, 1024, 0, s>>>(h, part, S, sstride, ldp, d, gain, eps, row_map, xout, lo_off);
+    launch_k(k_resid_norm<T>, dim3(nrows), dim3(1024), 0, s, h, part, planes, sstride, ldp, d, gain, eps, row_map, xout, lo_off);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ SwiGLU
 // part columns: gate [0, F) | up [F, 2F).  out[r][f] = silu(gate) * up.
 template <typename T>
-__global__ void k_swiglu(const float *part, int S, long long sstride, int ldp, int nrows, int F, T *out,
-                         long long lo_off) {
+__global__ void k_swiglu(const float *part, const int *planes, long long sstride, int ldp, int nrows, int F,
+                         int up_off, T *out, long long lo_off) {
+    pdl_trigger();
+    pdl_wait();
     const long long n = static_cast<long long>(nrows) * F;
     for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
          t += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int r = static_cast<int>(t / F), f = static_cast<int>(t % F);
         const float *pr = part + static_cast<long long>(r) * ldp;
-        float g = 0.f, u = 0.f;
-        for (int sp = 0; sp < S; ++sp) {
-            g += pr[sp * sstride + f];
-            u += pr[sp * sstride + F + f];
-        }
+        const float g = sum_planes(pr, planes, sstride, f);
+        const float u = sum_planes(pr, planes, sstride, up_off + f);
         store_act(out, t, g / (1.f + expf(-g)) * u, lo_off);
     }
 }
 
 template <typename T>
-cudaError_t swiglu_launch(const float *part, int S, long long sstride, int ldp, int nrows, int F, T *out,
-                          long long lo_off, cudaStream_t s) {
+cudaError_t swiglu_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows, int F,
+                          int up_off, T *out, long long lo_off, cudaStream_t s) {
     const long long n = static_cast<long long>(nrows) * F;
     int blocks = static_cast<int>((n + 255) / 256);
     if (blocks > 152 * 64) blocks = 152 * 64;
-    k_swiglu<T><<<blocks, 256, 0, s>>>(part, S, sstride, ldp, nrows, F, out, lo_off);
+    launch_k(k_swiglu<T>, dim3(blocks), dim3(256), 0, s, part, planes, sstride, ldp, nrows, F, up_off, out, lo_off);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ argmax / softmax stats
 // Per row: index of the largest logit (lowest index among equals), the max,
 // and sum_v exp((l_v - max) * invT) when invT > 0.
-__global__ void __launch_bounds__(1024) k_argmax(const float *logits, int V, float invT, int *amax, float *lmax,
+__global__ void __launch_bounds__(1024) k_argmax(const float *part, const int *planes, long long sstride, int ldp,
+                                                 float *logits, int V, float invT, int *amax, float *lmax,
                                                  float *lsum) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float sv[32];
     __shared__ int si[32];
     __shared__ float red[32];
     const int r = blockIdx.x;
-    const float *l = logits + static_cast<long long>(r) * V;
+    const float *pr = part + static_cast<long long>(r) * ldp;
+    float *l = logits + static_cast<long long>(r) * V;
     float best = -INFINITY;
     int bi = 0x7fffffff;
     for (int v = threadIdx.x; v < V; v += 1024) {
-        const float x = l[v];
+        const float x = sum_planes(pr, planes, sstride, v);
+        l[v] = x;
         if (x > best) {
             best = x;
             bi = v;
@@ -255,18 +272,19 @@ __global__ void __launch_bounds__(1024) k_argmax(const float *logits, int V, flo
     }
 }
 
-cudaError_t argmax_launch(const float *logits, int rows, int V, float invT, int *amax, float *lmax, float *lsum,
-                          cudaStream_t s) {
-    k_argmax<<<rows, 1024, 0, s>>>(logits, V, invT, amax, lmax, lsum);
+cudaError_t argmax_launch(const float *part, const int *planes, long long sstride, int ldp, float *logits, int rows,
+                          int V, float invT, int *amax, float *lmax, float *lsum, cudaStream_t s) {
+    launch_k(k_argmax, dim3(rows), dim3(1024), 0, s, part, planes, sstride, ldp, logits, V, invT, amax, lmax, lsum);
     return cudaGetLastError();
 }
 
 #define LA_INST(T)                                                                                                   \
     template cudaError_t embed_norm_launch<T>(const T *, const int *, int, int, const T *, float, float *, T *,       \
                                               long long, cudaStream_t);                                              \
-    template cudaError_t resid_norm_launch<T>(float *, const float *, int, long long, int, int, const T *, float,    \
-                                              const int *, int, T *, long long, cudaStream_t);                       \
-    template cudaError_t swiglu_launch<T>(const float *, int, long long, int, int, int, T *, long long, cudaStream_t);
+    template cudaError_t resid_norm_launch<T>(float *, const float *, const int *, long long, int, int, const T *,   \
+                                              float, const int *, int, T *, long long, cudaStream_t);                \
+    template cudaError_t swiglu_launch<T>(const float *, const int *, long long, int, int, int, int, T *, long long, \
+                                          cudaStream_t);
 LA_INST(float)
 LA_INST(__nv_bfloat16)
 #undef LA_INST

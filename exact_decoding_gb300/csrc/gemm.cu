@@ -13,13 +13,49 @@
 // kernel, so results are deterministic.
 //
 // fp32 path -- a plain SIMT kernel (fp32 FMA, no tf32) for fp32 models.
+#include <algorithm>
 #include <cstdio>
+#include <vector>
 
 #include "la_kernels.h"
 
 namespace la {
 
 // ------------------------------------------------------------------ tcgen05 kernel
+// Work: a list of segments (tile, k-block range, partial plane).  With a
+// segment table each CTA runs the contiguous run of segments the host gave
+// it (stream-K: the flattened tile x k-block work split evenly over the
+// SMs); without one, CTA b runs the single segment (tile b / splits, split b
+// % splits, plane = split).  The accumulator is double-buffered in TMEM so a
+// segment's epilogue overlaps the next segment's main loop.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+struct SegInfo {
+    int seg, row0, kb0, kb1, plane;
+};
+
+__device__ __forceinline__ SegInfo segment(const TcGemmParams &p, int i) {
+    int tile, kb0, kb1, plane;
+    if (p.segs) {
+        const int4 s = p.segs[i];
+        tile = s.x;
+        kb0 = s.y;
+        kb1 = s.z;
+        plane = s.w;
+    } else {
+        tile = i / p.splits;
+        const int split = i % p.splits;
+        kb0 = static_cast<int>((static_cast<long long>(split) * p.n_kb) / p.splits);
+        kb1 = static_cast<int>((static_cast<long long>(split + 1) * p.n_kb) / p.splits);
+        plane = split;
+    }
+    int seg = 0;
+    while (seg + 1 < p.nseg && tile >= p.seg_tile0[seg + 1]) ++seg;
+    return SegInfo{seg, (tile - p.seg_tile0[seg]) * kTileM, kb0, kb1, plane};
+}
+
 __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -31,26 +67,34 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * stage_bytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + p.stages;
-    uint64_t *accb = bars + 2 * p.stages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.stages + 1);
+    uint64_t *accfull = bars + 2 * p.stages;       // [2]
+    uint64_t *accempty = bars + 2 * p.stages + 2;  // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.stages + 4);
 
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
-    int seg = 0;
-    while (seg + 1 < p.nseg && tile >= p.seg_tile0[seg + 1]) ++seg;
-    const int row0 = (tile - p.seg_tile0[seg]) * kTileM;
-    const int kb0 = static_cast<int>((static_cast<long long>(split) * p.n_kb) / p.splits);
-    const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * p.n_kb) / p.splits);
-    const int nk = kb1 - kb0;
+    int sbeg, send;
+    if (p.segs) {
+        sbeg = p.cta_first[blockIdx.x];
+        send = p.cta_first[blockIdx.x + 1];
+    } else {
+        sbeg = blockIdx.x;
+        send = blockIdx.x + 1;
+    }
+    // Two accumulator buffers when this CTA runs more than one segment.
+    const int nbuf = (send - sbeg) > 1 ? 2 : 1;
     uint32_t ncols = 32;
-    while (ncols < static_cast<uint32_t>(bn)) ncols <<= 1;
+    while (ncols < static_cast<uint32_t>(nbuf * bn)) ncols <<= 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < p.stages; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
             mbar_init(smem_u32(&empty[i]), 1);
         }
-        mbar_init(smem_u32(accb), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accfull[b]), 1);
+            mbar_init(smem_u32(&accempty[b]), 4);
+        }
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -66,49 +110,90 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
         if (lane == 0) {
             // TMA producer: weights stream through L2 once (evict first); the
             // small row block is re-read by every CTA (evict last).
-            prefetch_tensormap(&p.a[seg]);
+            for (int sg = 0; sg < p.nseg; ++sg) prefetch_tensormap(&p.a[sg]);
             prefetch_tensormap(&p.b);
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            for (int i = 0; i < nk; ++i) {
-                const int st = i % p.stages;
-                if (i >= p.stages && !mbar_wait(smem_u32(&empty[st]), ((i / p.stages) & 1) ^ 1, p.err, ERR_TIMEOUT_EMPTY))
-                    break;
-                const uint32_t sa = smem_u32(smem + st * stage_bytes);
-                const uint32_t fb = smem_u32(&full[st]);
-                mbar_arrive_expect_tx(fb, stage_bytes);
-                tma_load_2d(sa, &p.a[seg], (kb0 + i) * kBlockK, row0, fb, pol_w);
-                tma_load_2d(sa + a_bytes, &p.b, (kb0 + i) * kBlockK, 0, fb, pol_x);
+            // Weights do not depend on the previous kernel: fill the ring's
+            // weight halves before waiting for it, then load the input rows.
+            int it = 0;
+            for (int i = sbeg; i < send && it < p.stages; ++i) {
+                const SegInfo g = segment(p, i);
+                for (int kb = g.kb0; kb < g.kb1 && it < p.stages; ++kb, ++it) {
+                    const uint32_t fb = smem_u32(&full[it]);
+                    mbar_arrive_expect_tx(fb, stage_bytes);
+                    tma_load_2d(smem_u32(smem + it * stage_bytes), &p.a[g.seg], kb * kBlockK, g.row0, fb, pol_w);
+                }
+            }
+            const int npre = it;
+            pdl_wait();
+            it = 0;
+            bool ok = true;
+            for (int i = sbeg; i < send && ok; ++i) {
+                const SegInfo g = segment(p, i);
+                for (int kb = g.kb0; kb < g.kb1; ++kb, ++it) {
+                    const int st = it % p.stages;
+                    const uint32_t sa = smem_u32(smem + st * stage_bytes);
+                    const uint32_t fb = smem_u32(&full[st]);
+                    if (it < npre) {
+                        tma_load_2d(sa + a_bytes, &p.b, kb * kBlockK, 0, fb, pol_x);
+                        continue;
+                    }
+                    if (!mbar_wait(smem_u32(&empty[st]), ((it / p.stages) & 1) ^ 1, p.err, ERR_TIMEOUT_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(fb, stage_bytes);
+                    tma_load_2d(sa, &p.a[g.seg], kb * kBlockK, g.row0, fb, pol_w);
+                    tma_load_2d(sa + a_bytes, &p.b, kb * kBlockK, 0, fb, pol_x);
+                }
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // UMMA issuer: 4 instructions of K = 16 per 64-wide stage.
             const uint32_t idesc = umma_idesc_bf16(kTileM, bn);
-            for (int i = 0; i < nk; ++i) {
-                const int st = i % p.stages;
-                if (!mbar_wait(smem_u32(&full[st]), (i / p.stages) & 1, p.err, ERR_TIMEOUT_FULL)) break;
+            int it = 0, ul = 0;
+            bool ok = true;
+            for (int i = sbeg; i < send; ++i, ++ul) {
+                const SegInfo g = segment(p, i);
+                const int buf = ul & 1;
+                if (ok && ul >= 2)
+                    ok = mbar_wait(smem_u32(&accempty[buf]), ((ul >> 1) & 1) ^ 1, p.err, ERR_TIMEOUT_ACCUM);
                 tc_fence_after();
-                const uint32_t sa = smem_u32(smem + st * stage_bytes);
-                const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + a_bytes);
+                const uint32_t d = tmem + static_cast<uint32_t>(buf * bn);
+                for (int kb = g.kb0; kb < g.kb1 && ok; ++kb, ++it) {
+                    const int st = it % p.stages;
+                    if (!mbar_wait(smem_u32(&full[st]), (it / p.stages) & 1, p.err, ERR_TIMEOUT_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + st * stage_bytes);
+                    const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + a_bytes);
 #pragma unroll
-                for (int kk = 0; kk < kBlockK / 16; ++kk)
-                    umma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i | kk) != 0);
-                umma_commit(smem_u32(&empty[st]));
+                    for (int kk = 0; kk < kBlockK / 16; ++kk)
+                        umma_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (kb != g.kb0 || kk != 0) ? 1u : 0u);
+                    umma_commit(smem_u32(&empty[st]));
+                }
+                umma_commit(smem_u32(&accfull[buf]));
             }
-            umma_commit(smem_u32(accb));
         }
     } else {
         // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 = output features.
-        bool ok = mbar_wait(smem_u32(accb), 0, p.err, ERR_TIMEOUT_ACCUM);
-        ok = __all_sync(0xffffffffu, ok) && nk > 0;
-        __syncwarp();
-        tc_fence_after();
-        if (ok) {
-            const int q = warp & 3;
-            const int f = row0 + 32 * q + lane;
-            const bool fv = f < p.seg_out[seg];
-            float *out = p.out + static_cast<long long>(split) * p.split_stride + p.seg_col0[seg] + f;
-            const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        const int q = warp & 3;
+        int ul = 0;
+        for (int i = sbeg; i < send; ++i, ++ul) {
+            const SegInfo g = segment(p, i);
+            const int buf = ul & 1;
+            bool ok = mbar_wait(smem_u32(&accfull[buf]), (ul >> 1) & 1, p.err, ERR_TIMEOUT_ACCUM);
+            ok = __all_sync(0xffffffffu, ok);
+            __syncwarp();
+            tc_fence_after();
+            if (!ok) break;
+            const int f = g.row0 + 32 * q + lane;
+            const bool fv = f < p.seg_out[g.seg];
+            float *out = p.out + static_cast<long long>(g.plane) * p.split_stride + p.seg_col0[g.seg] + f;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * bn);
             if (p.bh > 0) {
                 // columns c (hi rows) + columns c + bh (lo rows) = one output row
                 for (int c0 = 0; c0 < p.bh; c0 += 32) {
@@ -139,6 +224,9 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
                     }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&accempty[buf]));
         }
     }
     tc_fence_before();
@@ -152,6 +240,35 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
 
 size_t tc_gemm_smem_bytes(int bn, int stages) {
     return static_cast<size_t>(stages) * (kTileM * kBlockK * 2 + bn * kBlockK * 2) + 1024 + 256;
+}
+
+// Stream-K schedule: the flattened (tile, k-block) work split into `ctas`
+// contiguous, equal runs (+-1 k-block); a run is cut at tile boundaries into
+// segments.  Partial plane of a segment = how many earlier CTAs touched its
+// tile, so tile t has tile_planes[t] planes, added in plane order.
+void stream_k_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, std::vector<int> &cta_first,
+                       std::vector<int> &tile_planes) {
+    const long long W = static_cast<long long>(tiles) * n_kb;
+    if (ctas > W) ctas = static_cast<int>(W);
+    segs.clear();
+    cta_first.assign(ctas + 1, 0);
+    tile_planes.assign(tiles, 0);
+    for (int c = 0; c < ctas; ++c) {
+        cta_first[c] = static_cast<int>(segs.size() / 4);
+        long long s = W * c / ctas;
+        const long long e = W * (c + 1) / ctas;
+        while (s < e) {
+            const int t = static_cast<int>(s / n_kb);
+            const int k0 = static_cast<int>(s % n_kb);
+            const int k1 = static_cast<int>(std::min<long long>(n_kb, k0 + (e - s)));
+            segs.push_back(t);
+            segs.push_back(k0);
+            segs.push_back(k1);
+            segs.push_back(tile_planes[t]++);
+            s += k1 - k0;
+        }
+    }
+    cta_first[ctas] = static_cast<int>(segs.size() / 4);
 }
 
 int tc_gemm_stages_for(int bn) {
@@ -200,14 +317,14 @@ int choose_splits(int tiles, int n_kb, int slots) {
 }
 
 void tc_gemm_finalize(TcGemm &g) {
-    g.grid = g.p.seg_tile0[g.p.nseg] * g.p.splits;
+    g.grid = g.p.segs ? g.ctas : g.p.seg_tile0[g.p.nseg] * g.p.splits;
     g.smem = tc_gemm_smem_bytes(g.p.bn, g.p.stages);
 }
 
 cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s) {
     cudaError_t e = gemm_smem_attr();
     if (e != cudaSuccess) return e;
-    k_gemm_tc<<<g.grid, 192, g.smem, s>>>(g.p);
+    launch_k(k_gemm_tc, dim3(g.grid), dim3(192), g.smem, s, g.p);
     return cudaGetLastError();
 }
 
@@ -246,6 +363,8 @@ int make_tmap_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t ou
 
 // ------------------------------------------------------------------ fp32 SIMT path
 __global__ void k_gemm_simt(const SimtGemmParams p, int total_f) {
+    pdl_trigger();
+    pdl_wait();
     const int f = blockIdx.x * 64 + (threadIdx.x & 63);
     const int r = blockIdx.y * 4 + (threadIdx.x >> 6);
     if (f >= total_f || r >= p.nrows) return;
@@ -261,11 +380,13 @@ __global__ void k_gemm_simt(const SimtGemmParams p, int total_f) {
 
 cudaError_t simt_gemm_launch(const SimtGemmParams &p, int total_f, cudaStream_t s) {
     dim3 grid((total_f + 63) / 64, (p.nrows + 3) / 4);
-    k_gemm_simt<<<grid, 256, 0, s>>>(p, total_f);
+    launch_k(k_gemm_simt, dim3(grid), dim3(256), 0, s, p, total_f);
     return cudaGetLastError();
 }
 
 __global__ void k_reduce_splits(const float *part, int splits, long long stride, long long n, float *y) {
+    pdl_trigger();
+    pdl_wait();
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
         float acc = part[i];
@@ -279,7 +400,7 @@ cudaError_t reduce_splits_launch(const float *part, int splits, long long stride
     const long long n = static_cast<long long>(rows) * cols;
     int blocks = static_cast<int>((n + 255) / 256);
     if (blocks > 4096) blocks = 4096;
-    k_reduce_splits<<<blocks, 256, 0, s>>>(part, splits, stride, n, y);
+    launch_k(k_reduce_splits, dim3(blocks), dim3(256), 0, s, part, splits, stride, n, y);
     return cudaGetLastError();
 }
 

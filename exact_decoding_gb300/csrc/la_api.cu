@@ -90,8 +90,18 @@ struct la_handle {
     // GEMM plans (bf16): [mode][kind][layer]
     std::vector<TcGemm> plan[2][4];
     TcGemm plan_lm;
-    int splits[2][4] = {{1, 1, 1, 1}, {1, 1, 1, 1}};
-    size_t part_elems = 0;
+    // Column layout of the GEMM partials: every matrix starts on a 128-column
+    // tile boundary, so column c belongs to tile c >> 7.
+    int tq = 0, tk = 0, tg = 0, td = 0, tv = 0;       // tiles of q, k (= v), gate (= up), d, vocab
+    int ldo[4] = {0, 0, 0, 0}, ldo_lm = 0;
+    int k_off = 0, v_off = 0, up_off = 0;
+    // Per-tile partial-plane counts of each stream-K schedule ([mode][kind]);
+    // null on the fp32 path (one plane).
+    int *planes[2][4] = {{nullptr, nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr, nullptr}};
+    int *planes_lm = nullptr;
+    float *lm_part = nullptr;
+    long long lm_stride = 0;
+    size_t part_elems = 0, lm_part_elems = 0;
 
     // profiling (la_opts.profile): event pairs around GEMM / attention launches
     bool prof_on = false;
@@ -245,7 +255,7 @@ double gemm_bytes(const la_handle *h, Kind kind, int nrows) {
 }
 
 int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
-    const int ldo = kind == QKV ? h->qkv_out : kind == GATEUP ? 2 * h->F : h->d;
+    const int ldo = h->ldo[kind];
     h->launches += 1;
     const int pe = mode == STEP ? h->prof_begin() : -1;
     if (h->bf16) {
@@ -264,10 +274,11 @@ int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
         p.a[1] = static_cast<const float *>(h->wk[l]);
         p.a[2] = static_cast<const float *>(h->wv[l]);
         const int outs[3] = {h->qd, h->kvd, h->kvd};
+        const int col0[3] = {0, h->k_off, h->v_off};
         int acc = 0;
         for (int i = 0; i < 3; ++i) {
             p.seg_f0[i] = acc;
-            p.seg_col0[i] = acc;
+            p.seg_col0[i] = col0[i];
             acc += outs[i];
         }
         p.seg_f0[3] = acc;
@@ -278,7 +289,7 @@ int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
         p.seg_f0[0] = 0;
         p.seg_col0[0] = 0;
         p.seg_f0[1] = h->F;
-        p.seg_col0[1] = h->F;
+        p.seg_col0[1] = h->up_off;
         p.seg_f0[2] = 2 * h->F;
     } else {
         p.nseg = 1;
@@ -321,8 +332,8 @@ int run_lm_head(la_handle *h, int nrows, bool step) {
     p.ldx = h->d;
     p.K = h->d;
     p.nrows = nrows;
-    p.ldo = h->V;
-    p.out = h->logits;
+    p.ldo = h->ldo_lm;
+    p.out = h->lm_part;
     CK(simt_gemm_launch(p, h->V, h->stream));
     h->prof_end(pe, 0, bytes);
     return LA_OK;
@@ -347,10 +358,10 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
     for (int l = 0; l < h->L; ++l) {
         int rc;
         if ((rc = run_gemm(h, mode, QKV, l, nrows)) != LA_OK) return rc;
-        const long long ss_qkv = static_cast<long long>(h->R) * h->qkv_out;
-        CK(qkv_rope_launch(h->part, h->splits[mode][QKV], ss_qkv, h->qkv_out, nrows, h->nh, h->nkv, h->hd, h->rope,
-                           P, mode == STEP ? h->depth : nullptr, h->q, h->kv_layer(l, 0), h->kv_layer(l, 1),
-                           h->max_seq, s));
+        const long long ss_qkv = static_cast<long long>(h->R) * h->ldo[QKV];
+        CK(qkv_rope_launch(h->part, h->planes[mode][QKV], ss_qkv, h->ldo[QKV], nrows, h->nh, h->nkv, h->hd,
+                           h->k_off, h->v_off, h->rope, P, mode == STEP ? h->depth : nullptr, h->q,
+                           h->kv_layer(l, 0), h->kv_layer(l, 1), h->max_seq, s));
         AttnArgs a{};
         a.q = h->q;
         a.kc = h->kv_layer(l, 0);
@@ -375,24 +386,25 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
                     (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * 4.0 + 4.0 * nrows * h->qd + 4.0 * nrows * h->qd);
         h->launches += 1 + (h->bf16 ? 2 : 1 + (nch > 0 ? 1 : 0));   // qkv_rope, attention passes
         if ((rc = run_gemm(h, mode, OPROJ, l, nrows)) != LA_OK) return rc;
-        const long long ss_d = static_cast<long long>(h->R) * h->d;
-        CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][OPROJ], ss_d, h->d, h->d,
+        const long long ss_d = static_cast<long long>(h->R) * h->ldo[OPROJ];
+        CK(resid_norm_launch<T>(h->h, h->part, h->planes[mode][OPROJ], ss_d, h->ldo[OPROJ], h->d,
                                 static_cast<const T *>(h->ffn_norm[l]), eps, nullptr, nrows,
                                 static_cast<T *>(h->xn), bh * h->d, s));
         if ((rc = run_gemm(h, mode, GATEUP, l, nrows)) != LA_OK) return rc;
-        const long long ss_gu = static_cast<long long>(h->R) * 2 * h->F;
-        CK(swiglu_launch<T>(h->part, h->splits[mode][GATEUP], ss_gu, 2 * h->F, nrows, h->F,
+        const long long ss_gu = static_cast<long long>(h->R) * h->ldo[GATEUP];
+        CK(swiglu_launch<T>(h->part, h->planes[mode][GATEUP], ss_gu, h->ldo[GATEUP], nrows, h->F, h->up_off,
                             static_cast<T *>(h->fa), bh * h->F, s));
         h->launches += 3;   // resid_norm after O, swiglu, resid_norm after down
         if ((rc = run_gemm(h, mode, DOWN, l, nrows)) != LA_OK) return rc;
+        const long long ss_dn = static_cast<long long>(h->R) * h->ldo[DOWN];
         if (l + 1 < h->L) {
-            CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][DOWN], ss_d, h->d, h->d,
+            CK(resid_norm_launch<T>(h->h, h->part, h->planes[mode][DOWN], ss_dn, h->ldo[DOWN], h->d,
                                     static_cast<const T *>(h->attn_norm[l + 1]), eps, nullptr, nrows,
                                     static_cast<T *>(h->xn), bh * h->d, s));
         } else if (want_logits) {
             const int *map = mode == STEP ? h->used : h->iota + (nrows - 1);
             const int rows = mode == STEP ? h->U : 1;
-            CK(resid_norm_launch<T>(h->h, h->part, h->splits[mode][DOWN], ss_d, h->d, h->d,
+            CK(resid_norm_launch<T>(h->h, h->part, h->planes[mode][DOWN], ss_dn, h->ldo[DOWN], h->d,
                                     static_cast<const T *>(h->final_norm), eps, map, rows,
                                     static_cast<T *>(h->xu), static_cast<long long>(h->bh_u) * h->d, s));
         }
@@ -430,7 +442,8 @@ int run_prefix(la_handle *h, int n, bool want_logits) {
     if (want_logits) {
         int rc = run_lm_head(h, 1, false);
         if (rc != LA_OK) return rc;
-        CK(argmax_launch(h->logits, 1, h->V, h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
+        CK(argmax_launch(h->lm_part, h->planes_lm, h->lm_stride, h->ldo_lm, h->logits, 1, h->V,
+                         h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
                          h->lmax, h->lsum, h->stream));
     }
     return LA_OK;
@@ -444,50 +457,75 @@ int reset_pool(la_handle *h) {
     return LA_OK;
 }
 
+// Uploads one stream-K schedule; returns the device tables and max planes.
+int upload_schedule(la_handle *h, int tiles, int n_kb, int ctas, TcGemm &g, int **planes_dev, int *max_planes) {
+    std::vector<int> segs, first, planes;
+    stream_k_schedule(tiles, n_kb, ctas, segs, first, planes);
+    int *dsegs = nullptr, *dfirst = nullptr, *dplanes = nullptr;
+    int rc;
+    if ((rc = h->alloc(&dsegs, segs.size())) != LA_OK || (rc = h->alloc(&dfirst, first.size())) != LA_OK ||
+        (rc = h->alloc(&dplanes, planes.size())) != LA_OK)
+        return rc;
+    CK(cudaMemcpy(dsegs, segs.data(), segs.size() * sizeof(int), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(dfirst, first.data(), first.size() * sizeof(int), cudaMemcpyHostToDevice));
+    CK(cudaMemcpy(dplanes, planes.data(), planes.size() * sizeof(int), cudaMemcpyHostToDevice));
+    g.p.segs = reinterpret_cast<const int4 *>(dsegs);
+    g.p.cta_first = dfirst;
+    g.ctas = static_cast<int>(first.size()) - 1;
+    *planes_dev = dplanes;
+    *max_planes = *std::max_element(planes.begin(), planes.end());
+    return LA_OK;
+}
+
 int build_plans(la_handle *h) {
     int dev = 0;
     CK(cudaGetDevice(&dev));
     int nsm = 0;
     CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
     const int bhs[2] = {h->bh_step, h->bh_pf};
-    void *xs[2][4] = {{h->xn, h->ao, h->xn, h->fa}, {h->xn, h->ao, h->xn, h->fa}};
+    void *xs[4] = {h->xn, h->ao, h->xn, h->fa};
     const int Ks[4] = {h->d, h->qd, h->d, h->F};
-    const int ldos[4] = {h->qkv_out, h->d, 2 * h->F, h->d};
     size_t part_max = 0;
     for (int mode = 0; mode < 2; ++mode) {
         const int bhm = bhs[mode];
         const int bn = 2 * bhm;             // hi rows + lo rows
-        const int rows_map = bn;
         const int stages = tc_gemm_stages_for(bn);
-        const int slots = nsm * tc_gemm_ctas_per_sm(bn, stages);
+        const int ctas = nsm * tc_gemm_ctas_per_sm(bn, stages);
         for (int kind = 0; kind < 4; ++kind) {
             const int K = Ks[kind];
             CUtensorMap bmap;
-            if (make_tmap_bf16(&bmap, xs[mode][kind], K, rows_map, static_cast<uint64_t>(K) * 2, kBlockK, bn))
+            if (make_tmap_bf16(&bmap, xs[kind], K, bn, static_cast<uint64_t>(K) * 2, kBlockK, bn))
                 return fail(LA_ERR_CUDA, "tensor map for activations failed");
-            int outs[3], nseg;
+            int outs[3], col0[3], nseg;
             if (kind == QKV) {
                 nseg = 3;
                 outs[0] = h->qd;
-                outs[1] = h->kvd;
-                outs[2] = h->kvd;
+                outs[1] = outs[2] = h->kvd;
+                col0[0] = 0;
+                col0[1] = h->k_off;
+                col0[2] = h->v_off;
             } else if (kind == GATEUP) {
                 nseg = 2;
                 outs[0] = outs[1] = h->F;
+                col0[0] = 0;
+                col0[1] = h->up_off;
             } else {
                 nseg = 1;
                 outs[0] = h->d;
+                col0[0] = 0;
             }
             int tiles = 0;
             for (int i = 0; i < nseg; ++i) tiles += (outs[i] + kTileM - 1) / kTileM;
             const int n_kb = (K + kBlockK - 1) / kBlockK;
-            const int S = choose_splits(tiles, n_kb, slots);
-            h->splits[mode][kind] = S;
-            part_max = std::max(part_max, static_cast<size_t>(S) * h->R * ldos[kind]);
+            TcGemm proto;
+            std::memset(&proto.p, 0, sizeof(proto.p));
+            int maxp = 1, rc;
+            if ((rc = upload_schedule(h, tiles, n_kb, ctas, proto, &h->planes[mode][kind], &maxp)) != LA_OK) return rc;
+            part_max = std::max(part_max, static_cast<size_t>(maxp) * h->R * h->ldo[kind]);
             h->plan[mode][kind].resize(h->L);
             for (int l = 0; l < h->L; ++l) {
                 TcGemm &g = h->plan[mode][kind][l];
-                std::memset(&g.p, 0, sizeof(g.p));
+                g = proto;
                 const void *ws[3];
                 if (kind == QKV) {
                     ws[0] = h->wq[l];
@@ -499,57 +537,62 @@ int build_plans(la_handle *h) {
                 } else {
                     ws[0] = kind == OPROJ ? h->wo[l] : h->wd[l];
                 }
-                int t0 = 0, col = 0;
+                int t0 = 0;
                 for (int i = 0; i < nseg; ++i) {
                     if (make_tmap_bf16(&g.p.a[i], ws[i], K, outs[i], static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
                         return fail(LA_ERR_INVALID_ARG, "tensor map for a weight failed (16-byte alignment?)");
                     g.p.seg_tile0[i] = t0;
                     g.p.seg_out[i] = outs[i];
-                    g.p.seg_col0[i] = col;
+                    g.p.seg_col0[i] = col0[i];
                     t0 += (outs[i] + kTileM - 1) / kTileM;
-                    col += outs[i];
                 }
                 g.p.seg_tile0[nseg] = t0;
                 g.p.b = bmap;
                 g.p.nseg = nseg;
                 g.p.n_kb = n_kb;
-                g.p.splits = S;
+                g.p.splits = 1;
                 g.p.nrows = mode == STEP ? h->M : kPrefillRows;
                 g.p.bn = bn;
                 g.p.bh = bhm;
-                g.p.ldo = ldos[kind];
+                g.p.ldo = h->ldo[kind];
                 g.p.stages = stages;
-                g.p.split_stride = static_cast<long long>(h->R) * ldos[kind];
+                g.p.split_stride = static_cast<long long>(h->R) * h->ldo[kind];
                 g.p.out = h->part;
                 g.p.err = &h->st->err;
                 tc_gemm_finalize(g);
             }
         }
     }
-    // lm_head over the used rows (one split: the vocabulary gives enough tiles)
+    // lm_head over the used rows
     {
         TcGemm &g = h->plan_lm;
         std::memset(&g.p, 0, sizeof(g.p));
         const int bn = 2 * h->bh_u;
+        const int stages = tc_gemm_stages_for(bn);
+        const int ctas = nsm * tc_gemm_ctas_per_sm(bn, stages);
         if (make_tmap_bf16(&g.p.a[0], h->lm_head, h->d, h->V, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM) ||
             make_tmap_bf16(&g.p.b, h->xu, h->d, bn, static_cast<uint64_t>(h->d) * 2, kBlockK, bn))
             return fail(LA_ERR_INVALID_ARG, "tensor map for lm_head failed");
+        const int n_kb = (h->d + kBlockK - 1) / kBlockK;
+        int maxp = 1, rc;
+        if ((rc = upload_schedule(h, h->tv, n_kb, ctas, g, &h->planes_lm, &maxp)) != LA_OK) return rc;
         g.p.nseg = 1;
         g.p.seg_tile0[0] = 0;
-        g.p.seg_tile0[1] = (h->V + kTileM - 1) / kTileM;
+        g.p.seg_tile0[1] = h->tv;
         g.p.seg_out[0] = h->V;
         g.p.seg_col0[0] = 0;
-        g.p.n_kb = (h->d + kBlockK - 1) / kBlockK;
+        g.p.n_kb = n_kb;
         g.p.splits = 1;
         g.p.nrows = h->U;
         g.p.bn = bn;
         g.p.bh = h->bh_u;
-        g.p.ldo = h->V;
-        g.p.stages = tc_gemm_stages_for(bn);
-        g.p.split_stride = 0;
-        g.p.out = h->logits;
+        g.p.ldo = h->ldo_lm;
+        g.p.stages = stages;
+        g.p.split_stride = h->lm_stride;
+        g.p.out = h->lm_part;
         g.p.err = &h->st->err;
         tc_gemm_finalize(g);
+        h->lm_part_elems = static_cast<size_t>(maxp) * h->lm_stride;
     }
     h->part_elems = part_max;
     return LA_OK;
@@ -632,6 +675,20 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     h->bh_pf = kPrefillRows;
     h->bh_u = round_up(h->U, 32);
     h->act_rows = h->bf16 ? 2 * kPrefillRows : h->R;
+    h->tq = (h->qd + kTileM - 1) / kTileM;
+    h->tk = (h->kvd + kTileM - 1) / kTileM;
+    h->tg = (h->F + kTileM - 1) / kTileM;
+    h->td = (h->d + kTileM - 1) / kTileM;
+    h->tv = (h->V + kTileM - 1) / kTileM;
+    h->k_off = h->tq * kTileM;
+    h->v_off = (h->tq + h->tk) * kTileM;
+    h->up_off = h->tg * kTileM;
+    h->ldo[QKV] = (h->tq + 2 * h->tk) * kTileM;
+    h->ldo[OPROJ] = h->td * kTileM;
+    h->ldo[GATEUP] = 2 * h->tg * kTileM;
+    h->ldo[DOWN] = h->td * kTileM;
+    h->ldo_lm = h->tv * kTileM;
+    h->lm_stride = static_cast<long long>(std::max(h->U, 1)) * h->ldo_lm;
     if (h->bf16 && M > kPrefillRows) {
         delete h;
         return fail(LA_ERR_UNSUPPORTED, "bf16 models need 1 + (W+G)(N-1) <= 128");
@@ -761,13 +818,16 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     if (h->bf16) {
         rc = build_plans(h);
     } else {
-        h->part_elems = static_cast<size_t>(R) * std::max(h->qkv_out, std::max(2 * h->F, h->d));
+        h->part_elems = static_cast<size_t>(R) * std::max(std::max(h->ldo[QKV], h->ldo[GATEUP]), h->ldo[DOWN]);
+        h->lm_part_elems = static_cast<size_t>(h->lm_stride);
     }
     if (rc == LA_OK) rc = h->alloc(&h->part, h->part_elems);
+    if (rc == LA_OK) rc = h->alloc(&h->lm_part, h->lm_part_elems);
     if (rc == LA_OK && h->bf16) {
         for (int m = 0; m < 2; ++m)
             for (int k = 0; k < 4; ++k)
                 for (auto &g : h->plan[m][k]) g.p.out = h->part;
+        h->plan_lm.p.out = h->lm_part;
     }
     if (rc == LA_OK) rc = reset_pool(h);
     if (rc == LA_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = fail(LA_ERR_CUDA, "create sync failed");
@@ -849,7 +909,8 @@ int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     int rc = forward_any(h, STEP, h->tok, h->M, h->P, true);
     if (rc != LA_OK) return rc;
     if ((rc = run_lm_head(h, h->U, true)) != LA_OK) return rc;
-    CK(argmax_launch(h->logits, h->U, h->V, h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
+    CK(argmax_launch(h->lm_part, h->planes_lm, h->lm_stride, h->ldo_lm, h->logits, h->U, h->V,
+                     h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
                      h->lmax, h->lsum, s));
     CK(finish_step_launch(h->spec(), s));
     if ((rc = kv_commit(h)) != LA_OK) return rc;

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace la {
 
 // Device error word bits (the host turns any of them into LA_ERR_DEVICE_TIMEOUT).
@@ -43,6 +45,15 @@ __device__ __forceinline__ void store_act(__nv_bfloat16 *p, long long i, float v
     p[i] = hi;
     p[i + lo_off] = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
+
+// Programmatic dependent launch.  Every kernel of the step lets the next
+// kernel in the stream launch as soon as all its CTAs have started
+// (pdl_trigger), and waits for the previous kernel to complete and flush
+// (pdl_wait) before it touches anything that kernel wrote.  Because every
+// kernel waits before it can finish, completion stays ordered along the
+// whole chain.  Both are no-ops when the launch did not opt in.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t globaltimer() {
     uint64_t t;
@@ -191,6 +202,23 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
+}
+
+// Launch with programmatic stream serialization allowed (see pdl_trigger).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace la

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "la_common.cuh"
 
 namespace la {
@@ -28,14 +30,17 @@ struct TcGemmParams {
                                  //      epilogue adds columns c and c + bh.  0: plain bf16 rows
     int ldo;                     // output row stride (floats)
     int stages;                  // shared-memory pipeline depth
-    long long split_stride;      // floats between split partials
+    long long split_stride;      // floats between partial planes
     float *out;
     unsigned *err;
+    const int4 *segs;            // stream-K segments (tile, kb0, kb1, plane) or nullptr (one split per CTA)
+    const int *cta_first;        // [ctas + 1]: CTA c runs segs[cta_first[c] .. cta_first[c+1])
 };
 
 struct TcGemm {
     TcGemmParams p;
     int grid = 0;
+    int ctas = 0;                // CTAs of a stream-K schedule
     size_t smem = 0;
 };
 
@@ -64,6 +69,9 @@ size_t tc_gemm_smem_bytes(int bn, int stages);
 int tc_gemm_stages_for(int bn);
 int tc_gemm_ctas_per_sm(int bn, int stages);
 int choose_splits(int tiles, int n_kb, int slots);
+// Stream-K schedule over `ctas` CTAs: segs holds 4 ints per segment.
+void stream_k_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, std::vector<int> &cta_first,
+                       std::vector<int> &tile_planes);
 
 // Fill grid/smem of a plan whose params are set.
 void tc_gemm_finalize(TcGemm &g);
@@ -79,18 +87,28 @@ cudaError_t reduce_splits_launch(const float *part, int splits, long long stride
 template <typename T>
 cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, const T *gain, float eps, float *h,
                               T *xn, long long lo_off, cudaStream_t s);
-// Rotated q (fp32) and the rows' K/V into the fp32 cache at slots P + r.
-cudaError_t qkv_rope_launch(const float *part, int S, long long sstride, int ldp, int nrows, int nh, int nkv, int hd,
-                            const float2 *rope, int P, const int *depth, float *q, float *kc, float *vc, int max_seq,
-                            cudaStream_t s);
+// GEMM outputs arrive as fp32 partial planes part[plane][row][col] (plane
+// stride sstride, row stride ldp); column col belongs to 128-wide tile
+// col >> 7, which has planes[tile] planes (all 1 when planes is null).
+// Consumers add them in plane order.
+//
+// Rotated q (fp32) and the rows' K/V into the fp32 cache at slots P + r;
+// q, k, v columns start at 0, k_off, v_off.
+cudaError_t qkv_rope_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows, int nh,
+                            int nkv, int hd, int k_off, int v_off, const float2 *rope, int P, const int *depth,
+                            float *q, float *kc, float *vc, int max_seq, cudaStream_t s);
 template <typename T>
-cudaError_t resid_norm_launch(float *h, const float *part, int S, long long sstride, int ldp, int d, const T *gain,
-                              float eps, const int *row_map, int nrows, T *xout, long long lo_off, cudaStream_t s);
+cudaError_t resid_norm_launch(float *h, const float *part, const int *planes, long long sstride, int ldp, int d,
+                              const T *gain, float eps, const int *row_map, int nrows, T *xout, long long lo_off,
+                              cudaStream_t s);
+// gate columns [0, F), up columns [up_off, up_off + F).
 template <typename T>
-cudaError_t swiglu_launch(const float *part, int S, long long sstride, int ldp, int nrows, int F, T *out,
-                          long long lo_off, cudaStream_t s);
-cudaError_t argmax_launch(const float *logits, int rows, int V, float invT, int *amax, float *lmax, float *lsum,
-                          cudaStream_t s);
+cudaError_t swiglu_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows, int F,
+                          int up_off, T *out, long long lo_off, cudaStream_t s);
+// Sums the lm_head planes into logits[rows][V], then per row the argmax
+// (lowest id among equals), the max, and sum exp((l - max) * invT) if invT > 0.
+cudaError_t argmax_launch(const float *part, const int *planes, long long sstride, int ldp, float *logits, int rows,
+                          int V, float invT, int *amax, float *lmax, float *lsum, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention
 // Keys of row r: the cached prefix [0, P) plus in-step rows.  In tree mode the

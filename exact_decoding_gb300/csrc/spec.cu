@@ -120,6 +120,8 @@ __device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int 
 
 // ------------------------------------------------------------------ candidate lookup + step rows
 __global__ void __launch_bounds__(256) k_build_rows(SpecDev d) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int s_g;
     __shared__ int s_c[32 * 8];
     const int L = d.N - 1;
@@ -240,6 +242,8 @@ __device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, co
 constexpr int kFinishThreads = 1024;
 
 __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int s_acc[8];
     __shared__ int s_A, s_win, s_need_draw, s_dist_u, s_nrej;
     __shared__ int s_rej[32];
@@ -366,6 +370,8 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
 // Copy K/V of the winning candidate's rows m = 1..A-1 (slot P_old + its row)
 // to slots P_old + m.  Row 0 already sits at P_old.
 __global__ void k_kv_commit(SpecDev d, float *cache, int nkv, int hd) {
+    pdl_trigger();
+    pdl_wait();
     const int A = d.st->A, cs = d.st->cstar, P0 = d.st->P_old;
     if (A <= 1 || cs < 0) return;
     const int L = d.N - 1;
@@ -380,18 +386,24 @@ __global__ void k_kv_commit(SpecDev d, float *cache, int nkv, int hd) {
 
 // ------------------------------------------------------------------ pool seeding / import
 __global__ void k_pool_insert(SpecDev d, const int *records, int n) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x;
     const int N = d.N;
     for (int i = 0; i < n; ++i) pool_insert_warp(d, records[i * N], records + i * N + 1, lane);
 }
 
 __global__ void k_pool_seed_prompt(SpecDev d, int n) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x;
     const int N = d.N;
     for (int i = 0; i + N <= n; ++i) pool_insert_warp(d, d.tokens_log[i], d.tokens_log + i + 1, lane);
 }
 
 __global__ void __launch_bounds__(kFinishThreads) k_first_token(SpecDev d, int n) {
+    pdl_trigger();
+    pdl_wait();
     int y;
     if (d.T <= 0.f) {
         y = d.amax[0];
@@ -412,29 +424,29 @@ __global__ void __launch_bounds__(kFinishThreads) k_first_token(SpecDev d, int n
 
 // ------------------------------------------------------------------ launchers
 cudaError_t build_rows_launch(const SpecDev &d, cudaStream_t s) {
-    k_build_rows<<<1, 256, 0, s>>>(d);
+    launch_k(k_build_rows, dim3(1), dim3(256), 0, s, d);
     return cudaGetLastError();
 }
 cudaError_t finish_step_launch(const SpecDev &d, cudaStream_t s) {
-    k_finish_step<<<1, kFinishThreads, 0, s>>>(d);
+    launch_k(k_finish_step, dim3(1), dim3(kFinishThreads), 0, s, d);
     return cudaGetLastError();
 }
 cudaError_t kv_commit_launch(const SpecDev &d, float *cache, int L, int nkv, int hd, cudaStream_t s) {
-    k_kv_commit<<<L * 2 * nkv, 128, 0, s>>>(d, cache, nkv, hd);
+    launch_k(k_kv_commit, dim3(L * 2 * nkv), dim3(128), 0, s, d, cache, nkv, hd);
     return cudaGetLastError();
 }
 
 cudaError_t pool_insert_launch(const SpecDev &d, const int *records, int n, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    k_pool_insert<<<1, 32, 0, s>>>(d, records, n);
+    launch_k(k_pool_insert, dim3(1), dim3(32), 0, s, d, records, n);
     return cudaGetLastError();
 }
 cudaError_t pool_seed_prompt_launch(const SpecDev &d, int n, cudaStream_t s) {
-    k_pool_seed_prompt<<<1, 32, 0, s>>>(d, n);
+    launch_k(k_pool_seed_prompt, dim3(1), dim3(32), 0, s, d, n);
     return cudaGetLastError();
 }
 cudaError_t first_token_launch(const SpecDev &d, int n, cudaStream_t s) {
-    k_first_token<<<1, kFinishThreads, 0, s>>>(d, n);
+    launch_k(k_first_token, dim3(1), dim3(kFinishThreads), 0, s, d, n);
     return cudaGetLastError();
 }
 

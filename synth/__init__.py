@@ -108,6 +108,10 @@ WORKLOADS: Dict[str, Workload] = {
                                       temperature=1.0, prompt_as_reference=True, prompt_chunk=64),
     "codellama13b-bf16-greedy": Workload("codellama13b-bf16-greedy", CODELLAMA13B, 2048, 5, 10, 10, 512),
     "llama70b-bf16-greedy": Workload("llama70b-bf16-greedy", LLAMA70B, 512, 5, 5, 5, 128),
+    # 7B layer shapes with 2 layers (about 1.3 GB of weights): small enough
+    # for full-counter kernel profiles, same per-launch GEMM/attention shapes.
+    "llama7b-2layer-bf16-greedy": Workload("llama7b-2layer-bf16-greedy", dataclasses.replace(LLAMA7B, n_layers=2),
+                                           256, 5, 15, 15, 256),
 }
 
 
