@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs = [os.path.join(BUILD_DIR, s.replace(".cu", ".o")) for s in SOURCES]
     if force or jobs or not os.path.exists(LIB):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
+        run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-Xlinker", "--no-undefined"])
         os.replace(tmp, LIB)
     return LIB
 

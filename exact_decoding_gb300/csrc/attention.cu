@@ -290,8 +290,6 @@ __global__ void __launch_bounds__(128) k_attn_tc(const float *q, const float *kc
     __nv_bfloat16 *Kl = Kh + kTcChunk * LD;
     __nv_bfloat16 *Vh = Kl + kTcChunk * LD;
     __nv_bfloat16 *Vl = Vh + kTcChunk * LD;
-    __nv_bfloat16 *Qh = Vl + kTcChunk * LD;      // [kTcQ][LD] each
-    __nv_bfloat16 *Ql = Qh + kTcQ * LD;
 
     const int kvh = blockIdx.x, chunk = blockIdx.y, qb = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -302,45 +300,67 @@ __global__ void __launch_bounds__(128) k_attn_tc(const float *q, const float *kc
     const int slot0 = step_chunk ? P + key0 : key0;
     const int nkeys = step_chunk ? min(kTcChunk, nrows - key0) : min(kTcChunk, P - key0);
 
-    // K / V chunk -> shared hi/lo planes (keys past the chunk are zero)
-    const float *kb = kc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
-    const float *vb = vc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
-    for (int t = tid; t < kTcChunk * (HD / 4); t += 128) {
-        const int key = t / (HD / 4), c = (t % (HD / 4)) * 4;
-        float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
-        if (key < nkeys) {
-            kx = *reinterpret_cast<const float4 *>(kb + static_cast<long long>(key) * HD + c);
-            vx = *reinterpret_cast<const float4 *>(vb + static_cast<long long>(key) * HD + c);
+    // K / V chunk -> shared hi/lo planes (keys past the chunk are zero).
+    // All of a thread's loads are issued before any conversion.  Plain
+    // (coherent) loads: with programmatic dependent launch this kernel's
+    // lifetime overlaps the kernel that writes q, K and V, so the
+    // read-only cache path must not be used for them.
+    {
+        const float *kb = kc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
+        const float *vb = vc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
+        constexpr int PER = kTcChunk * (HD / 4) / 128;   // float4 per thread per tensor
+        float4 kx[PER], vx[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int t = tid + j * 128;
+            const int key = t / (HD / 4), c = (t % (HD / 4)) * 4;
+            if (key < nkeys) {
+                kx[j] = *reinterpret_cast<const float4 *>(kb + static_cast<long long>(key) * HD + c);
+                vx[j] = *reinterpret_cast<const float4 *>(vb + static_cast<long long>(key) * HD + c);
+            } else {
+                kx[j] = vx[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
-        uint2 h, l;
-        split2(kx.x, kx.y, h.x, l.x);
-        split2(kx.z, kx.w, h.y, l.y);
-        *reinterpret_cast<uint2 *>(Kh + key * LD + c) = h;
-        *reinterpret_cast<uint2 *>(Kl + key * LD + c) = l;
-        split2(vx.x, vx.y, h.x, l.x);
-        split2(vx.z, vx.w, h.y, l.y);
-        *reinterpret_cast<uint2 *>(Vh + key * LD + c) = h;
-        *reinterpret_cast<uint2 *>(Vl + key * LD + c) = l;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int t = tid + j * 128;
+            const int key = t / (HD / 4), c = (t % (HD / 4)) * 4;
+            uint2 h, l;
+            split2(kx[j].x, kx[j].y, h.x, l.x);
+            split2(kx[j].z, kx[j].w, h.y, l.y);
+            *reinterpret_cast<uint2 *>(Kh + key * LD + c) = h;
+            *reinterpret_cast<uint2 *>(Kl + key * LD + c) = l;
+            split2(vx[j].x, vx[j].y, h.x, l.x);
+            split2(vx[j].z, vx[j].w, h.y, l.y);
+            *reinterpret_cast<uint2 *>(Vh + key * LD + c) = h;
+            *reinterpret_cast<uint2 *>(Vl + key * LD + c) = l;
+        }
     }
-    // Q block -> shared hi/lo planes (scaled by 1/sqrt(hd))
+    // This warp's 16 query vectors: A fragments straight from global memory
+    // (fp32, scaled, split into hi/lo), rows ra = lane/4 and rb = ra + 8.
+    const int qv0 = qb * kTcQ + warp * 16;
+    const int qa_v = qv0 + (lane >> 2), qb_v = qa_v + 8;
+    const int ra = qa_v < QV ? qa_v / gq : -1, rb = qb_v < QV ? qb_v / gq : -1;
     const float scale = rsqrtf(static_cast<float>(HD));
-    for (int t = tid; t < kTcQ * (HD / 4); t += 128) {
-        const int i = t / (HD / 4), c = (t % (HD / 4)) * 4;
-        const int qv = qb * kTcQ + i;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (qv < QV) {
-            const int r = qv / gq, hq = kvh * gq + qv % gq;
-            x = *reinterpret_cast<const float4 *>(q + (static_cast<long long>(r) * nh + hq) * HD + c);
+    uint32_t qh[HD / 16][4], ql[HD / 16][4];
+    {
+        const float *qpa = ra >= 0 ? q + (static_cast<long long>(ra) * nh + kvh * gq + qa_v % gq) * HD : nullptr;
+        const float *qpb = rb >= 0 ? q + (static_cast<long long>(rb) * nh + kvh * gq + qb_v % gq) * HD : nullptr;
+        const int c0 = 2 * (lane & 3);
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks) {
+            const int c = ks * 16 + c0;
+            const float2 a0 = qpa ? *reinterpret_cast<const float2 *>(qpa + c) : make_float2(0.f, 0.f);
+            const float2 a2 = qpa ? *reinterpret_cast<const float2 *>(qpa + c + 8) : make_float2(0.f, 0.f);
+            const float2 b0 = qpb ? *reinterpret_cast<const float2 *>(qpb + c) : make_float2(0.f, 0.f);
+            const float2 b2 = qpb ? *reinterpret_cast<const float2 *>(qpb + c + 8) : make_float2(0.f, 0.f);
+            split2(a0.x * scale, a0.y * scale, qh[ks][0], ql[ks][0]);
+            split2(b0.x * scale, b0.y * scale, qh[ks][1], ql[ks][1]);
+            split2(a2.x * scale, a2.y * scale, qh[ks][2], ql[ks][2]);
+            split2(b2.x * scale, b2.y * scale, qh[ks][3], ql[ks][3]);
         }
-        uint2 h, l;
-        split2(x.x * scale, x.y * scale, h.x, l.x);
-        split2(x.z * scale, x.w * scale, h.y, l.y);
-        *reinterpret_cast<uint2 *>(Qh + i * LD + c) = h;
-        *reinterpret_cast<uint2 *>(Ql + i * LD + c) = l;
     }
     __syncthreads();
-
-    const int qv0 = qb * kTcQ + warp * 16;
     if (qv0 >= QV) return;   // whole warp past the last query (no later block-wide sync)
 
     // S = Q K^T : 16 queries x 64 keys (8 n-tiles of 8 keys), three passes
@@ -348,32 +368,25 @@ __global__ void __launch_bounds__(128) k_attn_tc(const float *q, const float *kc
 #pragma unroll
     for (int j = 0; j < kTcChunk / 8; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
     {
-        const int qrow = warp * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-        const int qcol = 8 * (lane >> 4);
         const int krow = (lane & 7) + 8 * (lane >> 4);
         const int kcol = 8 * ((lane >> 3) & 1);
 #pragma unroll
         for (int ks = 0; ks < HD / 16; ++ks) {
-            uint32_t ah[4], al[4];
-            ldsm_x4(smem_u32(Qh + qrow * LD + ks * 16 + qcol), ah[0], ah[1], ah[2], ah[3]);
-            ldsm_x4(smem_u32(Ql + qrow * LD + ks * 16 + qcol), al[0], al[1], al[2], al[3]);
 #pragma unroll
             for (int np = 0; np < kTcChunk / 16; ++np) {
                 uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
                 ldsm_x4(smem_u32(Kh + (np * 16 + krow) * LD + ks * 16 + kcol), h0, h1, h2, h3);
                 ldsm_x4(smem_u32(Kl + (np * 16 + krow) * LD + ks * 16 + kcol), l0, l1, l2, l3);
-                mma_bf16(sacc[2 * np], ah, h0, h1);
-                mma_bf16(sacc[2 * np], ah, l0, l1);
-                mma_bf16(sacc[2 * np], al, h0, h1);
-                mma_bf16(sacc[2 * np + 1], ah, h2, h3);
-                mma_bf16(sacc[2 * np + 1], ah, l2, l3);
-                mma_bf16(sacc[2 * np + 1], al, h2, h3);
+                mma_bf16(sacc[2 * np], qh[ks], h0, h1);
+                mma_bf16(sacc[2 * np], qh[ks], l0, l1);
+                mma_bf16(sacc[2 * np], ql[ks], h0, h1);
+                mma_bf16(sacc[2 * np + 1], qh[ks], h2, h3);
+                mma_bf16(sacc[2 * np + 1], qh[ks], l2, l3);
+                mma_bf16(sacc[2 * np + 1], ql[ks], h2, h3);
             }
         }
     }
-    // mask + softmax (rows ra = lane/4 and rb = ra + 8 of this warp's 16)
-    const int qa_v = qv0 + (lane >> 2), qb_v = qa_v + 8;
-    const int ra = qa_v < QV ? qa_v / gq : -1, rb = qb_v < QV ? qb_v / gq : -1;
+    // mask + softmax
     float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kTcChunk / 8; ++j) {
@@ -501,7 +514,7 @@ cudaError_t attention_tc_hd(const AttnArgs &a, cudaStream_t s) {
     const int nch_prefix = (a.P + kTcChunk - 1) / kTcChunk;
     const int nch = nch_prefix + (a.nrows + kTcChunk - 1) / kTcChunk;
     const int gq = a.nh / a.nkv;
-    const size_t smem = static_cast<size_t>(4 * kTcChunk + 2 * kTcQ) * (HD + 8) * sizeof(__nv_bfloat16);
+    const size_t smem = static_cast<size_t>(4 * kTcChunk) * (HD + 8) * sizeof(__nv_bfloat16);
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
