@@ -124,6 +124,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def gemm_traffic():
+    """DRAM bytes per k_gemm_tc launch from the committed ncu summary, or None
+    when the kernel sources changed since those counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "k_gemm_tc_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    rec = dict(line.split() for line in open(path) if line.strip())
+    csrc = os.path.join(ROOT, "exact_decoding_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "la_common.cuh", "la_kernels.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != rec.get("gemm_source_fp"):
+        return None
+    return float(rec["traffic_bytes_per_launch"])
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -332,7 +350,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "gpu_launches": int(launches),
         "roofline": {"bound": "hbm", "kernel": "k_gemm_tc (tcgen05 projection GEMM, all launches of a step)",
                      "achieved": gemm_gbs, "peak": peak, "unit": "GB/s",
-                     "frac": (gemm_gbs / peak) if gemm_gbs else None, "traffic": None,
+                     "frac": (gemm_gbs / peak) if gemm_gbs else None, "traffic": gemm_traffic(),
                      "peak_source": peak_kind, "launch_ms": pst["gemm_ms"] / max(pst["gemm_launches"], 1),
                      "bytes_per_launch": pst["gemm_bytes"] / max(pst["gemm_launches"], 1),
                      "share_of_step": pst["gemm_ms"] / max(pst["steps"], 1) / ms_per_step},
