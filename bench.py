@@ -223,6 +223,20 @@ def run_reference(args, wl):
     return line
 
 
+def combine_ranks(accepted: float, total_ms: float, world: int, device: str = "cpu"):
+    """Whole-job figures for N independent replicas (one per rank): committed
+    tokens summed over ranks, timed region = the slowest rank's."""
+    if world <= 1:
+        return float(accepted), float(total_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(accepted)], dtype=torch.float64, device=device)
+    m = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    dist.all_reduce(m, op=dist.ReduceOp.MAX)
+    return float(t[0]), float(m[0])
+
+
 def log(*a):
     print("[bench]", *a, file=sys.stderr, flush=True)
 
@@ -305,17 +319,10 @@ def run_ours(args, wl, rank, world, local_rank):
     pst = pdec.stats()
     pdec.close()
     log(f"profile: gemm {pst['gemm_ms']:.2f} ms / {pst['gemm_launches']} launches, "
-        f"attn {pst['attn_ms']:.2f} ms / {pst['attn_launches']}, steps {pst['steps']}")
+        f"attn {pst['attn_ms']:.2f} ms / {pst['attn_launches']}, row-wise {pst['elem_ms']:.2f} ms, "
+        f"speculation {pst['spec_ms']:.2f} ms, steps {pst['steps']}")
 
-    tot = torch.tensor([float(accepted), total_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        acc_t = tot.clone()
-        torch.distributed.all_reduce(acc_t[:1], op=torch.distributed.ReduceOp.SUM)
-        mx = tot.clone()
-        torch.distributed.all_reduce(mx[1:], op=torch.distributed.ReduceOp.MAX)
-        accepted_all, max_ms = float(acc_t[0]), float(mx[1])
-    else:
-        accepted_all, max_ms = float(accepted), total_ms
+    accepted_all, max_ms = combine_ranks(accepted, total_ms, world, device="cuda")
     if rank != 0:
         dec.close()
         return None
@@ -359,6 +366,7 @@ def run_ours(args, wl, rank, world, local_rank):
                           "roofline_ms": step_bytes / (peak * 1e9) * 1e3},
         "attention": {"achieved": attn_gbs, "unit": "GB/s",
                       "ms_per_step": pst["attn_ms"] / max(pst["steps"], 1)},
+        "breakdown_ms_per_step": {k: pst[k + "_ms"] / max(pst["steps"], 1) for k in ("gemm", "attn", "elem", "spec")},
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and not args.ncu and world == 1:
@@ -382,15 +390,16 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        # CPU oracle arm: rank 0 alone works and prints; other ranks exit 0.
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl)), flush=True)
+        return
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    if args.impl == "reference":
-        if rank == 0:
-            print(json.dumps(run_reference(args, wl)), flush=True)
-        return
+        dist.init_process_group("nccl")
     import synth as _s
     _s.build_generator()
     from exact_decoding_gb300 import build as b

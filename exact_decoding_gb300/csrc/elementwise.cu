@@ -57,10 +57,19 @@ cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, 
 // part: [S][nrows][ldp] with q | k | v columns.  Row r sits at position
 // P + depth[r] (P + r when depth is null) and its K/V go to cache slot P + r.
 // One thread per work item: a rotated (q or k) pair, or one v element.
+// Partial planes of column col, added in plane order.  Beyond two planes the
+// loads go out in predicated batches of 4 so that they are in flight together.
 __device__ __forceinline__ float sum_planes(const float *pr, const int *planes, long long sstride, int col) {
     const int n = planes ? planes[col >> 7] : 1;
-    float v = pr[col];
-    for (int sp = 1; sp < n; ++sp) v += pr[sp * sstride + col];
+    if (n <= 2) return n == 2 ? pr[col] + pr[sstride + col] : pr[col];
+    float v = 0.f;
+    for (int b = 0; b < n; b += 4) {
+        float x[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[j] = (b + j < n) ? pr[(b + j) * sstride + col] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v += x[j];
+    }
     return v;
 }
 
@@ -138,12 +147,19 @@ __global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part
         if (c < d4) {
             float4 a = hr[c];
             const int np = planes ? planes[(4 * c) >> 7] : 1;
-            for (int sp = 0; sp < np; ++sp) {
-                const float4 b = *reinterpret_cast<const float4 *>(pr + sp * sstride + 4 * c);
-                a.x += b.x;
-                a.y += b.y;
-                a.z += b.z;
-                a.w += b.w;
+            for (int b0 = 0; b0 < np; b0 += 8) {
+                float4 x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    x[j] = (b0 + j < np) ? *reinterpret_cast<const float4 *>(pr + (b0 + j) * sstride + 4 * c)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    a.x += x[j].x;
+                    a.y += x[j].y;
+                    a.z += x[j].z;
+                    a.w += x[j].w;
+                }
             }
             v[j] = a;
             hr[c] = a;

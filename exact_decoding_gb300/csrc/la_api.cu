@@ -109,8 +109,9 @@ struct la_handle {
     std::vector<int> ev_cls;
     std::vector<double> ev_bytes;
     int ev_used = 0;
-    double prof_ms[2] = {0, 0}, prof_bytes[2] = {0, 0};
-    int64_t prof_launches[2] = {0, 0};
+    // classes: 0 GEMM, 1 attention, 2 row-wise kernels, 3 speculation kernels
+    double prof_ms[4] = {0, 0, 0, 0}, prof_bytes[4] = {0, 0, 0, 0};
+    int64_t prof_launches[4] = {0, 0, 0, 0};
     int64_t launches = 0;
 
     // host-side bookkeeping
@@ -351,17 +352,21 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
     const float eps = h->dims.rms_eps;
     h->launches += 1;
     const long long bh = h->bh(mode);
+    int pe = mode == STEP ? h->prof_begin() : -1;
     CK(embed_norm_launch<T>(static_cast<const T *>(h->embed), tok, nrows, h->d,
                             static_cast<const T *>(h->attn_norm[0]), eps, h->h, static_cast<T *>(h->xn), bh * h->d,
                             s));
+    h->prof_end(pe, 2, 0.0);
     const int nch = (P + kAttnChunk - 1) / kAttnChunk;
     for (int l = 0; l < h->L; ++l) {
         int rc;
         if ((rc = run_gemm(h, mode, QKV, l, nrows)) != LA_OK) return rc;
         const long long ss_qkv = static_cast<long long>(h->R) * h->ldo[QKV];
+        pe = mode == STEP ? h->prof_begin() : -1;
         CK(qkv_rope_launch(h->part, h->planes[mode][QKV], ss_qkv, h->ldo[QKV], nrows, h->nh, h->nkv, h->hd,
                            h->k_off, h->v_off, h->rope, P, mode == STEP ? h->depth : nullptr, h->q,
                            h->kv_layer(l, 0), h->kv_layer(l, 1), h->max_seq, s));
+        h->prof_end(pe, 2, 0.0);
         AttnArgs a{};
         a.q = h->q;
         a.kc = h->kv_layer(l, 0);
@@ -380,23 +385,28 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         a.vis_bits = mode == STEP ? h->vis_bits : nullptr;
         a.out = h->ao;
         a.out_lo_off = bh * h->qd;
-        const int pe = mode == STEP ? h->prof_begin() : -1;
+        pe = mode == STEP ? h->prof_begin() : -1;
         CK(attention_launch<T>(a, s));
         h->prof_end(pe, 1,
                     (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * 4.0 + 4.0 * nrows * h->qd + 4.0 * nrows * h->qd);
         h->launches += 1 + (h->bf16 ? 2 : 1 + (nch > 0 ? 1 : 0));   // qkv_rope, attention passes
         if ((rc = run_gemm(h, mode, OPROJ, l, nrows)) != LA_OK) return rc;
         const long long ss_d = static_cast<long long>(h->R) * h->ldo[OPROJ];
+        pe = mode == STEP ? h->prof_begin() : -1;
         CK(resid_norm_launch<T>(h->h, h->part, h->planes[mode][OPROJ], ss_d, h->ldo[OPROJ], h->d,
                                 static_cast<const T *>(h->ffn_norm[l]), eps, nullptr, nrows,
                                 static_cast<T *>(h->xn), bh * h->d, s));
+        h->prof_end(pe, 2, 0.0);
         if ((rc = run_gemm(h, mode, GATEUP, l, nrows)) != LA_OK) return rc;
         const long long ss_gu = static_cast<long long>(h->R) * h->ldo[GATEUP];
+        pe = mode == STEP ? h->prof_begin() : -1;
         CK(swiglu_launch<T>(h->part, h->planes[mode][GATEUP], ss_gu, h->ldo[GATEUP], nrows, h->F, h->up_off,
                             static_cast<T *>(h->fa), bh * h->F, s));
+        h->prof_end(pe, 2, 0.0);
         h->launches += 3;   // resid_norm after O, swiglu, resid_norm after down
         if ((rc = run_gemm(h, mode, DOWN, l, nrows)) != LA_OK) return rc;
         const long long ss_dn = static_cast<long long>(h->R) * h->ldo[DOWN];
+        pe = mode == STEP ? h->prof_begin() : -1;
         if (l + 1 < h->L) {
             CK(resid_norm_launch<T>(h->h, h->part, h->planes[mode][DOWN], ss_dn, h->ldo[DOWN], h->d,
                                     static_cast<const T *>(h->attn_norm[l + 1]), eps, nullptr, nrows,
@@ -408,6 +418,7 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
                                     static_cast<const T *>(h->final_norm), eps, map, rows,
                                     static_cast<T *>(h->xu), static_cast<long long>(h->bh_u) * h->d, s));
         }
+        h->prof_end(pe, 2, 0.0);
     }
     return LA_OK;
 }
@@ -888,7 +899,7 @@ static int la_prefill_impl(la_handle *h, const int32_t *prompt, int32_t n, int32
     h->logits_rows = 1;
     h->launches = 0;
     h->ev_used = 0;
-    for (int c = 0; c < 2; ++c) h->prof_ms[c] = h->prof_bytes[c] = 0, h->prof_launches[c] = 0;
+    for (int c = 0; c < 4; ++c) h->prof_ms[c] = h->prof_bytes[c] = 0, h->prof_launches[c] = 0;
     return LA_OK;
 }
 
@@ -905,15 +916,19 @@ int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     if (!h->prefilled) return fail(LA_ERR_STATE, "la_step before la_prefill");
     if (h->P + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "max_seq reached");
     cudaStream_t s = h->stream;
+    int pe = h->prof_begin();
     CK(build_rows_launch(h->spec(), s));
+    h->prof_end(pe, 3, 0.0);
     int rc = forward_any(h, STEP, h->tok, h->M, h->P, true);
     if (rc != LA_OK) return rc;
     if ((rc = run_lm_head(h, h->U, true)) != LA_OK) return rc;
+    pe = h->prof_begin();
     CK(argmax_launch(h->lm_part, h->planes_lm, h->lm_stride, h->ldo_lm, h->logits, h->U, h->V,
                      h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
                      h->lmax, h->lsum, s));
     CK(finish_step_launch(h->spec(), s));
     if ((rc = kv_commit(h)) != LA_OK) return rc;
+    h->prof_end(pe, 3, 0.0);
     h->launches += 4;   // build_rows, argmax, finish_step, kv_commit
     CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));
@@ -970,6 +985,8 @@ int la_stats(const la_handle *h, la_stats_t *o) {
     o->attn_bytes = h->prof_bytes[1];
     o->attn_launches = h->prof_launches[1];
     o->kernel_launches = h->launches;
+    o->elem_ms = h->prof_ms[2];
+    o->spec_ms = h->prof_ms[3];
     return LA_OK;
 }
 

@@ -54,7 +54,7 @@ class la_stats_t(ctypes.Structure):
                 ("last_candidates", ctypes.c_int32), ("prefix_len", ctypes.c_int32), ("rows", ctypes.c_int32),
                 ("gemm_ms", ctypes.c_double), ("gemm_bytes", ctypes.c_double), ("gemm_launches", ctypes.c_int64),
                 ("attn_ms", ctypes.c_double), ("attn_bytes", ctypes.c_double), ("attn_launches", ctypes.c_int64),
-                ("kernel_launches", ctypes.c_int64)]
+                ("kernel_launches", ctypes.c_int64), ("elem_ms", ctypes.c_double), ("spec_ms", ctypes.c_double)]
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)

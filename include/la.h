@@ -127,6 +127,8 @@ typedef struct la_stats_t {
     double  attn_bytes;
     int64_t attn_launches;
     int64_t kernel_launches;  /* kernels launched by la_step calls since la_prefill */
+    double  elem_ms;          /* profile: row-wise kernels (embedding, norms, rotary/KV write, SwiGLU) */
+    double  spec_ms;          /* profile: lookup, argmax, verification/pool/window, KV commit */
 } la_stats_t;
 
 /* Host-side snapshot of the decoding state, for resume and for checking a
