@@ -238,6 +238,232 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
     }
 }
 
+// ------------------------------------------------------------------ 2-SM (cta_group::2) kernel
+// A cluster of two CTAs computes a 256-feature tile: UMMA M = 256 weight rows
+// (128 in each CTA's shared memory), N = 256 input rows (hi rows 0..127 held
+// by rank 0, lo rows 128..255 by rank 1), K = 16.  Rank 0 issues every MMA;
+// both CTAs' TMA loads complete on rank 0's full barrier; the MMA commits are
+// multicast to both CTAs.  Each CTA's TMEM holds D for its 128 weight rows
+// (columns c = hi row c, c + 128 = lo row c), drained by its own epilogue.
+// Compared with the 1-SM kernel, a shared-memory stage per SM is half as
+// large (16 KB weights + 16 KB rows) and one MMA covers twice the weights.
+__global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcGemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    constexpr uint32_t a_bytes = kTileM * kBlockK * 2;     // 128 weight rows
+    constexpr uint32_t b_bytes = kTileM * kBlockK * 2;     // 128 input rows (this CTA's half)
+    constexpr uint32_t stage_bytes = a_bytes + b_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * stage_bytes);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + p.stages;
+    uint64_t *accfull = bars + 2 * p.stages;       // [2]
+    uint64_t *accempty = bars + 2 * p.stages + 2;  // [2]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.stages + 4);
+
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int sbeg = p.cta_first[pair], send = p.cta_first[pair + 1];
+    constexpr uint32_t ncols = 512;   // two 256-column accumulators
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.stages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&accfull[b]), 1);
+            mbar_init(smem_u32(&accempty[b]), 8);    // 4 epilogue warps in each CTA
+        }
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), ncols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();   // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int sg = 0; sg < p.nseg; ++sg) prefetch_tensormap(&p.a[sg]);
+            prefetch_tensormap(&p.b);
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            const int brow = static_cast<int>(rank) * kTileM;   // hi rows (rank 0) or lo rows (rank 1)
+            auto weight_row = [&](const SegInfo &g) { return 2 * g.row0 + static_cast<int>(rank) * kTileM; };
+            int it = 0;
+            for (int i = sbeg; i < send && it < p.stages; ++i) {
+                const SegInfo g = segment(p, i);
+                for (int kb = g.kb0; kb < g.kb1 && it < p.stages; ++kb, ++it) {
+                    const uint32_t fl = mapa_shared(smem_u32(&full[it]), 0);
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full[it]), 2 * stage_bytes);
+                    tma_load_2d_pair(smem_u32(smem + it * stage_bytes), &p.a[g.seg], kb * kBlockK, weight_row(g), fl,
+                                     pol_w);
+                }
+            }
+            const int npre = it;
+            pdl_wait();
+            it = 0;
+            bool ok = true;
+            for (int i = sbeg; i < send && ok; ++i) {
+                const SegInfo g = segment(p, i);
+                for (int kb = g.kb0; kb < g.kb1; ++kb, ++it) {
+                    const int st = it % p.stages;
+                    const uint32_t sa = smem_u32(smem + st * stage_bytes);
+                    const uint32_t fl = mapa_shared(smem_u32(&full[st]), 0);
+                    if (it < npre) {
+                        tma_load_2d_pair(sa + a_bytes, &p.b, kb * kBlockK, brow, fl, pol_x);
+                        continue;
+                    }
+                    if (!mbar_wait_cluster(smem_u32(&empty[st]), ((it / p.stages) & 1) ^ 1, p.err, ERR_TIMEOUT_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&full[st]), 2 * stage_bytes);
+                    tma_load_2d_pair(sa, &p.a[g.seg], kb * kBlockK, weight_row(g), fl, pol_w);
+                    tma_load_2d_pair(sa + a_bytes, &p.b, kb * kBlockK, brow, fl, pol_x);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // Pair UMMA issuer: M = 256, N = 256, 4 k-steps of 16 per k-block.
+            const uint32_t idesc = umma_idesc_bf16(2 * kTileM, 2 * kTileM);
+            int it = 0, ul = 0;
+            bool ok = true;
+            for (int i = sbeg; i < send; ++i, ++ul) {
+                const SegInfo g = segment(p, i);
+                const int buf = ul & 1;
+                if (ok && ul >= 2)
+                    ok = mbar_wait_cluster(smem_u32(&accempty[buf]), ((ul >> 1) & 1) ^ 1, p.err, ERR_TIMEOUT_ACCUM);
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(buf * 2 * kTileM);
+                for (int kb = g.kb0; kb < g.kb1 && ok; ++kb, ++it) {
+                    const int st = it % p.stages;
+                    if (!mbar_wait_cluster(smem_u32(&full[st]), (it / p.stages) & 1, p.err, ERR_TIMEOUT_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + st * stage_bytes);
+                    const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + a_bytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / 16; ++kk)
+                        umma_pair_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (kb != g.kb0 || kk != 0) ? 1u : 0u);
+                    umma_pair_commit(smem_u32(&empty[st]), 0x3);
+                }
+                umma_pair_commit(smem_u32(&accfull[buf]), 0x3);
+            }
+        }
+    } else {
+        // Epilogue: TMEM lanes 32*(w%4).. = this CTA's weight rows; columns c
+        // and c + 128 are the hi and lo input row c.
+        const int q = warp & 3;
+        const uint32_t acc_leader[2] = {mapa_shared(smem_u32(&accempty[0]), 0), mapa_shared(smem_u32(&accempty[1]), 0)};
+        int ul = 0;
+        for (int i = sbeg; i < send; ++i, ++ul) {
+            const SegInfo g = segment(p, i);
+            const int buf = ul & 1;
+            bool ok = mbar_wait_cluster(smem_u32(&accfull[buf]), (ul >> 1) & 1, p.err, ERR_TIMEOUT_ACCUM);
+            ok = __all_sync(0xffffffffu, ok);
+            __syncwarp();
+            tc_fence_after();
+            if (!ok) break;
+            const int f = 2 * g.row0 + static_cast<int>(rank) * kTileM + 32 * q + lane;
+            const bool fv = f < p.seg_out[g.seg];
+            float *out = p.out + static_cast<long long>(g.plane) * p.split_stride + p.seg_col0[g.seg] + f;
+            const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * 2 * kTileM);
+            for (int c0 = 0; c0 < kTileM; c0 += 32) {
+                uint32_t r[32], s2[32];
+                tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0), r);
+                tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0 + kTileM), s2);
+                tmem_ld_wait();
+                if (fv && c0 < p.nrows) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int row = c0 + j;
+                        if (row < p.nrows)
+                            out[static_cast<long long>(row) * p.ldo] = __uint_as_float(r[j]) + __uint_as_float(s2[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_leader[buf]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // the leader's MMAs read both CTAs' shared memory: finish together
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, ncols);
+    }
+}
+
+size_t tc_gemm2_smem_bytes(int stages) {
+    return static_cast<size_t>(stages) * (2 * kTileM * kBlockK * 2) + 1024 + 256;
+}
+
+int tc_gemm2_stages() {
+    return static_cast<int>((200 * 1024) / (2 * kTileM * kBlockK * 2));   // 6
+}
+
+static cudaError_t gemm2_smem_attr() {
+    static int done = 0;
+    if (done) return cudaSuccess;
+    int dev = 0, mx = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) done = 1;
+    return e;
+}
+
+int tc_gemm2_max_pairs() {
+    if (gemm2_smem_attr() != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 512);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = tc_gemm2_smem_bytes(tc_gemm2_stages());
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc2, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+cudaError_t tc_gemm2_launch(const TcGemm &g, cudaStream_t s) {
+    cudaError_t e = gemm2_smem_attr();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * g.ctas);
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = g.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc2, g.p);
+}
+
 size_t tc_gemm_smem_bytes(int bn, int stages) {
     return static_cast<size_t>(stages) * (kTileM * kBlockK * 2 + bn * kBlockK * 2) + 1024 + 256;
 }
@@ -317,11 +543,18 @@ int choose_splits(int tiles, int n_kb, int slots) {
 }
 
 void tc_gemm_finalize(TcGemm &g) {
+    if (g.pair) {
+        g.p.stages = tc_gemm2_stages();
+        g.grid = 2 * g.ctas;
+        g.smem = tc_gemm2_smem_bytes(g.p.stages);
+        return;
+    }
     g.grid = g.p.segs ? g.ctas : g.p.seg_tile0[g.p.nseg] * g.p.splits;
     g.smem = tc_gemm_smem_bytes(g.p.bn, g.p.stages);
 }
 
 cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s) {
+    if (g.pair) return tc_gemm2_launch(g, s);
     cudaError_t e = gemm_smem_attr();
     if (e != cudaSuccess) return e;
     launch_k(k_gemm_tc, dim3(g.grid), dim3(192), g.smem, s, g.p);

@@ -468,10 +468,23 @@ int reset_pool(la_handle *h) {
     return LA_OK;
 }
 
-// Uploads one stream-K schedule; returns the device tables and max planes.
-int upload_schedule(la_handle *h, int tiles, int n_kb, int ctas, TcGemm &g, int **planes_dev, int *max_planes) {
-    std::vector<int> segs, first, planes;
-    stream_k_schedule(tiles, n_kb, ctas, segs, first, planes);
+// Uploads one stream-K schedule over tile groups (tp consecutive 128-row
+// weight tiles of one matrix: a 256-feature tile of the 2-SM kernel when
+// tp = 2); returns per-128-column-tile plane counts for the consumers, the
+// max plane count and each matrix's first group.
+int upload_schedule(la_handle *h, const int *tiles, int nseg, int tp, int n_kb, int ctas, TcGemm &g,
+                    int **planes_dev, int *max_planes, int *group0) {
+    int ngroups = 0;
+    for (int i = 0; i < nseg; ++i) {
+        group0[i] = ngroups;
+        ngroups += (tiles[i] + tp - 1) / tp;
+    }
+    group0[nseg] = ngroups;
+    std::vector<int> segs, first, gplanes;
+    stream_k_schedule(ngroups, n_kb, ctas, segs, first, gplanes);
+    std::vector<int> planes;   // per 128-column tile, in column order
+    for (int i = 0; i < nseg; ++i)
+        for (int t = 0; t < tiles[i]; ++t) planes.push_back(gplanes[group0[i] + t / tp]);
     int *dsegs = nullptr, *dfirst = nullptr, *dplanes = nullptr;
     int rc;
     if ((rc = h->alloc(&dsegs, segs.size())) != LA_OK || (rc = h->alloc(&dfirst, first.size())) != LA_OK ||
@@ -484,7 +497,7 @@ int upload_schedule(la_handle *h, int tiles, int n_kb, int ctas, TcGemm &g, int 
     g.p.cta_first = dfirst;
     g.ctas = static_cast<int>(first.size()) - 1;
     *planes_dev = dplanes;
-    *max_planes = *std::max_element(planes.begin(), planes.end());
+    *max_planes = *std::max_element(gplanes.begin(), gplanes.end());
     return LA_OK;
 }
 
@@ -497,15 +510,16 @@ int build_plans(la_handle *h) {
     void *xs[4] = {h->xn, h->ao, h->xn, h->fa};
     const int Ks[4] = {h->d, h->qd, h->d, h->F};
     size_t part_max = 0;
+    // 2-SM UMMA over 256-feature tiles, one CTA pair per two SMs.
+    int pairs = std::min(nsm / 2, tc_gemm2_max_pairs());
+    if (pairs < 1) return fail(LA_ERR_CUDA, "no CTA pair of the 2-SM GEMM fits on this device");
     for (int mode = 0; mode < 2; ++mode) {
         const int bhm = bhs[mode];
         const int bn = 2 * bhm;             // hi rows + lo rows
-        const int stages = tc_gemm_stages_for(bn);
-        const int ctas = nsm * tc_gemm_ctas_per_sm(bn, stages);
         for (int kind = 0; kind < 4; ++kind) {
             const int K = Ks[kind];
             CUtensorMap bmap;
-            if (make_tmap_bf16(&bmap, xs[kind], K, bn, static_cast<uint64_t>(K) * 2, kBlockK, bn))
+            if (make_tmap_bf16(&bmap, xs[kind], K, bn, static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
                 return fail(LA_ERR_CUDA, "tensor map for activations failed");
             int outs[3], col0[3], nseg;
             if (kind == QKV) {
@@ -525,13 +539,16 @@ int build_plans(la_handle *h) {
                 outs[0] = h->d;
                 col0[0] = 0;
             }
-            int tiles = 0;
-            for (int i = 0; i < nseg; ++i) tiles += (outs[i] + kTileM - 1) / kTileM;
+            int tiles[3];
+            for (int i = 0; i < nseg; ++i) tiles[i] = (outs[i] + kTileM - 1) / kTileM;
             const int n_kb = (K + kBlockK - 1) / kBlockK;
             TcGemm proto;
             std::memset(&proto.p, 0, sizeof(proto.p));
-            int maxp = 1, rc;
-            if ((rc = upload_schedule(h, tiles, n_kb, ctas, proto, &h->planes[mode][kind], &maxp)) != LA_OK) return rc;
+            proto.pair = true;
+            int maxp = 1, rc, group0[4];
+            if ((rc = upload_schedule(h, tiles, nseg, 2, n_kb, pairs, proto, &h->planes[mode][kind], &maxp, group0)) !=
+                LA_OK)
+                return rc;
             part_max = std::max(part_max, static_cast<size_t>(maxp) * h->R * h->ldo[kind]);
             h->plan[mode][kind].resize(h->L);
             for (int l = 0; l < h->L; ++l) {
@@ -548,16 +565,14 @@ int build_plans(la_handle *h) {
                 } else {
                     ws[0] = kind == OPROJ ? h->wo[l] : h->wd[l];
                 }
-                int t0 = 0;
                 for (int i = 0; i < nseg; ++i) {
                     if (make_tmap_bf16(&g.p.a[i], ws[i], K, outs[i], static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
                         return fail(LA_ERR_INVALID_ARG, "tensor map for a weight failed (16-byte alignment?)");
-                    g.p.seg_tile0[i] = t0;
+                    g.p.seg_tile0[i] = group0[i];
                     g.p.seg_out[i] = outs[i];
                     g.p.seg_col0[i] = col0[i];
-                    t0 += (outs[i] + kTileM - 1) / kTileM;
                 }
-                g.p.seg_tile0[nseg] = t0;
+                g.p.seg_tile0[nseg] = group0[nseg];
                 g.p.b = bmap;
                 g.p.nseg = nseg;
                 g.p.n_kb = n_kb;
@@ -566,7 +581,6 @@ int build_plans(la_handle *h) {
                 g.p.bn = bn;
                 g.p.bh = bhm;
                 g.p.ldo = h->ldo[kind];
-                g.p.stages = stages;
                 g.p.split_stride = static_cast<long long>(h->R) * h->ldo[kind];
                 g.p.out = h->part;
                 g.p.err = &h->st->err;
@@ -579,17 +593,16 @@ int build_plans(la_handle *h) {
         TcGemm &g = h->plan_lm;
         std::memset(&g.p, 0, sizeof(g.p));
         const int bn = 2 * h->bh_u;
-        const int stages = tc_gemm_stages_for(bn);
-        const int ctas = nsm * tc_gemm_ctas_per_sm(bn, stages);
+        g.pair = true;
         if (make_tmap_bf16(&g.p.a[0], h->lm_head, h->d, h->V, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM) ||
-            make_tmap_bf16(&g.p.b, h->xu, h->d, bn, static_cast<uint64_t>(h->d) * 2, kBlockK, bn))
+            make_tmap_bf16(&g.p.b, h->xu, h->d, bn, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM))
             return fail(LA_ERR_INVALID_ARG, "tensor map for lm_head failed");
         const int n_kb = (h->d + kBlockK - 1) / kBlockK;
-        int maxp = 1, rc;
-        if ((rc = upload_schedule(h, h->tv, n_kb, ctas, g, &h->planes_lm, &maxp)) != LA_OK) return rc;
+        int maxp = 1, rc, group0[2];
+        if ((rc = upload_schedule(h, &h->tv, 1, 2, n_kb, pairs, g, &h->planes_lm, &maxp, group0)) != LA_OK) return rc;
         g.p.nseg = 1;
         g.p.seg_tile0[0] = 0;
-        g.p.seg_tile0[1] = h->tv;
+        g.p.seg_tile0[1] = group0[1];
         g.p.seg_out[0] = h->V;
         g.p.seg_col0[0] = 0;
         g.p.n_kb = n_kb;
@@ -598,7 +611,6 @@ int build_plans(la_handle *h) {
         g.p.bn = bn;
         g.p.bh = h->bh_u;
         g.p.ldo = h->ldo_lm;
-        g.p.stages = stages;
         g.p.split_stride = h->lm_stride;
         g.p.out = h->lm_part;
         g.p.err = &h->st->err;
@@ -682,9 +694,10 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     h->bn_step = round_up(M, 16);
     h->bn_pf = kPrefillRows;
     h->bn_u = round_up(h->U, 16);
-    h->bh_step = round_up(M, 32);
-    h->bh_pf = kPrefillRows;
-    h->bh_u = round_up(h->U, 32);
+    // bf16 GEMM inputs: hi rows [0, 128), lo rows [128, 256) of each buffer
+    h->bh_step = kTileM;
+    h->bh_pf = kTileM;
+    h->bh_u = kTileM;
     h->act_rows = h->bf16 ? 2 * kPrefillRows : h->R;
     h->tq = (h->qd + kTileM - 1) / kTileM;
     h->tk = (h->kvd + kTileM - 1) / kTileM;

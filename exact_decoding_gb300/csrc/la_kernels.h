@@ -40,8 +40,9 @@ struct TcGemmParams {
 struct TcGemm {
     TcGemmParams p;
     int grid = 0;
-    int ctas = 0;                // CTAs of a stream-K schedule
+    int ctas = 0;                // CTAs (CTA pairs for the 2-SM kernel) of a stream-K schedule
     size_t smem = 0;
+    bool pair = false;           // run k_gemm_tc2 (2-SM UMMA, 256-feature tiles, hi/lo rows, bh = 128)
 };
 
 struct SimtGemmParams {
@@ -76,6 +77,11 @@ void stream_k_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, st
 // Fill grid/smem of a plan whose params are set.
 void tc_gemm_finalize(TcGemm &g);
 cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s);
+// 2-SM kernel: shared memory, ring depth, and CTA pairs that fit at once.
+size_t tc_gemm2_smem_bytes(int stages);
+int tc_gemm2_stages();
+int tc_gemm2_max_pairs();
+cudaError_t tc_gemm2_launch(const TcGemm &g, cudaStream_t s);
 cudaError_t simt_gemm_launch(const SimtGemmParams &p, int total_f, cudaStream_t s);
 // Sum `splits` fp32 partials [split][rows][cols] into y [rows][cols] (fixed order).
 cudaError_t reduce_splits_launch(const float *part, int splits, long long stride, int rows, int cols, float *y,
