@@ -14,6 +14,8 @@
 // Pass 2 (k_attn_final): one warp per (row, head) merges the chunk partials
 //   in fixed order, then adds the row's in-step keys with an online softmax
 //   (warp-shuffle dot products) and writes the normalised output.
+#include <algorithm>
+
 #include "la_kernels.h"
 
 namespace la {
@@ -225,324 +227,465 @@ static cudaError_t attention_launch_hd(const AttnArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <typename T>
 cudaError_t attention_launch(const AttnArgs &a, cudaStream_t s) {
-    if (a.hd == 128) return attention_launch_hd<T, 128>(a, s);
-    if (a.hd == 64) return attention_launch_hd<T, 64>(a, s);
+    if (a.hd == 128) return attention_launch_hd<float, 128>(a, s);
+    if (a.hd == 64) return attention_launch_hd<float, 64>(a, s);
     return cudaErrorInvalidValue;
 }
 
-template cudaError_t attention_launch<float>(const AttnArgs &, cudaStream_t);
+// ========================================================================== tcgen05 path (bf16 models)
+// One cluster of `cs` CTAs per (KV head g, tile of 128 query vectors); CTA
+// rank j of the cluster takes the 128-key chunks [j n / cs, (j + 1) n / cs)
+// of the keys [0, P + nrows): the cached prefix, then this step's own rows.
+// Per chunk:
+//   TMA   K (hi, lo) [128 keys x hd] and V^T (hi, lo) [hd x 128 keys]
+//   UMMA  S = Qh Kh^T + Qh Kl^T + Ql Kh^T          (TMEM columns 0..127)
+//   warps 16 warps, each a 32-query x 32-key block of S (a warp reads only
+//         its own quarter of the TMEM lanes): mask, running max through
+//         shared memory, P = exp(S - m) split into (hi, lo) and stored as
+//         the next UMMA's A operand; O of earlier chunks rescaled in TMEM
+//   UMMA  O += Ph Vh + Ph Vl + Pl Vh                (TMEM columns 128..)
+// The products keep about 16 mantissa bits (the lo * lo term is dropped),
+// the softmax is fp32.  At the end each CTA leaves (O, m, l) per query
+// vector in its shared memory, and after a cluster barrier CTA j merges
+// rows [j 128 / cs, (j + 1) 128 / cs) of all cs partials, read through
+// distributed shared memory, and writes the normalised output.
+constexpr int kUKeys = 128;                  // keys per chunk
+constexpr int kUQ = 128;                     // query vectors per tile (UMMA M)
+constexpr int kUThreads = 512;               // 16 warps: 4 lane quarters x 4 column quarters
+constexpr uint32_t kUBox = 128u * 128u;      // bytes of a [128 rows x 64 bf16] swizzled box
+constexpr float kLog2e = 1.4426950408889634f;
 
-// ========================================================================== tensor-core path (bf16 models)
-// One CTA = (KV head, 64-key chunk, 64 query vectors); 4 warps x 16 queries.
-// Chunks [0, nch_prefix) cover the cached prefix [0, P), visible to every
-// row.  Chunks from nch_prefix on cover this step's own rows (slots P + s):
-// row r sees step key s iff bit s of vis_bits[r] is set (tree mode) or s <= r
-// (causal mode).
-//
-// Precision: K, V and q are fp32.  Each is split into bf16 planes hi + lo in
-// shared memory and every product runs as three bf16 MMAs (hi*hi + hi*lo +
-// lo*hi, fp32 accumulate) on mma.sync m16n8k16, which keeps about 16
-// mantissa bits; the softmax is fp32 in registers and P is split the same
-// way for P V.  Each CTA writes the chunk's (unnormalised O, max, sum) per
-// query; k_attn_merge combines the chunks in order.
-namespace {
+template <int HD>
+struct AttnLayout {
+    static constexpr uint32_t q_bytes = 2u * (HD / 64) * kUBox;          // (hi, lo) x d blocks of 64
+    static constexpr uint32_t k_bytes = 2u * (HD / 64) * kUBox;
+    static constexpr uint32_t p_bytes = 2u * (kUKeys / 64) * kUBox;      // (hi, lo) x key blocks of 64
+    static constexpr uint32_t kp_bytes = k_bytes > p_bytes ? k_bytes : p_bytes;
+    static constexpr uint32_t vbox = static_cast<uint32_t>(HD) * 128u;   // [hd rows x 64 keys]
+    static constexpr uint32_t v_bytes = 2u * (kUKeys / 64) * vbox;
+    static constexpr int o_ld = HD + 4;                                  // floats per merge row
+    static constexpr uint32_t q_off = 0, kp_off = q_bytes, v_off = kp_off + kp_bytes;
+    static constexpr uint32_t ml_off = v_off + v_bytes;                  // m[128], l[128]
+    static constexpr uint32_t red_off = ml_off + 2u * kUQ * 4u;          // [4][128] per-quarter partials
+    static constexpr uint32_t vis_off = red_off + 4u * kUQ * 4u;         // [128][8] visibility words; merge weights
+    static constexpr uint32_t bar_off = vis_off + kUQ * 8u * 4u;         // 4 mbarriers + TMEM slot
+    static constexpr uint32_t bytes = bar_off + 64u + 1024u;             // + alignment slack
+    static_assert(static_cast<uint32_t>(kUQ) * o_ld * 4u <= q_bytes + kp_bytes, "merge rows overlay Q and K/P");
+};
 
-constexpr int kTcChunk = 64;
-constexpr int kTcQ = 64;
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// bf16 pair (lo element first) for hi and for the remainder lo.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
+static __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&v);
 }
 
 template <int HD>
-__global__ void __launch_bounds__(128) k_attn_tc(const float *q, const float *kc, const float *vc, int max_seq, int P,
-                                                 int nrows, int nh, int nkv, int nch_prefix, const uint32_t *vis_bits,
-                                                 float *ws) {
+__global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constant__ AttnUmmaParams p) {
+    using Lay = AttnLayout<HD>;
+    constexpr int kCW = HD / 4;   // O columns per warp
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const uint32_t s_q = smem_u32(smem + Lay::q_off), s_kp = smem_u32(smem + Lay::kp_off);
+    const uint32_t s_v = smem_u32(smem + Lay::v_off);
+    float *sm_m = reinterpret_cast<float *>(smem + Lay::ml_off);
+    float *sm_l = sm_m + kUQ;
+    float *red = reinterpret_cast<float *>(smem + Lay::red_off);
+    uint32_t *svis = reinterpret_cast<uint32_t *>(smem + Lay::vis_off);
+    float *wsm = reinterpret_cast<float *>(smem + Lay::vis_off);   // merge weights, after the last chunk
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::bar_off);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 4);
+    float *so = reinterpret_cast<float *>(smem);   // merge rows, over Q and K/P once the MMAs are done
+
     pdl_trigger();
-    pdl_wait();
-    constexpr int LD = HD + 8;   // smem row stride (bf16): 16-byte aligned rows, conflict-free ldmatrix
-    extern __shared__ __align__(16) __nv_bfloat16 smb[];
-    __nv_bfloat16 *Kh = smb;                     // [kTcChunk][LD] each
-    __nv_bfloat16 *Kl = Kh + kTcChunk * LD;
-    __nv_bfloat16 *Vh = Kl + kTcChunk * LD;
-    __nv_bfloat16 *Vl = Vh + kTcChunk * LD;
-
-    const int kvh = blockIdx.x, chunk = blockIdx.y, qb = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gq = nh / nkv;
-    const int QV = nrows * gq;
-    const bool step_chunk = chunk >= nch_prefix;
-    const int key0 = step_chunk ? (chunk - nch_prefix) * kTcChunk : chunk * kTcChunk;   // step index or position
-    const int slot0 = step_chunk ? P + key0 : key0;
-    const int nkeys = step_chunk ? min(kTcChunk, nrows - key0) : min(kTcChunk, P - key0);
+    const int qw = warp & 3, cw = warp >> 2;   // TMEM lane quarter, column quarter
+    const int row = 32 * qw + lane;            // this thread's query vector within the tile
+    const uint32_t rank = cluster_ctarank();
+    const int cs = static_cast<int>(gridDim.x);   // the cluster spans x
+    const int g = static_cast<int>(blockIdx.y) / p.mtiles, qt = static_cast<int>(blockIdx.y) % p.mtiles;
+    const int c_beg = static_cast<int>(static_cast<long long>(rank) * p.nchunks / cs);
+    const int c_end = static_cast<int>(static_cast<long long>(rank + 1) * p.nchunks / cs);
+    // bar_ld: Q (first chunk) and K landed; bar_v: V landed; bar_s / bar_pv: MMAs done.
+    const uint32_t bar_ld = smem_u32(&bars[0]), bar_s = smem_u32(&bars[1]), bar_pv = smem_u32(&bars[2]);
+    const uint32_t bar_v = smem_u32(&bars[3]);
 
-    // K / V chunk -> shared hi/lo planes (keys past the chunk are zero).
-    // All of a thread's loads are issued before any conversion.  Plain
-    // (coherent) loads: with programmatic dependent launch this kernel's
-    // lifetime overlaps the kernel that writes q, K and V, so the
-    // read-only cache path must not be used for them.
-    {
-        const float *kb = kc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
-        const float *vb = vc + (static_cast<long long>(kvh) * max_seq + slot0) * HD;
-        constexpr int PER = kTcChunk * (HD / 4) / 128;   // float4 per thread per tensor
-        float4 kx[PER], vx[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int t = tid + j * 128;
-            const int key = t / (HD / 4), c = (t % (HD / 4)) * 4;
-            if (key < nkeys) {
-                kx[j] = *reinterpret_cast<const float4 *>(kb + static_cast<long long>(key) * HD + c);
-                vx[j] = *reinterpret_cast<const float4 *>(vb + static_cast<long long>(key) * HD + c);
-            } else {
-                kx[j] = vx[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int t = tid + j * 128;
-            const int key = t / (HD / 4), c = (t % (HD / 4)) * 4;
-            uint2 h, l;
-            split2(kx[j].x, kx[j].y, h.x, l.x);
-            split2(kx[j].z, kx[j].w, h.y, l.y);
-            *reinterpret_cast<uint2 *>(Kh + key * LD + c) = h;
-            *reinterpret_cast<uint2 *>(Kl + key * LD + c) = l;
-            split2(vx[j].x, vx[j].y, h.x, l.x);
-            split2(vx[j].z, vx[j].w, h.y, l.y);
-            *reinterpret_cast<uint2 *>(Vh + key * LD + c) = h;
-            *reinterpret_cast<uint2 *>(Vl + key * LD + c) = l;
-        }
+    if (tid == 0) {
+        mbar_init(bar_ld, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_pv, 1);
+        mbar_init(bar_v, 1);
+        fence_barrier_init();
+        prefetch_tensormap(&p.tq);
+        prefetch_tensormap(&p.tk);
+        prefetch_tensormap(&p.tv);
     }
-    // This warp's 16 query vectors: A fragments straight from global memory
-    // (fp32, scaled, split into hi/lo), rows ra = lane/4 and rb = ra + 8.
-    const int qv0 = qb * kTcQ + warp * 16;
-    const int qa_v = qv0 + (lane >> 2), qb_v = qa_v + 8;
-    const int ra = qa_v < QV ? qa_v / gq : -1, rb = qb_v < QV ? qb_v / gq : -1;
-    const float scale = rsqrtf(static_cast<float>(HD));
-    uint32_t qh[HD / 16][4], ql[HD / 16][4];
-    {
-        const float *qpa = ra >= 0 ? q + (static_cast<long long>(ra) * nh + kvh * gq + qa_v % gq) * HD : nullptr;
-        const float *qpb = rb >= 0 ? q + (static_cast<long long>(rb) * nh + kvh * gq + qb_v % gq) * HD : nullptr;
-        const int c0 = 2 * (lane & 3);
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-            const int c = ks * 16 + c0;
-            const float2 a0 = qpa ? *reinterpret_cast<const float2 *>(qpa + c) : make_float2(0.f, 0.f);
-            const float2 a2 = qpa ? *reinterpret_cast<const float2 *>(qpa + c + 8) : make_float2(0.f, 0.f);
-            const float2 b0 = qpb ? *reinterpret_cast<const float2 *>(qpb + c) : make_float2(0.f, 0.f);
-            const float2 b2 = qpb ? *reinterpret_cast<const float2 *>(qpb + c + 8) : make_float2(0.f, 0.f);
-            split2(a0.x * scale, a0.y * scale, qh[ks][0], ql[ks][0]);
-            split2(b0.x * scale, b0.y * scale, qh[ks][1], ql[ks][1]);
-            split2(a2.x * scale, a2.y * scale, qh[ks][2], ql[ks][2]);
-            split2(b2.x * scale, b2.y * scale, qh[ks][3], ql[ks][3]);
-        }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_relinquish();
     }
+    tc_fence_before();
     __syncthreads();
-    if (qv0 >= QV) return;   // whole warp past the last query (no later block-wide sync)
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qw) << 16;
+    const uint32_t t_s = tmem + lane_off + static_cast<uint32_t>(32 * cw);              // 32 S columns
+    const uint32_t t_o = tmem + lane_off + static_cast<uint32_t>(kUKeys + kCW * cw);    // kCW O columns
 
-    // S = Q K^T : 16 queries x 64 keys (8 n-tiles of 8 keys), three passes
-    float sacc[kTcChunk / 8][4];
+    const int QV = p.nrows * p.gq;
+    const int qv = qt * kUQ + row;
+    const bool valid = qv < QV;
+    const int r = valid ? qv / p.gq : 0;
+
+    pdl_wait();   // q, the cache rows of this step and the visibility bits come from earlier kernels
+    if (cw == 0) {
 #pragma unroll
-    for (int j = 0; j < kTcChunk / 8; ++j) sacc[j][0] = sacc[j][1] = sacc[j][2] = sacc[j][3] = 0.f;
-    {
-        const int krow = (lane & 7) + 8 * (lane >> 4);
-        const int kcol = 8 * ((lane >> 3) & 1);
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks) {
-#pragma unroll
-            for (int np = 0; np < kTcChunk / 16; ++np) {
-                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-                ldsm_x4(smem_u32(Kh + (np * 16 + krow) * LD + ks * 16 + kcol), h0, h1, h2, h3);
-                ldsm_x4(smem_u32(Kl + (np * 16 + krow) * LD + ks * 16 + kcol), l0, l1, l2, l3);
-                mma_bf16(sacc[2 * np], qh[ks], h0, h1);
-                mma_bf16(sacc[2 * np], qh[ks], l0, l1);
-                mma_bf16(sacc[2 * np], ql[ks], h0, h1);
-                mma_bf16(sacc[2 * np + 1], qh[ks], h2, h3);
-                mma_bf16(sacc[2 * np + 1], qh[ks], l2, l3);
-                mma_bf16(sacc[2 * np + 1], ql[ks], h2, h3);
-            }
-        }
+        for (int w = 0; w < 8; ++w) svis[row * 8 + w] = (valid && p.vis_bits) ? p.vis_bits[r * 8 + w] : 0u;
     }
-    // mask + softmax
-    float ma = -INFINITY, mb = -INFINITY;
+    const uint32_t *myvis = svis + row * 8;
+    // Visibility of keys [k0, k0 + 32) for this query vector, bit j = key k0 + j.
+    auto vis_word = [&](int k0) -> uint32_t {
+        if (!valid) return 0u;
+        const int s0 = k0 - p.P;   // step index of bit 0 (negative: cached prefix)
+        uint32_t pre = 0u;
+        if (s0 <= -32) return 0xffffffffu;
+        if (s0 < 0) pre = (1u << (-s0)) - 1u;
+        // in-step keys: bit j is step index s0 + j, valid for 0 <= s0 + j < nrows
+        uint32_t st;
+        if (p.vis_bits) {
+            if (s0 >= 0) {
+                const int w = s0 >> 5, sh = s0 & 31;
+                const uint32_t lo = w < 8 ? myvis[w] : 0u, hi = w + 1 < 8 ? myvis[w + 1] : 0u;
+                st = __funnelshift_r(lo, hi, sh);
+            } else {
+                st = myvis[0] << (-s0);
+            }
+        } else {
+            // causal: step indices 0..r
+            const int last = r - s0;   // highest visible bit
+            st = last < 0 ? 0u : (last >= 31 ? 0xffffffffu : ((2u << last) - 1u));
+            if (s0 < 0) st &= ~pre;
+        }
+        const int lim = p.nrows - s0;   // bits at or above lim are past the step rows
+        const uint32_t live = lim <= 0 ? 0u : (lim >= 32 ? 0xffffffffu : ((1u << lim) - 1u));
+        return pre | (st & live & ~pre);
+    };
+
+    const long long krows_plane = static_cast<long long>(p.nkv) * p.seq;   // K rows from hi to lo plane
+    const int vrows_plane = p.nkv * HD;
+    const int ky0 = (p.layer * 2 * p.nkv + g) * p.seq;
+    const int vy0 = (p.layer * 2 * p.nkv + g) * HD;
+    // K of chunk c completes on bar_ld, V on bar_v (S can start while V lands).
+    auto issue_kv = [&](int c, uint64_t pol) {
+        const int key0 = c * kUKeys;
 #pragma unroll
-    for (int j = 0; j < kTcChunk / 8; ++j) {
+        for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int kk = j * 8 + 2 * (lane & 3) + e;
-            bool va = kk < nkeys && ra >= 0, vb2 = kk < nkeys && rb >= 0;
-            if (step_chunk) {
-                const int sidx = key0 + kk;
-                if (vis_bits) {
-                    va = va && ((vis_bits[ra * 8 + (sidx >> 5)] >> (sidx & 31)) & 1u);
-                    vb2 = vb2 && ((vis_bits[rb * 8 + (sidx >> 5)] >> (sidx & 31)) & 1u);
-                } else {
-                    va = va && sidx <= ra;
-                    vb2 = vb2 && sidx <= rb;
+            for (int db = 0; db < HD / 64; ++db)
+                tma_load_2d(s_kp + (pl * (HD / 64) + db) * kUBox, &p.tk, db * 64,
+                            static_cast<int>(ky0 + pl * krows_plane + key0), bar_ld, pol);
+        mbar_arrive_expect_tx(bar_v, Lay::v_bytes);
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int kb = 0; kb < kUKeys / 64; ++kb)
+                tma_load_2d(s_v + (pl * (kUKeys / 64) + kb) * Lay::vbox, &p.tv, key0 + kb * 64, vy0 + pl * vrows_plane,
+                            bar_v, pol);
+    };
+    if (tid == 0 && c_beg < c_end) {
+        const uint64_t pol = policy_evict_normal();   // other query tiles of this KV head read the same chunks
+        mbar_arrive_expect_tx(bar_ld, Lay::q_bytes + Lay::k_bytes);
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int db = 0; db < HD / 64; ++db)
+                tma_load_2d(s_q + (pl * (HD / 64) + db) * kUBox, &p.tq, db * 64, (pl * p.nkv + g) * p.qv_pad + qt * kUQ,
+                            bar_ld, pol);
+        issue_kv(c_beg, pol);
+    }
+
+    const uint32_t idesc_s = umma_idesc_bf16(kUQ, kUKeys), idesc_o = umma_idesc_bf16(kUQ, HD);
+    float m_run = -INFINITY, l_part = 0.f;   // l_part: this warp's quarter of the keys
+    bool ok = true;
+    int it = 0;
+    for (int c = c_beg; c < c_end; ++c, ++it) {
+        const uint32_t ph = static_cast<uint32_t>(it & 1);
+        bool w0 = true;
+        if (tid == 0) w0 = mbar_wait(bar_ld, ph, p.err, ERR_TIMEOUT_ATTN);
+        ok = __syncthreads_and(ok && w0);
+        if (!ok) break;
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int db = 0; db < HD / 64; ++db) {
+                const uint64_t qh = umma_desc_sw128(s_q + db * kUBox), ql = umma_desc_sw128(s_q + (HD / 64 + db) * kUBox);
+                const uint64_t kh = umma_desc_sw128(s_kp + db * kUBox), kl = umma_desc_sw128(s_kp + (HD / 64 + db) * kUBox);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    umma_bf16(tmem, qh + 2 * kk, kh + 2 * kk, idesc_s, (db | kk) ? 1u : 0u);
+                    umma_bf16(tmem, qh + 2 * kk, kl + 2 * kk, idesc_s, 1u);
+                    umma_bf16(tmem, ql + 2 * kk, kh + 2 * kk, idesc_s, 1u);
                 }
             }
-            if (!va) sacc[j][e] = -INFINITY;
-            if (!vb2) sacc[j][2 + e] = -INFINITY;
-            ma = fmaxf(ma, sacc[j][e]);
-            mb = fmaxf(mb, sacc[j][2 + e]);
+            umma_commit(bar_s);
+            w0 = mbar_wait(bar_s, ph, p.err, ERR_TIMEOUT_ATTN);
         }
-    }
-    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
-    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-    float la_ = 0.f, lb = 0.f;
+        ok = __syncthreads_and(w0);
+        if (!ok) break;
+        tc_fence_after();
+
+        // This warp's 32 x 32 block of S: masked max, shared with the other
+        // three column quarters of the same query vectors.
+        const int key0 = c * kUKeys;
+        const uint32_t mw = vis_word(key0 + 32 * cw);
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(t_s, v);
+        tmem_ld_wait();
+        float mc = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kTcChunk / 8; ++j) {
+        for (int j = 0; j < 32; ++j)
+            if ((mw >> j) & 1u) mc = fmaxf(mc, __uint_as_float(v[j]));
+        red[cw * kUQ + row] = mc;
+        __syncthreads();
+        mc = fmaxf(fmaxf(red[row], red[kUQ + row]), fmaxf(red[2 * kUQ + row], red[3 * kUQ + row]));
+        const float m_new = fmaxf(m_run, mc);
+        const float alpha = m_run == -INFINITY ? 0.f : exp2f((m_run - m_new) * kLog2e);
+        float pv[32];
+        float ls = 0.f;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const float pa = ma == -INFINITY ? 0.f : expf(sacc[j][e] - ma);
-            const float pb = mb == -INFINITY ? 0.f : expf(sacc[j][2 + e] - mb);
-            sacc[j][e] = pa;
-            sacc[j][2 + e] = pb;
-            la_ += pa;
-            lb += pb;
+        for (int j = 0; j < 32; ++j) {
+            pv[j] = ((mw >> j) & 1u) ? exp2f((__uint_as_float(v[j]) - m_new) * kLog2e) : 0.f;
+            ls += pv[j];
         }
-    }
-    la_ += __shfl_xor_sync(0xffffffffu, la_, 1);
-    la_ += __shfl_xor_sync(0xffffffffu, la_, 2);
-    lb += __shfl_xor_sync(0xffffffffu, lb, 1);
-    lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-    // O = P V : 16 queries x HD dims, three passes
-    float oacc[HD / 8][4];
+        l_part = l_part * alpha + ls;
+        // Keys 32 cw .. 32 cw + 31 of this query vector's P row: four 16-byte
+        // chunks of the 128-byte row in key block cw / 2, 128-byte swizzle.
+        {
+            const uint32_t rowh = s_kp + (cw / 2) * kUBox + row * 128u;
+            const uint32_t rowl = rowh + 2u * kUBox;
 #pragma unroll
-    for (int j = 0; j < HD / 8; ++j) oacc[j][0] = oacc[j][1] = oacc[j][2] = oacc[j][3] = 0.f;
-    {
-        const int vrow = (lane & 7) + 8 * ((lane >> 3) & 1);
-        const int vcol = 8 * (lane >> 4);
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t hh[4], ll[4];
 #pragma unroll
-        for (int kk = 0; kk < kTcChunk / 16; ++kk) {
-            uint32_t ph[4], pl[4];
-            split2(sacc[2 * kk][0], sacc[2 * kk][1], ph[0], pl[0]);
-            split2(sacc[2 * kk][2], sacc[2 * kk][3], ph[1], pl[1]);
-            split2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1], ph[2], pl[2]);
-            split2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3], ph[3], pl[3]);
-#pragma unroll
-            for (int dp = 0; dp < HD / 16; ++dp) {
-                uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
-                ldsm_x4_t(smem_u32(Vh + (kk * 16 + vrow) * LD + dp * 16 + vcol), h0, h1, h2, h3);
-                ldsm_x4_t(smem_u32(Vl + (kk * 16 + vrow) * LD + dp * 16 + vcol), l0, l1, l2, l3);
-                mma_bf16(oacc[2 * dp], ph, h0, h1);
-                mma_bf16(oacc[2 * dp], ph, l0, l1);
-                mma_bf16(oacc[2 * dp], pl, h0, h1);
-                mma_bf16(oacc[2 * dp + 1], ph, h2, h3);
-                mma_bf16(oacc[2 * dp + 1], ph, l2, l3);
-                mma_bf16(oacc[2 * dp + 1], pl, h2, h3);
+                for (int e = 0; e < 4; ++e) {
+                    const float a = pv[q4 * 8 + 2 * e], b = pv[q4 * 8 + 2 * e + 1];
+                    const __nv_bfloat162 hb = __floats2bfloat162_rn(a, b);
+                    const float2 hf = __bfloat1622float2(hb);
+                    hh[e] = *reinterpret_cast<const uint32_t *>(&hb);
+                    ll[e] = pack_bf16x2(a - hf.x, b - hf.y);
+                }
+                const uint32_t chunk = static_cast<uint32_t>((cw % 2) * 4 + q4) ^ static_cast<uint32_t>(row & 7);
+                st_shared_u32x4(rowh + chunk * 16u, hh[0], hh[1], hh[2], hh[3]);
+                st_shared_u32x4(rowl + chunk * 16u, ll[0], ll[1], ll[2], ll[3]);
             }
         }
+        // O of the earlier chunks (in TMEM) to the new running max.
+        if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if constexpr (kCW == 32) {
+                uint32_t o[32];
+                tmem_ld_32x32b_x32(t_o, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                tmem_st_32x32b_x32(t_o, o);
+            } else {
+                uint32_t o[16];
+                tmem_ld_32x32b_x16(t_o, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                tmem_st_32x32b_x16(t_o, o);
+            }
+            tmem_st_wait();
+        }
+        m_run = m_new;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && mbar_wait(bar_v, ph, p.err, ERR_TIMEOUT_ATTN)) {
+            tc_fence_after();
+#pragma unroll
+            for (int kb = 0; kb < kUKeys / 64; ++kb) {
+                const uint64_t ph_ = umma_desc_sw128(s_kp + kb * kUBox), pl_ = umma_desc_sw128(s_kp + (2 + kb) * kUBox);
+                const uint64_t vh = umma_desc_sw128(s_v + kb * Lay::vbox);
+                const uint64_t vl = umma_desc_sw128(s_v + (kUKeys / 64 + kb) * Lay::vbox);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    umma_bf16(tmem + kUKeys, ph_ + 2 * kk, vh + 2 * kk, idesc_o, (it | kb | kk) ? 1u : 0u);
+                    umma_bf16(tmem + kUKeys, ph_ + 2 * kk, vl + 2 * kk, idesc_o, 1u);
+                    umma_bf16(tmem + kUKeys, pl_ + 2 * kk, vh + 2 * kk, idesc_o, 1u);
+                }
+            }
+            umma_commit(bar_pv);
+            w0 = mbar_wait(bar_pv, ph, p.err, ERR_TIMEOUT_ATTN);
+            if (w0 && c + 1 < c_end) {   // K/P and V are free again
+                mbar_arrive_expect_tx(bar_ld, Lay::k_bytes);
+                issue_kv(c + 1, policy_evict_normal());
+            }
+        } else if (tid == 0) {
+            w0 = false;   // V never landed
+        }
+        ok = __syncthreads_and(w0);
+        if (!ok) break;
+        tc_fence_after();
     }
-    // partials: ws[chunk][r][h][HD + 4] = (O, max, sum)
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int qvv = half ? qb_v : qa_v;
-        if (qvv >= QV) continue;
-        const int r = qvv / gq, hq = kvh * gq + qvv % gq;
-        float *w = ws + ((static_cast<long long>(chunk) * nrows + r) * nh + hq) * (HD + 4);
-#pragma unroll
-        for (int j = 0; j < HD / 8; ++j)
-            *reinterpret_cast<float2 *>(w + j * 8 + 2 * (lane & 3)) =
-                make_float2(oacc[j][2 * half], oacc[j][2 * half + 1]);
-        if ((lane & 3) == 0) {
-            w[HD] = half ? mb : ma;
-            w[HD + 1] = half ? lb : la_;
+    if (!ok) {   // a load or an MMA never completed: wait (bounded) for TMA still in flight
+        m_run = -INFINITY;
+        l_part = 0.f;
+        if (tid == 0 && it < c_end - c_beg) {
+            mbar_wait(bar_ld, static_cast<uint32_t>(it & 1), p.err, ERR_TIMEOUT_ATTN);
+            mbar_wait(bar_v, static_cast<uint32_t>(it & 1), p.err, ERR_TIMEOUT_ATTN);
         }
     }
-}
 
-template <int HD>
-__global__ void __launch_bounds__(256) k_attn_merge(const float *ws, int nch, int nrows, int nh, __nv_bfloat16 *out,
-                                                    long long lo_off) {
-    pdl_trigger();
-    pdl_wait();
-    constexpr int DPL = HD / 32;
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= nrows * nh) return;
-    const int r = gw / nh, h = gw % nh;
-    float m = -INFINITY, l = 0.f, o[DPL];
+    // Partials to this CTA's shared memory: O rows, m, and l summed over the
+    // four column quarters.
+    __syncthreads();
+    {
+        float *orow = so + row * Lay::o_ld + kCW * cw;
+        const bool have = ok && it > 0;
+        if constexpr (kCW == 32) {
+            uint32_t o[32];
+            if (have) {
+                tmem_ld_32x32b_x32(t_o, o);
+                tmem_ld_wait();
+            }
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) o[j] = 0.f;
-    for (int c = 0; c < nch; ++c) {
-        const float *w = ws + ((static_cast<long long>(c) * nrows + r) * nh + h) * (HD + 4);
-        const float pm = w[HD];
-        if (pm == -INFINITY) continue;
-        const float pl = w[HD + 1];
-        const float nm = fmaxf(m, pm);
-        const float a = (m == -INFINITY) ? 0.f : expf(m - nm);
-        const float b = expf(pm - nm);
-        l = l * a + pl * b;
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(orow + j) =
+                    have ? make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]), __uint_as_float(o[j + 2]),
+                                       __uint_as_float(o[j + 3]))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            uint32_t o[16];
+            if (have) {
+                tmem_ld_32x32b_x16(t_o, o);
+                tmem_ld_wait();
+            }
 #pragma unroll
-        for (int j = 0; j < DPL; ++j) o[j] = o[j] * a + w[lane * DPL + j] * b;
-        m = nm;
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4 *>(orow + j) =
+                    have ? make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]), __uint_as_float(o[j + 2]),
+                                       __uint_as_float(o[j + 3]))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        red[cw * kUQ + row] = l_part;
+        if (cw == 0) sm_m[row] = m_run;
     }
-    const float inv = 1.f / l;
-    const long long base = static_cast<long long>(r) * nh * HD + h * HD + lane * DPL;
+    __syncthreads();
+    if (cw == 0) sm_l[row] = red[row] + red[kUQ + row] + red[2 * kUQ + row] + red[3 * kUQ + row];
+    tc_fence_before();
+    cluster_sync_all();
+    // Merge rows [rank 128 / cs, (rank + 1) 128 / cs) of the cs partials:
+    // per-row weights exp(m_j - max) / sum first, then float4 columns.
+    const int r_beg = static_cast<int>(rank) * kUQ / cs, rows_per = (static_cast<int>(rank) + 1) * kUQ / cs - r_beg;
+    for (int i = tid; i < rows_per; i += kUThreads) {
+        const int mr = r_beg + i;
+        float mj[8];
+        float mx = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) store_act(out, base + j, o[j] * inv, lo_off);
+        for (int j = 0; j < 8; ++j) {
+            mj[j] = j < cs ? ld_cluster_f32(mapa_shared(smem_u32(&sm_m[mr]), static_cast<uint32_t>(j))) : -INFINITY;
+            mx = fmaxf(mx, mj[j]);
+        }
+        float L = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            mj[j] = mj[j] == -INFINITY ? 0.f : exp2f((mj[j] - mx) * kLog2e);
+            if (mj[j] != 0.f) L += mj[j] * ld_cluster_f32(mapa_shared(smem_u32(&sm_l[mr]), static_cast<uint32_t>(j)));
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wsm[i * 8 + j] = mj[j] * inv;
+    }
+    __syncthreads();
+    constexpr int G4 = HD / 4;
+    for (int i = tid; i < rows_per * G4; i += kUThreads) {
+        const int li = i / G4, d = (i % G4) * 4;
+        const int mr = r_beg + li;
+        const int qvr = qt * kUQ + mr;
+        if (qvr >= QV) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float w = wsm[li * 8 + j];
+            if (w == 0.f) continue;
+            const float4 x = ld_cluster_f32x4(mapa_shared(smem_u32(so + mr * Lay::o_ld + d), static_cast<uint32_t>(j)));
+            acc.x += w * x.x;
+            acc.y += w * x.y;
+            acc.z += w * x.z;
+            acc.w += w * x.w;
+        }
+        const int rr = qvr / p.gq, head = g * p.gq + qvr % p.gq;
+        const long long ob = (static_cast<long long>(rr) * p.nh + head) * HD + d;
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(acc.x, acc.y), h23 = __floats2bfloat162_rn(acc.z, acc.w);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        uint2 hv, lv;
+        hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+        hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+        lv.x = pack_bf16x2(acc.x - f01.x, acc.y - f01.y);
+        lv.y = pack_bf16x2(acc.z - f23.x, acc.w - f23.y);
+        *reinterpret_cast<uint2 *>(p.out + ob) = hv;
+        *reinterpret_cast<uint2 *>(p.out + ob + p.out_lo_off) = lv;
+    }
+    cluster_sync_all();   // peers are done reading this CTA's shared memory
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
 }
 
 template <int HD>
-cudaError_t attention_tc_hd(const AttnArgs &a, cudaStream_t s) {
-    const int nch_prefix = (a.P + kTcChunk - 1) / kTcChunk;
-    const int nch = nch_prefix + (a.nrows + kTcChunk - 1) / kTcChunk;
-    const int gq = a.nh / a.nkv;
-    const size_t smem = static_cast<size_t>(4 * kTcChunk) * (HD + 8) * sizeof(__nv_bfloat16);
+static cudaError_t attention_umma_hd(const AttnUmmaParams &p, int cs, cudaStream_t s) {
+    using Lay = AttnLayout<HD>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn_tc<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(Lay::bytes));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid(a.nkv, nch, (a.nrows * gq + kTcQ - 1) / kTcQ);
-    launch_k(k_attn_tc<HD>, dim3(grid), dim3(128), smem, s, a.q, a.kc, a.vc, a.max_seq, a.P, a.nrows, a.nh, a.nkv, nch_prefix,
-                                          a.vis_bits, a.ws);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int warps = a.nrows * a.nh;
-    launch_k(k_attn_merge<HD>, dim3((warps + 7) / 8), dim3(256), 0, s, a.ws, nch, a.nrows, a.nh, static_cast<__nv_bfloat16 *>(a.out),
-                                                     a.out_lo_off);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs, p.nkv * p.mtiles);
+    cfg.blockDim = dim3(kUThreads);
+    cfg.dynamicSmemBytes = Lay::bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_attn_umma<HD>, p);
 }
 
-}  // namespace
-
-int attention_tc_chunks(int P, int nrows) {
-    return (P + kTcChunk - 1) / kTcChunk + (nrows + kTcChunk - 1) / kTcChunk;
+bool attention_umma_maps(AttnUmmaParams &p, const void *q, const void *kc, const void *vc, int L) {
+    const int hd = p.hd;
+    if (make_tmap_bf16(&p.tq, q, hd, static_cast<uint64_t>(2) * p.nkv * p.qv_pad, static_cast<uint64_t>(hd) * 2, 64,
+                       kUQ))
+        return false;
+    if (make_tmap_bf16(&p.tk, kc, hd, static_cast<uint64_t>(L) * 2 * p.nkv * p.seq, static_cast<uint64_t>(hd) * 2, 64,
+                       kUKeys))
+        return false;
+    if (make_tmap_bf16(&p.tv, vc, p.seq, static_cast<uint64_t>(L) * 2 * p.nkv * hd, static_cast<uint64_t>(p.seq) * 2,
+                       64, static_cast<uint32_t>(hd)))
+        return false;
+    return true;
 }
 
-template <>
-cudaError_t attention_launch<__nv_bfloat16>(const AttnArgs &a, cudaStream_t s) {
-    if (a.hd == 128) return attention_tc_hd<128>(a, s);
-    if (a.hd == 64) return attention_tc_hd<64>(a, s);
+cudaError_t attention_umma_launch(AttnUmmaParams p, int nsm, cudaStream_t s) {
+    p.nchunks = (p.P + p.nrows + kUKeys - 1) / kUKeys;
+    p.mtiles = (p.nrows * p.gq + kUQ - 1) / kUQ;
+    const int units = p.nkv * p.mtiles;
+    // One chunk per CTA where the SMs allow it (clusters of up to 8 CTAs).
+    int cs = std::min(std::min(8, p.nchunks), std::max(1, nsm / units));
+    if (p.hd == 128) return attention_umma_hd<128>(p, cs, s);
+    if (p.hd == 64) return attention_umma_hd<64>(p, cs, s);
     return cudaErrorInvalidValue;
 }
 

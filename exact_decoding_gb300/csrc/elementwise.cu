@@ -121,6 +121,100 @@ cudaError_t qkv_rope_launch(const float *part, const int *planes, long long sstr
     return cudaGetLastError();
 }
 
+// bf16 models: one CTA = 32 rows x one head slot (a q, k or v head).  The
+// tile is summed into shared memory with coalesced row reads; q and k are
+// rotated and written along d, v is written transposed (consecutive rows are
+// consecutive cache columns).
+template <int HD>
+__global__ void __launch_bounds__(256) k_qkv_rope_split(const float *part, const int *planes, long long sstride,
+                                                        int ldp, int nrows, int nh, int nkv, int k_off, int v_off,
+                                                        const float2 *rope, int P, const int *depth,
+                                                        __nv_bfloat16 *q, int qv_pad, __nv_bfloat16 *kc,
+                                                        __nv_bfloat16 *vc, int layer, int seq) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float t[32][HD + 1];
+    const int r0 = blockIdx.x * 32, hs = blockIdx.y;
+    const bool isq = hs < nh, isk = !isq && hs < nh + nkv;
+    const int col0 = isq ? hs * HD : isk ? k_off + (hs - nh) * HD : v_off + (hs - nh - nkv) * HD;
+    // A head's columns start on a 128-column tile, so the whole tile has one
+    // plane count; each plane's loads are all issued before they are added.
+    {
+        constexpr int PER = 32 * HD / 256;
+        const int np = planes ? planes[col0 >> 7] : 1;
+        float acc[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+        for (int pl = 0; pl < np; ++pl) {
+            const float *base = part + pl * sstride + col0;
+            float x[PER];
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const int i = threadIdx.x + j * 256, rr = i / HD, d = i % HD, r = r0 + rr;
+                x[j] = r < nrows ? base[static_cast<long long>(r) * ldp + d] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < PER; ++j) acc[j] += x[j];
+        }
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int i = threadIdx.x + j * 256;
+            t[i / HD][i % HD] = acc[j];
+        }
+    }
+    __syncthreads();
+    constexpr int half = HD / 2;
+    if (isq || isk) {
+        const int gq = nh / nkv;
+        const float scale = rsqrtf(static_cast<float>(HD));
+        for (int i = threadIdx.x; i < 32 * half; i += 256) {
+            const int rr = i / half, ii = i % half, r = r0 + rr;
+            if (r >= nrows) continue;
+            const int pos = P + (depth ? depth[r] : r);
+            const float2 c = rope[static_cast<long long>(pos) * half + ii];
+            const float x1 = t[rr][ii], x2 = t[rr][ii + half];
+            float y1 = x1 * c.x - x2 * c.y, y2 = x1 * c.y + x2 * c.x;
+            if (isq) {
+                const int g = hs / gq, qv = r * gq + hs % gq;
+                const long long base = (static_cast<long long>(g) * qv_pad + qv) * HD;
+                const long long lo = static_cast<long long>(nkv) * qv_pad * HD;
+                store_act(q, base + ii, y1 * scale, lo);
+                store_act(q, base + ii + half, y2 * scale, lo);
+            } else {
+                const long long base = ((static_cast<long long>(layer) * 2 * nkv + (hs - nh)) * seq + P + r) * HD;
+                const long long lo = static_cast<long long>(nkv) * seq * HD;
+                store_act(kc, base + ii, y1, lo);
+                store_act(kc, base + ii + half, y2, lo);
+            }
+        }
+    } else {
+        const int vh = hs - nh - nkv;
+        const long long lo = static_cast<long long>(nkv) * HD * seq;
+        for (int i = threadIdx.x; i < 32 * HD; i += 256) {
+            const int d = i / 32, rr = i % 32, r = r0 + rr;
+            if (r >= nrows) continue;
+            const long long idx = ((static_cast<long long>(layer) * 2 * nkv + vh) * HD + d) * seq + P + r;
+            store_act(vc, idx, t[rr][d], lo);
+        }
+    }
+}
+
+cudaError_t qkv_rope_split_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows,
+                                  int nh, int nkv, int hd, int k_off, int v_off, const float2 *rope, int P,
+                                  const int *depth, __nv_bfloat16 *q, int qv_pad, __nv_bfloat16 *kc,
+                                  __nv_bfloat16 *vc, int layer, int seq, cudaStream_t s) {
+    dim3 grid((nrows + 31) / 32, nh + 2 * nkv);
+    if (hd == 128)
+        launch_k(k_qkv_rope_split<128>, grid, dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv, k_off,
+                 v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
+    else if (hd == 64)
+        launch_k(k_qkv_rope_split<64>, grid, dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv, k_off,
+                 v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ residual + norm
 // Output row i reads residual row r = row_map[i] (or i): h[r] += sum_s part[s][r];
 // xout[i] = rmsnorm(h[r]) * gain.  d % 4 == 0; float4 accesses, all loads of

@@ -74,6 +74,12 @@ struct la_handle {
     float *h = nullptr, *part = nullptr, *q = nullptr, *logits = nullptr, *lmax = nullptr, *lsum = nullptr;
     float *attn_ws = nullptr;
     void *xn = nullptr, *ao = nullptr, *fa = nullptr, *xu = nullptr, *cache = nullptr;
+    // bf16 models: q planes [2][nkv][qv_pad][hd], K planes [L][2][nkv][seq][hd]
+    // and V^T planes [L][2][nkv][hd][seq] (cache = K then V^T); seq =
+    // max_seq rounded up to 64 slots.
+    __nv_bfloat16 *qs = nullptr, *kcs = nullptr, *vcs = nullptr;
+    int qv_pad = 0, seq = 0, nsm = 0;
+    AttnUmmaParams attn_proto{};
     float2 *rope = nullptr;
     int *amax = nullptr, *tok = nullptr, *depth = nullptr, *anc = nullptr, *anc_cnt = nullptr, *used = nullptr;
     int *iota = nullptr;
@@ -362,6 +368,25 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         int rc;
         if ((rc = run_gemm(h, mode, QKV, l, nrows)) != LA_OK) return rc;
         const long long ss_qkv = static_cast<long long>(h->R) * h->ldo[QKV];
+        const double attn_bytes =
+            (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * 4.0 + 4.0 * nrows * h->qd + 4.0 * nrows * h->qd;
+        if (h->bf16) {
+            pe = mode == STEP ? h->prof_begin() : -1;
+            CK(qkv_rope_split_launch(h->part, h->planes[mode][QKV], ss_qkv, h->ldo[QKV], nrows, h->nh, h->nkv, h->hd,
+                                     h->k_off, h->v_off, h->rope, P, mode == STEP ? h->depth : nullptr, h->qs,
+                                     h->qv_pad, h->kcs, h->vcs, l, h->seq, s));
+            h->prof_end(pe, 2, 0.0);
+            AttnUmmaParams ap = h->attn_proto;
+            ap.layer = l;
+            ap.P = P;
+            ap.nrows = nrows;
+            ap.vis_bits = mode == STEP ? h->vis_bits : nullptr;
+            ap.out_lo_off = bh * h->qd;
+            pe = mode == STEP ? h->prof_begin() : -1;
+            CK(attention_umma_launch(ap, h->nsm, s));
+            h->prof_end(pe, 1, attn_bytes);
+            h->launches += 2;   // qkv_rope_split, attention
+        } else {
         pe = mode == STEP ? h->prof_begin() : -1;
         CK(qkv_rope_launch(h->part, h->planes[mode][QKV], ss_qkv, h->ldo[QKV], nrows, h->nh, h->nkv, h->hd,
                            h->k_off, h->v_off, h->rope, P, mode == STEP ? h->depth : nullptr, h->q,
@@ -386,10 +411,10 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         a.out = h->ao;
         a.out_lo_off = bh * h->qd;
         pe = mode == STEP ? h->prof_begin() : -1;
-        CK(attention_launch<T>(a, s));
-        h->prof_end(pe, 1,
-                    (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * 4.0 + 4.0 * nrows * h->qd + 4.0 * nrows * h->qd);
-        h->launches += 1 + (h->bf16 ? 2 : 1 + (nch > 0 ? 1 : 0));   // qkv_rope, attention passes
+        CK(attention_launch(a, s));
+        h->prof_end(pe, 1, attn_bytes);
+        h->launches += 2 + (nch > 0 ? 1 : 0);   // qkv_rope, attention passes
+        }
         if ((rc = run_gemm(h, mode, OPROJ, l, nrows)) != LA_OK) return rc;
         const long long ss_d = static_cast<long long>(h->R) * h->ldo[OPROJ];
         pe = mode == STEP ? h->prof_begin() : -1;
@@ -429,7 +454,10 @@ int forward_any(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool 
 }
 
 int kv_commit(la_handle *h) {
-    CK(kv_commit_launch(h->spec(), static_cast<float *>(h->cache), h->L, h->nkv, h->hd, h->stream));
+    if (h->bf16)
+        CK(kv_commit_split_launch(h->spec(), h->kcs, h->vcs, h->L, h->nkv, h->hd, h->seq, h->stream));
+    else
+        CK(kv_commit_launch(h->spec(), static_cast<float *>(h->cache), h->L, h->nkv, h->hd, h->stream));
     return LA_OK;
 }
 
@@ -699,6 +727,8 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     h->bh_pf = kTileM;
     h->bh_u = kTileM;
     h->act_rows = h->bf16 ? 2 * kPrefillRows : h->R;
+    h->seq = h->bf16 ? round_up(h->max_seq, 64) : h->max_seq;
+    h->qv_pad = kPrefillRows * (h->nh / h->nkv);
     h->tq = (h->qd + kTileM - 1) / kTileM;
     h->tk = (h->kvd + kTileM - 1) / kTileM;
     h->tg = (h->F + kTileM - 1) / kTileM;
@@ -755,9 +785,15 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     A(h->alloc(&h->amax, std::max(h->U, 1)));
     A(h->alloc(&h->lmax, std::max(h->U, 1)));
     A(h->alloc(&h->lsum, std::max(h->U, 1)));
-    const int nch_max = std::max((h->max_seq + kAttnChunk - 1) / kAttnChunk, attention_tc_chunks(h->max_seq, R));
-    A(h->alloc(&h->attn_ws, static_cast<size_t>(nch_max) * R * h->nh * (h->hd + 4)));
-    A(h->alloc_bytes(&h->cache, static_cast<size_t>(h->L) * 2 * h->nkv * h->max_seq * h->hd * sizeof(float)));
+    const size_t cache_bytes = static_cast<size_t>(h->L) * 2 * h->nkv * h->seq * h->hd * sizeof(float);
+    if (h->bf16) {
+        A(h->alloc(&h->attn_ws, 1));
+        A(h->alloc(&h->qs, static_cast<size_t>(2) * h->nkv * h->qv_pad * h->hd));
+    } else {
+        const int nch_max = (h->max_seq + kAttnChunk - 1) / kAttnChunk;
+        A(h->alloc(&h->attn_ws, static_cast<size_t>(nch_max) * R * h->nh * (h->hd + 4)));
+    }
+    A(h->alloc_bytes(&h->cache, cache_bytes));
     A(h->alloc(&h->rope, static_cast<size_t>(h->max_seq) * (h->hd / 2)));
     A(h->alloc(&h->tok, M));
     A(h->alloc(&h->depth, M));
@@ -838,6 +874,37 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         cudaMemsetAsync(h->st, 0, sizeof(SpecState), s) != cudaSuccess) {
         delete h;
         return fail(LA_ERR_CUDA, "memset failed");
+    }
+    if (h->bf16) {
+        // The tensor-core attention reads whole 128-key chunks and 128-row
+        // query tiles: slots and rows past the live ones must hold finite
+        // values (they are masked, and 0 * finite = 0 in P V).
+        h->kcs = static_cast<__nv_bfloat16 *>(h->cache);
+        h->vcs = h->kcs + static_cast<size_t>(h->L) * 2 * h->nkv * h->seq * h->hd;
+        if (cudaMemsetAsync(h->cache, 0, cache_bytes, s) != cudaSuccess ||
+            cudaMemsetAsync(h->qs, 0, static_cast<size_t>(2) * h->nkv * h->qv_pad * h->hd * 2, s) != cudaSuccess) {
+            delete h;
+            return fail(LA_ERR_CUDA, "memset failed");
+        }
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&h->nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            delete h;
+            return fail(LA_ERR_CUDA, "device query failed");
+        }
+        AttnUmmaParams &ap = h->attn_proto;
+        ap.nh = h->nh;
+        ap.nkv = h->nkv;
+        ap.gq = h->nh / h->nkv;
+        ap.hd = h->hd;
+        ap.qv_pad = h->qv_pad;
+        ap.seq = h->seq;
+        ap.out = static_cast<__nv_bfloat16 *>(h->ao);
+        ap.err = &h->st->err;
+        if (!attention_umma_maps(ap, h->qs, h->kcs, h->vcs, h->L)) {
+            delete h;
+            return fail(LA_ERR_CUDA, "tensor maps for the attention failed");
+        }
     }
     if (h->bf16) {
         rc = build_plans(h);

@@ -103,6 +103,17 @@ cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, 
 cudaError_t qkv_rope_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows, int nh,
                             int nkv, int hd, int k_off, int v_off, const float2 *rope, int P, const int *depth,
                             float *q, float *kc, float *vc, int max_seq, cudaStream_t s);
+// bf16 models: the same projection sums and rotation, written for the
+// tensor-core attention as bf16 (hi, lo) plane pairs (x = hi + lo):
+//   q  [2][nkv][qv_pad][hd]      query vector v = row * (nh / nkv) + j of KV
+//                                head g is q head g * (nh / nkv) + j; scaled
+//                                by 1 / sqrt(hd)
+//   kc [L][2][nkv][seq][hd]      rows P + r of layer `layer`
+//   vc [L][2][nkv][hd][seq]      V transposed: columns P + r
+cudaError_t qkv_rope_split_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows,
+                                  int nh, int nkv, int hd, int k_off, int v_off, const float2 *rope, int P,
+                                  const int *depth, __nv_bfloat16 *q, int qv_pad, __nv_bfloat16 *kc,
+                                  __nv_bfloat16 *vc, int layer, int seq, cudaStream_t s);
 template <typename T>
 cudaError_t resid_norm_launch(float *h, const float *part, const int *planes, long long sstride, int ldp, int d,
                               const T *gain, float eps, const int *row_map, int nrows, T *xout, long long lo_off,
@@ -136,13 +147,28 @@ struct AttnArgs {
 };
 constexpr int kAttnChunk = 64;
 // fp32 models: SIMT split-KV (64-key chunks) + per-row in-step pass.
-// bf16 models: tensor-core chunks of 128 keys (prefix and in-step) + merge.
-template <typename T>
 cudaError_t attention_launch(const AttnArgs &a, cudaStream_t s);
-template <>
-cudaError_t attention_launch<__nv_bfloat16>(const AttnArgs &a, cudaStream_t s);
-// Partial records the bf16 path writes for prefix length P and nrows rows.
-int attention_tc_chunks(int P, int nrows);
+
+// bf16 models: tcgen05 attention over the plane layouts qkv_rope_split
+// writes.  One thread-block cluster per (KV head, tile of 128 query
+// vectors); its CTAs split the keys [0, P + nrows) in 128-key chunks and
+// merge their partial softmax sums through distributed shared memory.
+struct AttnUmmaParams {
+    CUtensorMap tq;        // q planes as [2 * nkv * qv_pad][hd], box 64 x 128
+    CUtensorMap tk;        // K cache as [L * 2 * nkv * seq][hd], box 64 x 128
+    CUtensorMap tv;        // V^T cache as [L * 2 * nkv * hd][seq], box 64 x hd
+    int layer, nh, nkv, gq, hd, qv_pad, seq;
+    int P, nrows, nchunks, mtiles;
+    const uint32_t *vis_bits;   // [nrows][8] in-step visibility bits, or nullptr (causal)
+    __nv_bfloat16 *out;         // [nrows][nh * hd] hi plane; lo plane out_lo_off later
+    long long out_lo_off;
+    unsigned *err;
+};
+// Fills the tensor maps; false if the driver rejects one.
+bool attention_umma_maps(AttnUmmaParams &p, const void *q, const void *kc, const void *vc, int L);
+// Launch for the current P / nrows (fields P, nrows, layer, vis_bits set by
+// the caller); picks the cluster size from the SM count.
+cudaError_t attention_umma_launch(AttnUmmaParams p, int nsm, cudaStream_t s);
 
 // ------------------------------------------------------------------ speculation state
 struct SpecState {
@@ -180,6 +206,9 @@ struct SpecDev {
 cudaError_t build_rows_launch(const SpecDev &d, cudaStream_t s);
 cudaError_t finish_step_launch(const SpecDev &d, cudaStream_t s);
 cudaError_t kv_commit_launch(const SpecDev &d, float *cache, int L, int nkv, int hd, cudaStream_t s);
+// Same for the bf16 plane layouts (K rows, V^T columns).
+cudaError_t kv_commit_split_launch(const SpecDev &d, __nv_bfloat16 *kc, __nv_bfloat16 *vc, int L, int nkv, int hd,
+                                   int seq, cudaStream_t s);
 // Insert n records [n][N] (key, suffix) in order, one warp, sequential semantics.
 cudaError_t pool_insert_launch(const SpecDev &d, const int *records, int n, cudaStream_t s);
 // Insert the prompt's n-grams (tokens_log[0..n)) in ascending start position.

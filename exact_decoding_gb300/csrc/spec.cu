@@ -384,6 +384,30 @@ __global__ void k_kv_commit(SpecDev d, float *cache, int nkv, int hd) {
     }
 }
 
+// bf16 plane layouts: block = (layer, hi|lo, KV head); K rows move like the
+// fp32 cache, V^T moves column runs (the accepted rows are consecutive slots
+// on both sides, and the source run lies past the destination run).
+__global__ void k_kv_commit_split(SpecDev d, __nv_bfloat16 *kc, __nv_bfloat16 *vc, int hd, int seq) {
+    pdl_trigger();
+    pdl_wait();
+    const int A = d.st->A, cs = d.st->cstar, P0 = d.st->P_old;
+    if (A <= 1 || cs < 0) return;
+    const int n = A - 1;
+    const int span = d.N - 1;
+    const int src0 = P0 + 1 + span * d.W + cs * span;   // slot of the first accepted candidate token
+    const long long plane = static_cast<long long>(blockIdx.x);
+    __nv_bfloat16 *kb = kc + plane * seq * hd;
+    for (int t = threadIdx.x; t < n * hd; t += blockDim.x) {
+        const int m = t / hd, i = t % hd;
+        kb[static_cast<long long>(P0 + 1 + m) * hd + i] = kb[static_cast<long long>(src0 + m) * hd + i];
+    }
+    __nv_bfloat16 *vb = vc + plane * hd * seq;
+    for (int t = threadIdx.x; t < n * hd; t += blockDim.x) {
+        const int i = t / n, m = t % n;
+        vb[static_cast<long long>(i) * seq + P0 + 1 + m] = vb[static_cast<long long>(i) * seq + src0 + m];
+    }
+}
+
 // ------------------------------------------------------------------ pool seeding / import
 __global__ void k_pool_insert(SpecDev d, const int *records, int n) {
     pdl_trigger();
@@ -433,6 +457,12 @@ cudaError_t finish_step_launch(const SpecDev &d, cudaStream_t s) {
 }
 cudaError_t kv_commit_launch(const SpecDev &d, float *cache, int L, int nkv, int hd, cudaStream_t s) {
     launch_k(k_kv_commit, dim3(L * 2 * nkv), dim3(128), 0, s, d, cache, nkv, hd);
+    return cudaGetLastError();
+}
+
+cudaError_t kv_commit_split_launch(const SpecDev &d, __nv_bfloat16 *kc, __nv_bfloat16 *vc, int L, int nkv, int hd,
+                                   int seq, cudaStream_t s) {
+    launch_k(k_kv_commit_split, dim3(L * 2 * nkv), dim3(128), 0, s, d, kc, vc, hd, seq);
     return cudaGetLastError();
 }
 
