@@ -3,6 +3,8 @@
 //   write, split-K reduction + residual add + RMSNorm, split-K reduction +
 //   SwiGLU, and the vocabulary argmax (with softmax statistics for sampling).
 // The residual stream h stays fp32; T is the GEMM-input / KV-cache type.
+#include <algorithm>
+
 #include "la_kernels.h"
 
 namespace la {
@@ -121,10 +123,63 @@ cudaError_t qkv_rope_launch(const float *part, const int *planes, long long sstr
     return cudaGetLastError();
 }
 
-// bf16 models: one CTA = 32 rows x one head slot (a q, k or v head).  The
-// tile is summed into shared memory with coalesced row reads; q and k are
-// rotated and written along d, v is written transposed (consecutive rows are
-// consecutive cache columns).
+// Resident-SM count of the current device (cached per device): the grids
+// below are sized to run in one wave beside a resident GEMM CTA.
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 152;
+    }
+    return cached[dev];
+}
+
+__device__ __forceinline__ void add4(float4 &a, const float4 &b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+// Four consecutive activations (i % 4 == 0) in store_act form.
+__device__ __forceinline__ void store_act4(float *p, long long i, float4 v, long long) {
+    *reinterpret_cast<float4 *>(p + i) = v;
+}
+__device__ __forceinline__ void store_act4(__nv_bfloat16 *p, long long i, float4 v, long long lo_off) {
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+    uint2 hv, lv;
+    hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+    hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+    lv.x = *reinterpret_cast<const uint32_t *>(&l01);
+    lv.y = *reinterpret_cast<const uint32_t *>(&l23);
+    *reinterpret_cast<uint2 *>(p + i) = hv;
+    *reinterpret_cast<uint2 *>(p + i + lo_off) = lv;
+}
+// Sum of the partial planes of four consecutive columns (one 128-column
+// tile, np planes), added in plane order; loads go out two planes at a time.
+__device__ __forceinline__ float4 sum_planes4(const float *pc, long long sstride, int np) {
+    float4 a = *reinterpret_cast<const float4 *>(pc);
+    for (int b = 1; b < np; b += 2) {
+        const float4 x0 = *reinterpret_cast<const float4 *>(pc + b * sstride);
+        const float4 x1 = b + 1 < np ? *reinterpret_cast<const float4 *>(pc + (b + 1) * sstride)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        add4(a, x0);
+        if (b + 1 < np) add4(a, x1);
+    }
+    return a;
+}
+
+// bf16 models.  Work items, grid-stride over a grid sized to the SMs:
+//   q / k: (row, head, 4 rotary pairs i..i+3): columns i and i + hd/2 are
+//          summed over the planes, rotated (q also scaled by 1/sqrt(hd)) and
+//          written as (hi, lo) planes;
+//   v:     (KV head, 8 dims, row) with rows fastest, so the transposed cache
+//          stores of a warp hit 32 consecutive slots.
 template <int HD>
 __global__ void __launch_bounds__(256) k_qkv_rope_split(const float *part, const int *planes, long long sstride,
                                                         int ldp, int nrows, int nh, int nkv, int k_off, int v_off,
@@ -133,68 +188,57 @@ __global__ void __launch_bounds__(256) k_qkv_rope_split(const float *part, const
                                                         __nv_bfloat16 *vc, int layer, int seq) {
     pdl_trigger();
     pdl_wait();
-    __shared__ float t[32][HD + 1];
-    const int r0 = blockIdx.x * 32, hs = blockIdx.y;
-    const bool isq = hs < nh, isk = !isq && hs < nh + nkv;
-    const int col0 = isq ? hs * HD : isk ? k_off + (hs - nh) * HD : v_off + (hs - nh - nkv) * HD;
-    // A head's columns start on a 128-column tile, so the whole tile has one
-    // plane count; each plane's loads are all issued before they are added.
-    {
-        constexpr int PER = 32 * HD / 256;
-        const int np = planes ? planes[col0 >> 7] : 1;
-        float acc[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-        for (int pl = 0; pl < np; ++pl) {
-            const float *base = part + pl * sstride + col0;
-            float x[PER];
-#pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                const int i = threadIdx.x + j * 256, rr = i / HD, d = i % HD, r = r0 + rr;
-                x[j] = r < nrows ? base[static_cast<long long>(r) * ldp + d] : 0.f;
-            }
-#pragma unroll
-            for (int j = 0; j < PER; ++j) acc[j] += x[j];
-        }
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int i = threadIdx.x + j * 256;
-            t[i / HD][i % HD] = acc[j];
-        }
-    }
-    __syncthreads();
-    constexpr int half = HD / 2;
-    if (isq || isk) {
-        const int gq = nh / nkv;
-        const float scale = rsqrtf(static_cast<float>(HD));
-        for (int i = threadIdx.x; i < 32 * half; i += 256) {
-            const int rr = i / half, ii = i % half, r = r0 + rr;
-            if (r >= nrows) continue;
+    constexpr int half = HD / 2, Q4 = half / 4, D8 = HD / 8;
+    const int nhs = nh + nkv, gq = nh / nkv;
+    const long long nqk = static_cast<long long>(nrows) * nhs * Q4;
+    const long long nv = static_cast<long long>(nkv) * D8 * nrows;
+    const float scale = rsqrtf(static_cast<float>(HD));
+    for (long long t = blockIdx.x * 256ll + threadIdx.x; t < nqk + nv; t += gridDim.x * 256ll) {
+        if (t < nqk) {
+            const int j = static_cast<int>(t % Q4);
+            const long long u = t / Q4;
+            const int hs = static_cast<int>(u % nhs), r = static_cast<int>(u / nhs);
+            const bool isq = hs < nh;
+            const int col0 = isq ? hs * HD : k_off + (hs - nh) * HD;
+            const int np = planes ? planes[col0 >> 7] : 1;
+            const float *pr = part + static_cast<long long>(r) * ldp + col0 + 4 * j;
+            const float4 x1 = sum_planes4(pr, sstride, np), x2 = sum_planes4(pr + half, sstride, np);
             const int pos = P + (depth ? depth[r] : r);
-            const float2 c = rope[static_cast<long long>(pos) * half + ii];
-            const float x1 = t[rr][ii], x2 = t[rr][ii + half];
-            float y1 = x1 * c.x - x2 * c.y, y2 = x1 * c.y + x2 * c.x;
+            const float4 c01 = *reinterpret_cast<const float4 *>(rope + static_cast<long long>(pos) * half + 4 * j);
+            const float4 c23 = *reinterpret_cast<const float4 *>(rope + static_cast<long long>(pos) * half + 4 * j + 2);
+            // (cos, sin) pairs: c01 = (c0, s0, c1, s1), c23 = (c2, s2, c3, s3)
+            float4 y1 = make_float4(x1.x * c01.x - x2.x * c01.y, x1.y * c01.z - x2.y * c01.w,
+                                    x1.z * c23.x - x2.z * c23.y, x1.w * c23.z - x2.w * c23.w);
+            float4 y2 = make_float4(x1.x * c01.y + x2.x * c01.x, x1.y * c01.w + x2.y * c01.z,
+                                    x1.z * c23.y + x2.z * c23.x, x1.w * c23.w + x2.w * c23.z);
             if (isq) {
+                y1 = make_float4(y1.x * scale, y1.y * scale, y1.z * scale, y1.w * scale);
+                y2 = make_float4(y2.x * scale, y2.y * scale, y2.z * scale, y2.w * scale);
                 const int g = hs / gq, qv = r * gq + hs % gq;
                 const long long base = (static_cast<long long>(g) * qv_pad + qv) * HD;
                 const long long lo = static_cast<long long>(nkv) * qv_pad * HD;
-                store_act(q, base + ii, y1 * scale, lo);
-                store_act(q, base + ii + half, y2 * scale, lo);
+                store_act4(q, base + 4 * j, y1, lo);
+                store_act4(q, base + half + 4 * j, y2, lo);
             } else {
                 const long long base = ((static_cast<long long>(layer) * 2 * nkv + (hs - nh)) * seq + P + r) * HD;
                 const long long lo = static_cast<long long>(nkv) * seq * HD;
-                store_act(kc, base + ii, y1, lo);
-                store_act(kc, base + ii + half, y2, lo);
+                store_act4(kc, base + 4 * j, y1, lo);
+                store_act4(kc, base + half + 4 * j, y2, lo);
             }
-        }
-    } else {
-        const int vh = hs - nh - nkv;
-        const long long lo = static_cast<long long>(nkv) * HD * seq;
-        for (int i = threadIdx.x; i < 32 * HD; i += 256) {
-            const int d = i / 32, rr = i % 32, r = r0 + rr;
-            if (r >= nrows) continue;
-            const long long idx = ((static_cast<long long>(layer) * 2 * nkv + vh) * HD + d) * seq + P + r;
-            store_act(vc, idx, t[rr][d], lo);
+        } else {
+            const long long t2 = t - nqk;
+            const int r = static_cast<int>(t2 % nrows);
+            const long long u = t2 / nrows;
+            const int d8 = static_cast<int>(u % D8), vh = static_cast<int>(u / D8);
+            const int col = v_off + vh * HD + 8 * d8;
+            const int np = planes ? planes[col >> 7] : 1;
+            const float *pr = part + static_cast<long long>(r) * ldp + col;
+            const float4 a = sum_planes4(pr, sstride, np), b = sum_planes4(pr + 4, sstride, np);
+            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            const long long lo = static_cast<long long>(nkv) * HD * seq;
+            const long long base = ((static_cast<long long>(layer) * 2 * nkv + vh) * HD + 8 * d8) * seq + P + r;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) store_act(vc, base + static_cast<long long>(e) * seq, v[e], lo);
         }
     }
 }
@@ -203,13 +247,14 @@ cudaError_t qkv_rope_split_launch(const float *part, const int *planes, long lon
                                   int nh, int nkv, int hd, int k_off, int v_off, const float2 *rope, int P,
                                   const int *depth, __nv_bfloat16 *q, int qv_pad, __nv_bfloat16 *kc,
                                   __nv_bfloat16 *vc, int layer, int seq, cudaStream_t s) {
-    dim3 grid((nrows + 31) / 32, nh + 2 * nkv);
+    const long long items = static_cast<long long>(nrows) * (nh + nkv) * (hd / 8) + static_cast<long long>(nkv) * (hd / 8) * nrows;
+    const int grid = static_cast<int>(std::min<long long>((items + 255) / 256, 3ll * sm_count()));
     if (hd == 128)
-        launch_k(k_qkv_rope_split<128>, grid, dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv, k_off,
-                 v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
+        launch_k(k_qkv_rope_split<128>, dim3(grid), dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv,
+                 k_off, v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
     else if (hd == 64)
-        launch_k(k_qkv_rope_split<64>, grid, dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv, k_off,
-                 v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
+        launch_k(k_qkv_rope_split<64>, dim3(grid), dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv,
+                 k_off, v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();
@@ -217,13 +262,16 @@ cudaError_t qkv_rope_split_launch(const float *part, const int *planes, long lon
 
 // ------------------------------------------------------------------ residual + norm
 // Output row i reads residual row r = row_map[i] (or i): h[r] += sum_s part[s][r];
-// xout[i] = rmsnorm(h[r]) * gain.  d % 4 == 0; float4 accesses, all loads of
-// a thread issued before the reduction.
-template <typename T>
-__global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part, const int *planes,
-                                                     long long sstride, int ldp,
-                                                     int d, const T *gain, float eps, const int *row_map, T *xout,
-                                                     long long lo_off) {
+// xout[i] = rmsnorm(h[r]) * gain.  One CTA of 512 threads per row, PER float4
+// columns per thread (d <= 2048 PER), the planes of all of a thread's
+// columns loaded together.  512 threads keep the CTA small enough to sit
+// beside a resident GEMM CTA.
+constexpr int kNormThreads = 512;
+template <typename T, int PER>
+__global__ void __launch_bounds__(kNormThreads) k_resid_norm(float *h, const float *part, const int *planes,
+                                                             long long sstride, int ldp, int d, const T *gain,
+                                                             float eps, const int *row_map, T *xout,
+                                                             long long lo_off) {
     pdl_trigger();
     pdl_wait();
     __shared__ float red[32];
@@ -232,45 +280,46 @@ __global__ void __launch_bounds__(1024) k_resid_norm(float *h, const float *part
     float4 *hr = reinterpret_cast<float4 *>(h + static_cast<long long>(r) * d);
     const float *pr = part + static_cast<long long>(r) * ldp;
     const int d4 = d / 4;
-    constexpr int kMaxPer = 4;   // d <= 16384
-    float4 v[kMaxPer];
+    float4 acc[PER];
+    int np[PER];
+    int npmax = 1;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+        const int c = threadIdx.x + j * kNormThreads;
+        acc[j] = c < d4 ? hr[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        np[j] = c < d4 ? (planes ? planes[(4 * c) >> 7] : 1) : 0;
+        npmax = max(npmax, np[j]);
+    }
+    for (int b = 0; b < npmax; ++b) {
+        float4 x[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int c = threadIdx.x + j * kNormThreads;
+            x[j] = b < np[j] ? *reinterpret_cast<const float4 *>(pr + b * sstride + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < PER; ++j) add4(acc[j], x[j]);
+    }
     float ss = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxPer; ++j) {
-        const int c = threadIdx.x + j * 1024;
+    for (int j = 0; j < PER; ++j) {
+        const int c = threadIdx.x + j * kNormThreads;
         if (c < d4) {
-            float4 a = hr[c];
-            const int np = planes ? planes[(4 * c) >> 7] : 1;
-            for (int b0 = 0; b0 < np; b0 += 8) {
-                float4 x[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    x[j] = (b0 + j < np) ? *reinterpret_cast<const float4 *>(pr + (b0 + j) * sstride + 4 * c)
-                                         : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    a.x += x[j].x;
-                    a.y += x[j].y;
-                    a.z += x[j].z;
-                    a.w += x[j].w;
-                }
-            }
-            v[j] = a;
-            hr[c] = a;
-            ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w;
+            hr[c] = acc[j];
+            ss += acc[j].x * acc[j].x + acc[j].y * acc[j].y + acc[j].z * acc[j].z + acc[j].w * acc[j].w;
         }
     }
-    const float inv = rsqrtf(block_sum<1024>(ss, red) / d + eps);
+    const float inv = rsqrtf(block_sum<kNormThreads>(ss, red) / d + eps);
     const long long o = static_cast<long long>(i) * d;
 #pragma unroll
-    for (int j = 0; j < kMaxPer; ++j) {
-        const int c = threadIdx.x + j * 1024;
+    for (int j = 0; j < PER; ++j) {
+        const int c = threadIdx.x + j * kNormThreads;
         if (c < d4) {
-            const float4 a = v[j];
-            store_act(xout, o + 4 * c + 0, a.x * inv * to_f32(gain[4 * c + 0]), lo_off);
-            store_act(xout, o + 4 * c + 1, a.y * inv * to_f32(gain[4 * c + 1]), lo_off);
-            store_act(xout, o + 4 * c + 2, a.z * inv * to_f32(gain[4 * c + 2]), lo_off);
-            store_act(xout, o + 4 * c + 3, a.w * inv * to_f32(gain[4 * c + 3]), lo_off);
+            const float4 a = acc[j];
+            store_act4(xout, o + 4 * c,
+                       make_float4(a.x * inv * to_f32(gain[4 * c + 0]), a.y * inv * to_f32(gain[4 * c + 1]),
+                                   a.z * inv * to_f32(gain[4 * c + 2]), a.w * inv * to_f32(gain[4 * c + 3])),
+                       lo_off);
         }
     }
 }
@@ -280,34 +329,46 @@ cudaError_t resid_norm_launch(float *h, const float *part, const int *planes, lo
                               const T *gain, float eps, const int *row_map, int nrows, T *xout, long long lo_off,
                               cudaStream_t s) {
     if (d % 4 || d > 16384) return cudaErrorInvalidValue;
-    launch_k(k_resid_norm<T>, dim3(nrows), dim3(1024), 0, s, h, part, planes, sstride, ldp, d, gain, eps, row_map, xout, lo_off);
+    const int per = (d / 4 + kNormThreads - 1) / kNormThreads;
+    const dim3 g(nrows), b(kNormThreads);
+    switch (per) {
+        case 1: launch_k(k_resid_norm<T, 1>, g, b, 0, s, h, part, planes, sstride, ldp, d, gain, eps, row_map, xout, lo_off); break;
+        case 2: launch_k(k_resid_norm<T, 2>, g, b, 0, s, h, part, planes, sstride, ldp, d, gain, eps, row_map, xout, lo_off); break;
+        case 3: launch_k(k_resid_norm<T, 3>, g, b, 0, s, h, part, planes, sstride, ldp, d, gain, eps, row_map, xout, lo_off); break;
+        case 4: launch_k(k_resid_norm<T, 4>, g, b, 0, s, h, part, planes, sstride, ldp, d, gain, eps, row_map, xout, lo_off); break;
+        default: launch_k(k_resid_norm<T, 8>, g, b, 0, s, h, part, planes, sstride, ldp, d, gain, eps, row_map, xout, lo_off); break;
+    }
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ SwiGLU
-// part columns: gate [0, F) | up [F, 2F).  out[r][f] = silu(gate) * up.
+// part columns: gate [0, F) | up [up_off, up_off + F).  out[r][f] = silu(gate) * up.
+// Items of four columns, grid-stride over a grid sized to the SMs; F % 4 == 0.
 template <typename T>
-__global__ void k_swiglu(const float *part, const int *planes, long long sstride, int ldp, int nrows, int F,
-                         int up_off, T *out, long long lo_off) {
+__global__ void __launch_bounds__(256) k_swiglu(const float *part, const int *planes, long long sstride, int ldp,
+                                                int nrows, int F, int up_off, T *out, long long lo_off) {
     pdl_trigger();
     pdl_wait();
-    const long long n = static_cast<long long>(nrows) * F;
-    for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
-         t += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int r = static_cast<int>(t / F), f = static_cast<int>(t % F);
+    const int F4 = F / 4;
+    const long long n = static_cast<long long>(nrows) * F4;
+    for (long long t = blockIdx.x * 256ll + threadIdx.x; t < n; t += gridDim.x * 256ll) {
+        const int r = static_cast<int>(t / F4), f = 4 * static_cast<int>(t % F4);
         const float *pr = part + static_cast<long long>(r) * ldp;
-        const float g = sum_planes(pr, planes, sstride, f);
-        const float u = sum_planes(pr, planes, sstride, up_off + f);
-        store_act(out, t, g / (1.f + expf(-g)) * u, lo_off);
+        const int npg = planes ? planes[f >> 7] : 1, npu = planes ? planes[(up_off + f) >> 7] : 1;
+        const float4 g = sum_planes4(pr + f, sstride, npg), u = sum_planes4(pr + up_off + f, sstride, npu);
+        store_act4(out, static_cast<long long>(r) * F + f,
+                   make_float4(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y,
+                               g.z / (1.f + expf(-g.z)) * u.z, g.w / (1.f + expf(-g.w)) * u.w),
+                   lo_off);
     }
 }
 
 template <typename T>
 cudaError_t swiglu_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows, int F,
                           int up_off, T *out, long long lo_off, cudaStream_t s) {
-    const long long n = static_cast<long long>(nrows) * F;
-    int blocks = static_cast<int>((n + 255) / 256);
-    if (blocks > 152 * 64) blocks = 152 * 64;
+    if (F % 4) return cudaErrorInvalidValue;
+    const long long n = static_cast<long long>(nrows) * (F / 4);
+    const int blocks = static_cast<int>(std::min<long long>((n + 255) / 256, 3ll * sm_count()));
     launch_k(k_swiglu<T>, dim3(blocks), dim3(256), 0, s, part, planes, sstride, ldp, nrows, F, up_off, out, lo_off);
     return cudaGetLastError();
 }
