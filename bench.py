@@ -43,7 +43,7 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=32)
+    ap.add_argument("--steps", type=int, default=240)
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama7b-bf16-greedy")
@@ -84,7 +84,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except Exception:
@@ -125,10 +125,10 @@ class ClockSampler:
 
 
 def gemm_traffic():
-    """DRAM bytes per k_gemm_tc launch from the committed ncu summary, or None
+    """DRAM bytes per k_gemm_tc2 launch from the committed ncu summary, or None
     when the kernel sources changed since those counters were taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "k_gemm_tc_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "k_gemm_tc2_traffic.txt")
     if not os.path.exists(path):
         return None
     rec = dict(line.split() for line in open(path) if line.strip())
@@ -330,7 +330,7 @@ def run_ours(args, wl, rank, world, local_rank):
     d = wl.dims
     act = 2 if d.dtype == "bf16" else 4
     weight_bytes = sum(t.numel() * t.element_size() for t in dw._keep if hasattr(t, "numel")) - d.vocab * d.d_model * act
-    kv_per_tok = 2 * d.n_layers * d.n_kv_heads * d.head_dim * 4   # fp32 KV cache
+    kv_per_tok = 2 * d.n_layers * d.n_kv_heads * d.head_dim * 4   # K, V as fp32 or bf16 (hi, lo): 4 bytes each
     mean_P = statistics.mean(prefixes)
     step_bytes = weight_bytes + mean_P * kv_per_tok + wl.M * d.d_model * act + wl.N * kv_per_tok
     peak, peak_kind = peaks()
@@ -355,7 +355,7 @@ def run_ours(args, wl, rank, world, local_rank):
                 "d2h_bytes_per_step": 64.0 * (gen_steps + 1) / max(gen_steps, 1) + 4.0,
                 "tokens": len(toks), "steps": gen_steps, "seconds": e2e_s},
         "gpu_launches": int(launches),
-        "roofline": {"bound": "hbm", "kernel": "k_gemm_tc (tcgen05 projection GEMM, all launches of a step)",
+        "roofline": {"bound": "hbm", "kernel": "k_gemm_tc2 (2-SM tcgen05 projection GEMM, all launches of a step)",
                      "achieved": gemm_gbs, "peak": peak, "unit": "GB/s",
                      "frac": (gemm_gbs / peak) if gemm_gbs else None, "traffic": gemm_traffic(),
                      "peak_source": peak_kind, "launch_ms": pst["gemm_ms"] / max(pst["gemm_launches"], 1),

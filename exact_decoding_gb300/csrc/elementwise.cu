@@ -160,18 +160,27 @@ __device__ __forceinline__ void store_act4(__nv_bfloat16 *p, long long i, float4
     *reinterpret_cast<uint2 *>(p + i) = hv;
     *reinterpret_cast<uint2 *>(p + i + lo_off) = lv;
 }
-// Sum of the partial planes of four consecutive columns (one 128-column
-// tile, np planes), added in plane order; loads go out two planes at a time.
-__device__ __forceinline__ float4 sum_planes4(const float *pc, long long sstride, int np) {
-    float4 a = *reinterpret_cast<const float4 *>(pc);
-    for (int b = 1; b < np; b += 2) {
-        const float4 x0 = *reinterpret_cast<const float4 *>(pc + b * sstride);
-        const float4 x1 = b + 1 < np ? *reinterpret_cast<const float4 *>(pc + (b + 1) * sstride)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        add4(a, x0);
-        if (b + 1 < np) add4(a, x1);
+// Sums of the partial planes of two runs of four consecutive columns (each
+// inside one 128-column tile with na / nb planes), added in plane order.
+// All loads of a batch of four planes per run are issued before any add.
+__device__ __forceinline__ void sum_planes4x2(const float *pa, int na, const float *pb, int nb, long long sstride,
+                                              float4 &ra, float4 &rb) {
+    ra = make_float4(0.f, 0.f, 0.f, 0.f);
+    rb = ra;
+    const int n = max(na, nb);
+    for (int b0 = 0; b0 < n; b0 += 4) {
+        float4 xa[4], xb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            xa[k] = b0 + k < na ? *reinterpret_cast<const float4 *>(pa + (b0 + k) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xb[k] = b0 + k < nb ? *reinterpret_cast<const float4 *>(pb + (b0 + k) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (b0 + k < na) add4(ra, xa[k]);
+            if (b0 + k < nb) add4(rb, xb[k]);
+        }
     }
-    return a;
 }
 
 // bf16 models.  Work items, grid-stride over a grid sized to the SMs:
@@ -200,12 +209,13 @@ __global__ void __launch_bounds__(256) k_qkv_rope_split(const float *part, const
             const int hs = static_cast<int>(u % nhs), r = static_cast<int>(u / nhs);
             const bool isq = hs < nh;
             const int col0 = isq ? hs * HD : k_off + (hs - nh) * HD;
-            const int np = planes ? planes[col0 >> 7] : 1;
-            const float *pr = part + static_cast<long long>(r) * ldp + col0 + 4 * j;
-            const float4 x1 = sum_planes4(pr, sstride, np), x2 = sum_planes4(pr + half, sstride, np);
             const int pos = P + (depth ? depth[r] : r);
             const float4 c01 = *reinterpret_cast<const float4 *>(rope + static_cast<long long>(pos) * half + 4 * j);
             const float4 c23 = *reinterpret_cast<const float4 *>(rope + static_cast<long long>(pos) * half + 4 * j + 2);
+            const int np = planes ? planes[col0 >> 7] : 1;
+            const float *pr = part + static_cast<long long>(r) * ldp + col0 + 4 * j;
+            float4 x1, x2;
+            sum_planes4x2(pr, np, pr + half, np, sstride, x1, x2);
             // (cos, sin) pairs: c01 = (c0, s0, c1, s1), c23 = (c2, s2, c3, s3)
             float4 y1 = make_float4(x1.x * c01.x - x2.x * c01.y, x1.y * c01.z - x2.y * c01.w,
                                     x1.z * c23.x - x2.z * c23.y, x1.w * c23.z - x2.w * c23.w);
@@ -233,7 +243,8 @@ __global__ void __launch_bounds__(256) k_qkv_rope_split(const float *part, const
             const int col = v_off + vh * HD + 8 * d8;
             const int np = planes ? planes[col >> 7] : 1;
             const float *pr = part + static_cast<long long>(r) * ldp + col;
-            const float4 a = sum_planes4(pr, sstride, np), b = sum_planes4(pr + 4, sstride, np);
+            float4 a, b;
+            sum_planes4x2(pr, np, pr + 4, np, sstride, a, b);
             const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
             const long long lo = static_cast<long long>(nkv) * HD * seq;
             const long long base = ((static_cast<long long>(layer) * 2 * nkv + vh) * HD + 8 * d8) * seq + P + r;
@@ -290,15 +301,23 @@ __global__ void __launch_bounds__(kNormThreads) k_resid_norm(float *h, const flo
         np[j] = c < d4 ? (planes ? planes[(4 * c) >> 7] : 1) : 0;
         npmax = max(npmax, np[j]);
     }
-    for (int b = 0; b < npmax; ++b) {
-        float4 x[PER];
+    // Planes in batches: up to 8 / PER planes of every column in flight.
+    constexpr int BP = PER >= 8 ? 1 : 8 / PER;
+    for (int b0 = 0; b0 < npmax; b0 += BP) {
+        float4 x[PER][BP];
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int c = threadIdx.x + j * kNormThreads;
-            x[j] = b < np[j] ? *reinterpret_cast<const float4 *>(pr + b * sstride + 4 * c) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < BP; ++k)
+                x[j][k] = b0 + k < np[j] ? *reinterpret_cast<const float4 *>(pr + (b0 + k) * sstride + 4 * c)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int j = 0; j < PER; ++j) add4(acc[j], x[j]);
+        for (int j = 0; j < PER; ++j)
+#pragma unroll
+            for (int k = 0; k < BP; ++k)
+                if (b0 + k < np[j]) add4(acc[j], x[j][k]);
     }
     float ss = 0.f;
 #pragma unroll
@@ -355,7 +374,8 @@ __global__ void __launch_bounds__(256) k_swiglu(const float *part, const int *pl
         const int r = static_cast<int>(t / F4), f = 4 * static_cast<int>(t % F4);
         const float *pr = part + static_cast<long long>(r) * ldp;
         const int npg = planes ? planes[f >> 7] : 1, npu = planes ? planes[(up_off + f) >> 7] : 1;
-        const float4 g = sum_planes4(pr + f, sstride, npg), u = sum_planes4(pr + up_off + f, sstride, npu);
+        float4 g, u;
+        sum_planes4x2(pr + f, npg, pr + up_off + f, npu, sstride, g, u);
         store_act4(out, static_cast<long long>(r) * F + f,
                    make_float4(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y,
                                g.z / (1.f + expf(-g.z)) * u.z, g.w / (1.f + expf(-g.w)) * u.w),
