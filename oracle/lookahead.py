@@ -12,7 +12,7 @@ Decoding" (arXiv 2402.02057), paper-graph-ui summary, section 3.4:
 Autoregressive greedy decoding (section 3.4, "The autoregressive system") is
 the reference the method must reproduce exactly (lossless).
 
-Readings taken where the pages are open (each is listed in the design doc):
+Readings taken where the pages are open:
   R1 Step rows.  Row 0 is the last committed token o at position P (the
      prefix [0, P) is cached).  Lookahead row (k, j), level k in [0, N-2],
      column j in [0, W-1], holds window token V[k][j] at position P+1+j+k.
