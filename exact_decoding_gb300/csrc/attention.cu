@@ -234,7 +234,12 @@ cudaError_t attention_launch(const AttnArgs &a, cudaStream_t s) {
 }
 
 // ========================================================================== tcgen05 path (bf16 models)
-// One cluster of `cs` CTAs per (KV head g, tile of 128 query vectors); CTA
+// One cluster of `cs` CTAs per (KV head g, tile of 128 query vectors).
+// Prologue: the cluster's CTAs share the work of summing the QKV GEMM's
+// partial planes for KV head g, rotating q and k, scaling q, and writing the
+// (hi, lo) planes of the tile's query vectors and of this step's K/V rows
+// (clusters of the same KV head write identical K/V bytes); a proxy fence and
+// a cluster barrier then make those writes visible to the TMA loads.  CTA
 // rank j of the cluster takes the 128-key chunks [j n / cs, (j + 1) n / cs)
 // of the keys [0, P + nrows): the cached prefix, then this step's own rows.
 // Per chunk:
@@ -269,7 +274,8 @@ struct AttnLayout {
     static constexpr uint32_t ml_off = v_off + v_bytes;                  // m[128], l[128]
     static constexpr uint32_t red_off = ml_off + 2u * kUQ * 4u;          // [4][128] per-quarter partials
     static constexpr uint32_t vis_off = red_off + 4u * kUQ * 4u;         // [128][8] visibility words; merge weights
-    static constexpr uint32_t bar_off = vis_off + kUQ * 8u * 4u;         // 4 mbarriers + TMEM slot
+    static constexpr uint32_t tab_off = vis_off + kUQ * 8u * 4u;         // [128] row depths, [256] plane counts
+    static constexpr uint32_t bar_off = tab_off + (kUQ + 256u) * 4u;     // 4 mbarriers + TMEM slot
     static constexpr uint32_t bytes = bar_off + 64u + 1024u;             // + alignment slack
     static_assert(static_cast<uint32_t>(kUQ) * o_ld * 4u <= q_bytes + kp_bytes, "merge rows overlay Q and K/P");
 };
@@ -337,7 +343,108 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     const bool valid = qv < QV;
     const int r = valid ? qv / p.gq : 0;
 
-    pdl_wait();   // q, the cache rows of this step and the visibility bits come from earlier kernels
+    // Tables written once at create time (safe to read before the wait):
+    // the step rows' depths and the QKV tiles' partial-plane counts.
+    int *sdep = reinterpret_cast<int *>(smem + Lay::tab_off);
+    int *splanes = sdep + kUQ;
+    for (int i = tid; i < kUQ + 256; i += kUThreads) {
+        if (i < kUQ) sdep[i] = i < p.nrows ? (p.depth ? p.depth[i] : i) : 0;
+        else splanes[i - kUQ] = (p.planes && i - kUQ < p.qkv_tiles) ? p.planes[i - kUQ] : 1;
+    }
+    __syncthreads();
+    auto nplanes = [&](int col) -> int {
+        const int t = col >> 7;
+        return !p.planes ? 1 : (t < 256 ? splanes[t] : p.planes[t]);
+    };
+    pdl_wait();   // the QKV planes and the visibility bits come from earlier kernels
+    {
+        // Prologue work items (rows fastest for v, so the transposed stores of a
+        // warp hit consecutive slots), two per iteration so that their loads
+        // are in flight together:
+        //   q: (query vector of this tile, 4 rotary pairs i..i+3)
+        //   k: (step row, 4 rotary pairs)          v: (step row, 8 dims)
+        constexpr int half = HD / 2, Q4 = HD / 8, D8 = HD / 8;
+        const int qv0 = qt * kUQ, nqv = max(0, min(kUQ, QV - qv0));
+        const int nq = nqv * Q4, nk = p.nrows * Q4, nv = p.nrows * D8, total = nq + nk + nv;
+        const float scale = rsqrtf(static_cast<float>(HD));
+        const int stride = cs * kUThreads;
+        struct Item {
+            float4 a, b, c01, c23;   // rotary: x1, x2, (cos, sin) pairs; v: dims 0..3, 4..7
+            long long dst, lo;
+            int kind, j;             // 0 q, 1 k, 2 v, -1 none
+        };
+        auto load = [&](int t, Item &it) {
+            it.kind = -1;
+            if (t >= total) return;
+            if (t < nq + nk) {
+                const bool isq = t < nq;
+                const int u = isq ? t : t - nq;
+                int r, col0;
+                it.j = u % Q4;
+                if (isq) {
+                    const int qvv = qv0 + u / Q4;
+                    r = qvv / p.gq;
+                    col0 = (g * p.gq + qvv % p.gq) * HD;
+                    it.dst = (static_cast<long long>(g) * p.qv_pad + qvv) * HD;
+                    it.lo = static_cast<long long>(p.nkv) * p.qv_pad * HD;
+                } else {
+                    r = u / Q4;
+                    col0 = p.k_off + g * HD;
+                    it.dst = ((static_cast<long long>(p.layer) * 2 * p.nkv + g) * p.seq + p.P + r) * HD;
+                    it.lo = static_cast<long long>(p.nkv) * p.seq * HD;
+                }
+                it.kind = isq ? 0 : 1;
+                const float2 *rr = p.rope + static_cast<long long>(p.P + sdep[r]) * half + 4 * it.j;
+                it.c01 = *reinterpret_cast<const float4 *>(rr);
+                it.c23 = *reinterpret_cast<const float4 *>(rr + 2);
+                const int np = nplanes(col0);
+                const float *pr = p.part + static_cast<long long>(r) * p.ldp + col0 + 4 * it.j;
+                sum_planes4x2(pr, np, pr + half, np, p.sstride, it.a, it.b);
+            } else {
+                const int u = t - nq - nk, r = u % p.nrows, d8 = u / p.nrows;
+                const int col = p.v_off + g * HD + 8 * d8;
+                const float *pr = p.part + static_cast<long long>(r) * p.ldp + col;
+                const int np = nplanes(col);
+                sum_planes4x2(pr, np, pr + 4, np, p.sstride, it.a, it.b);
+                it.kind = 2;
+                it.lo = static_cast<long long>(p.nkv) * HD * p.seq;
+                it.dst = ((static_cast<long long>(p.layer) * 2 * p.nkv + g) * HD + 8 * d8) * p.seq + p.P + r;
+            }
+        };
+        auto store = [&](const Item &it) {
+            if (it.kind < 0) return;
+            if (it.kind < 2) {
+                const float4 x1 = it.a, x2 = it.b, c01 = it.c01, c23 = it.c23;
+                float4 y1 = make_float4(x1.x * c01.x - x2.x * c01.y, x1.y * c01.z - x2.y * c01.w,
+                                        x1.z * c23.x - x2.z * c23.y, x1.w * c23.z - x2.w * c23.w);
+                float4 y2 = make_float4(x1.x * c01.y + x2.x * c01.x, x1.y * c01.w + x2.y * c01.z,
+                                        x1.z * c23.y + x2.z * c23.x, x1.w * c23.w + x2.w * c23.z);
+                if (it.kind == 0) {
+                    y1 = make_float4(y1.x * scale, y1.y * scale, y1.z * scale, y1.w * scale);
+                    y2 = make_float4(y2.x * scale, y2.y * scale, y2.z * scale, y2.w * scale);
+                }
+                __nv_bfloat16 *base = it.kind == 0 ? p.q : p.kc;
+                store_act4(base, it.dst + 4 * it.j, y1, it.lo);
+                store_act4(base, it.dst + half + 4 * it.j, y2, it.lo);
+            } else {
+                const float v[8] = {it.a.x, it.a.y, it.a.z, it.a.w, it.b.x, it.b.y, it.b.z, it.b.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) store_act(p.vc, it.dst + static_cast<long long>(e) * p.seq, v[e], it.lo);
+            }
+        };
+        for (int t = static_cast<int>(rank) * kUThreads + tid; t < total; t += 2 * stride) {
+            Item i0, i1;
+            load(t, i0);
+            load(t + stride, i1);
+            store(i0);
+            store(i1);
+        }
+        // These generic-proxy global writes are read next by TMA (async proxy)
+        // in every CTA of the cluster.
+        __threadfence();
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    cluster_sync_all();
     if (cw == 0) {
 #pragma unroll
         for (int w = 0; w < 8; ++w) svis[row * 8 + w] = (valid && p.vis_bits) ? p.vis_bits[r * 8 + w] : 0u;
@@ -393,6 +500,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
                             bar_v, pol);
     };
     if (tid == 0 && c_beg < c_end) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
         const uint64_t pol = policy_evict_normal();   // other query tiles of this KV head read the same chunks
         mbar_arrive_expect_tx(bar_ld, Lay::q_bytes + Lay::k_bytes);
 #pragma unroll

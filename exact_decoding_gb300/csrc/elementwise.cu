@@ -137,140 +137,6 @@ static int sm_count() {
     return cached[dev];
 }
 
-__device__ __forceinline__ void add4(float4 &a, const float4 &b) {
-    a.x += b.x;
-    a.y += b.y;
-    a.z += b.z;
-    a.w += b.w;
-}
-// Four consecutive activations (i % 4 == 0) in store_act form.
-__device__ __forceinline__ void store_act4(float *p, long long i, float4 v, long long) {
-    *reinterpret_cast<float4 *>(p + i) = v;
-}
-__device__ __forceinline__ void store_act4(__nv_bfloat16 *p, long long i, float4 v, long long lo_off) {
-    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
-    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
-    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
-    uint2 hv, lv;
-    hv.x = *reinterpret_cast<const uint32_t *>(&h01);
-    hv.y = *reinterpret_cast<const uint32_t *>(&h23);
-    lv.x = *reinterpret_cast<const uint32_t *>(&l01);
-    lv.y = *reinterpret_cast<const uint32_t *>(&l23);
-    *reinterpret_cast<uint2 *>(p + i) = hv;
-    *reinterpret_cast<uint2 *>(p + i + lo_off) = lv;
-}
-// Sums of the partial planes of two runs of four consecutive columns (each
-// inside one 128-column tile with na / nb planes), added in plane order.
-// All loads of a batch of four planes per run are issued before any add.
-__device__ __forceinline__ void sum_planes4x2(const float *pa, int na, const float *pb, int nb, long long sstride,
-                                              float4 &ra, float4 &rb) {
-    ra = make_float4(0.f, 0.f, 0.f, 0.f);
-    rb = ra;
-    const int n = max(na, nb);
-    for (int b0 = 0; b0 < n; b0 += 4) {
-        float4 xa[4], xb[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            xa[k] = b0 + k < na ? *reinterpret_cast<const float4 *>(pa + (b0 + k) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-            xb[k] = b0 + k < nb ? *reinterpret_cast<const float4 *>(pb + (b0 + k) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            if (b0 + k < na) add4(ra, xa[k]);
-            if (b0 + k < nb) add4(rb, xb[k]);
-        }
-    }
-}
-
-// bf16 models.  Work items, grid-stride over a grid sized to the SMs:
-//   q / k: (row, head, 4 rotary pairs i..i+3): columns i and i + hd/2 are
-//          summed over the planes, rotated (q also scaled by 1/sqrt(hd)) and
-//          written as (hi, lo) planes;
-//   v:     (KV head, 8 dims, row) with rows fastest, so the transposed cache
-//          stores of a warp hit 32 consecutive slots.
-template <int HD>
-__global__ void __launch_bounds__(256) k_qkv_rope_split(const float *part, const int *planes, long long sstride,
-                                                        int ldp, int nrows, int nh, int nkv, int k_off, int v_off,
-                                                        const float2 *rope, int P, const int *depth,
-                                                        __nv_bfloat16 *q, int qv_pad, __nv_bfloat16 *kc,
-                                                        __nv_bfloat16 *vc, int layer, int seq) {
-    pdl_trigger();
-    pdl_wait();
-    constexpr int half = HD / 2, Q4 = half / 4, D8 = HD / 8;
-    const int nhs = nh + nkv, gq = nh / nkv;
-    const long long nqk = static_cast<long long>(nrows) * nhs * Q4;
-    const long long nv = static_cast<long long>(nkv) * D8 * nrows;
-    const float scale = rsqrtf(static_cast<float>(HD));
-    for (long long t = blockIdx.x * 256ll + threadIdx.x; t < nqk + nv; t += gridDim.x * 256ll) {
-        if (t < nqk) {
-            const int j = static_cast<int>(t % Q4);
-            const long long u = t / Q4;
-            const int hs = static_cast<int>(u % nhs), r = static_cast<int>(u / nhs);
-            const bool isq = hs < nh;
-            const int col0 = isq ? hs * HD : k_off + (hs - nh) * HD;
-            const int pos = P + (depth ? depth[r] : r);
-            const float4 c01 = *reinterpret_cast<const float4 *>(rope + static_cast<long long>(pos) * half + 4 * j);
-            const float4 c23 = *reinterpret_cast<const float4 *>(rope + static_cast<long long>(pos) * half + 4 * j + 2);
-            const int np = planes ? planes[col0 >> 7] : 1;
-            const float *pr = part + static_cast<long long>(r) * ldp + col0 + 4 * j;
-            float4 x1, x2;
-            sum_planes4x2(pr, np, pr + half, np, sstride, x1, x2);
-            // (cos, sin) pairs: c01 = (c0, s0, c1, s1), c23 = (c2, s2, c3, s3)
-            float4 y1 = make_float4(x1.x * c01.x - x2.x * c01.y, x1.y * c01.z - x2.y * c01.w,
-                                    x1.z * c23.x - x2.z * c23.y, x1.w * c23.z - x2.w * c23.w);
-            float4 y2 = make_float4(x1.x * c01.y + x2.x * c01.x, x1.y * c01.w + x2.y * c01.z,
-                                    x1.z * c23.y + x2.z * c23.x, x1.w * c23.w + x2.w * c23.z);
-            if (isq) {
-                y1 = make_float4(y1.x * scale, y1.y * scale, y1.z * scale, y1.w * scale);
-                y2 = make_float4(y2.x * scale, y2.y * scale, y2.z * scale, y2.w * scale);
-                const int g = hs / gq, qv = r * gq + hs % gq;
-                const long long base = (static_cast<long long>(g) * qv_pad + qv) * HD;
-                const long long lo = static_cast<long long>(nkv) * qv_pad * HD;
-                store_act4(q, base + 4 * j, y1, lo);
-                store_act4(q, base + half + 4 * j, y2, lo);
-            } else {
-                const long long base = ((static_cast<long long>(layer) * 2 * nkv + (hs - nh)) * seq + P + r) * HD;
-                const long long lo = static_cast<long long>(nkv) * seq * HD;
-                store_act4(kc, base + 4 * j, y1, lo);
-                store_act4(kc, base + half + 4 * j, y2, lo);
-            }
-        } else {
-            const long long t2 = t - nqk;
-            const int r = static_cast<int>(t2 % nrows);
-            const long long u = t2 / nrows;
-            const int d8 = static_cast<int>(u % D8), vh = static_cast<int>(u / D8);
-            const int col = v_off + vh * HD + 8 * d8;
-            const int np = planes ? planes[col >> 7] : 1;
-            const float *pr = part + static_cast<long long>(r) * ldp + col;
-            float4 a, b;
-            sum_planes4x2(pr, np, pr + 4, np, sstride, a, b);
-            const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            const long long lo = static_cast<long long>(nkv) * HD * seq;
-            const long long base = ((static_cast<long long>(layer) * 2 * nkv + vh) * HD + 8 * d8) * seq + P + r;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) store_act(vc, base + static_cast<long long>(e) * seq, v[e], lo);
-        }
-    }
-}
-
-cudaError_t qkv_rope_split_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows,
-                                  int nh, int nkv, int hd, int k_off, int v_off, const float2 *rope, int P,
-                                  const int *depth, __nv_bfloat16 *q, int qv_pad, __nv_bfloat16 *kc,
-                                  __nv_bfloat16 *vc, int layer, int seq, cudaStream_t s) {
-    const long long items = static_cast<long long>(nrows) * (nh + nkv) * (hd / 8) + static_cast<long long>(nkv) * (hd / 8) * nrows;
-    const int grid = static_cast<int>(std::min<long long>((items + 255) / 256, 3ll * sm_count()));
-    if (hd == 128)
-        launch_k(k_qkv_rope_split<128>, dim3(grid), dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv,
-                 k_off, v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
-    else if (hd == 64)
-        launch_k(k_qkv_rope_split<64>, dim3(grid), dim3(256), 0, s, part, planes, sstride, ldp, nrows, nh, nkv,
-                 k_off, v_off, rope, P, depth, q, qv_pad, kc, vc, layer, seq);
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ residual + norm
 // Output row i reads residual row r = row_map[i] (or i): h[r] += sum_s part[s][r];
 // xout[i] = rmsnorm(h[r]) * gain.  One CTA of 512 threads per row, PER float4

@@ -371,12 +371,12 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         const double attn_bytes =
             (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * 4.0 + 4.0 * nrows * h->qd + 4.0 * nrows * h->qd;
         if (h->bf16) {
-            pe = mode == STEP ? h->prof_begin() : -1;
-            CK(qkv_rope_split_launch(h->part, h->planes[mode][QKV], ss_qkv, h->ldo[QKV], nrows, h->nh, h->nkv, h->hd,
-                                     h->k_off, h->v_off, h->rope, P, mode == STEP ? h->depth : nullptr, h->qs,
-                                     h->qv_pad, h->kcs, h->vcs, l, h->seq, s));
-            h->prof_end(pe, 2, 0.0);
             AttnUmmaParams ap = h->attn_proto;
+            ap.part = h->part;
+            ap.planes = h->planes[mode][QKV];
+            ap.sstride = ss_qkv;
+            ap.ldp = h->ldo[QKV];
+            ap.depth = mode == STEP ? h->depth : nullptr;
             ap.layer = l;
             ap.P = P;
             ap.nrows = nrows;
@@ -385,7 +385,7 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
             pe = mode == STEP ? h->prof_begin() : -1;
             CK(attention_umma_launch(ap, h->nsm, s));
             h->prof_end(pe, 1, attn_bytes);
-            h->launches += 2;   // qkv_rope_split, attention
+            h->launches += 1;   // attention (rotary prologue included)
         } else {
         pe = mode == STEP ? h->prof_begin() : -1;
         CK(qkv_rope_launch(h->part, h->planes[mode][QKV], ss_qkv, h->ldo[QKV], nrows, h->nh, h->nkv, h->hd,
@@ -901,6 +901,13 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         ap.seq = h->seq;
         ap.out = static_cast<__nv_bfloat16 *>(h->ao);
         ap.err = &h->st->err;
+        ap.k_off = h->k_off;
+        ap.qkv_tiles = h->ldo[QKV] / kTileM;
+        ap.v_off = h->v_off;
+        ap.rope = h->rope;
+        ap.q = h->qs;
+        ap.kc = h->kcs;
+        ap.vc = h->vcs;
         if (!attention_umma_maps(ap, h->qs, h->kcs, h->vcs, h->L)) {
             delete h;
             return fail(LA_ERR_CUDA, "tensor maps for the attention failed");

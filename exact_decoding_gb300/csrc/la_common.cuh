@@ -334,6 +334,53 @@ __device__ __forceinline__ void st_shared_u32x4(uint32_t addr, uint32_t a, uint3
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// ---------------------------------------------------------------- float4 helpers
+__device__ __forceinline__ void add4(float4 &a, const float4 &b) {
+    a.x += b.x;
+    a.y += b.y;
+    a.z += b.z;
+    a.w += b.w;
+}
+// Four consecutive activations (i % 4 == 0) in store_act form.
+__device__ __forceinline__ void store_act4(float *p, long long i, float4 v, long long) {
+    *reinterpret_cast<float4 *>(p + i) = v;
+}
+__device__ __forceinline__ void store_act4(__nv_bfloat16 *p, long long i, float4 v, long long lo_off) {
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(v.x - f01.x, v.y - f01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(v.z - f23.x, v.w - f23.y);
+    uint2 hv, lv;
+    hv.x = *reinterpret_cast<const uint32_t *>(&h01);
+    hv.y = *reinterpret_cast<const uint32_t *>(&h23);
+    lv.x = *reinterpret_cast<const uint32_t *>(&l01);
+    lv.y = *reinterpret_cast<const uint32_t *>(&l23);
+    *reinterpret_cast<uint2 *>(p + i) = hv;
+    *reinterpret_cast<uint2 *>(p + i + lo_off) = lv;
+}
+// Sums of the partial planes of two runs of four consecutive columns (each
+// inside one 128-column tile with na / nb planes), added in plane order.
+// All loads of a batch of four planes per run are issued before any add.
+__device__ __forceinline__ void sum_planes4x2(const float *pa, int na, const float *pb, int nb, long long sstride,
+                                              float4 &ra, float4 &rb) {
+    ra = make_float4(0.f, 0.f, 0.f, 0.f);
+    rb = ra;
+    const int n = max(na, nb);
+    for (int b0 = 0; b0 < n; b0 += 4) {
+        float4 xa[4], xb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            xa[k] = b0 + k < na ? *reinterpret_cast<const float4 *>(pa + (b0 + k) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xb[k] = b0 + k < nb ? *reinterpret_cast<const float4 *>(pb + (b0 + k) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (b0 + k < na) add4(ra, xa[k]);
+            if (b0 + k < nb) add4(rb, xb[k]);
+        }
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -103,17 +103,6 @@ cudaError_t embed_norm_launch(const T *embed, const int *tok, int nrows, int d, 
 cudaError_t qkv_rope_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows, int nh,
                             int nkv, int hd, int k_off, int v_off, const float2 *rope, int P, const int *depth,
                             float *q, float *kc, float *vc, int max_seq, cudaStream_t s);
-// bf16 models: the same projection sums and rotation, written for the
-// tensor-core attention as bf16 (hi, lo) plane pairs (x = hi + lo):
-//   q  [2][nkv][qv_pad][hd]      query vector v = row * (nh / nkv) + j of KV
-//                                head g is q head g * (nh / nkv) + j; scaled
-//                                by 1 / sqrt(hd)
-//   kc [L][2][nkv][seq][hd]      rows P + r of layer `layer`
-//   vc [L][2][nkv][hd][seq]      V transposed: columns P + r
-cudaError_t qkv_rope_split_launch(const float *part, const int *planes, long long sstride, int ldp, int nrows,
-                                  int nh, int nkv, int hd, int k_off, int v_off, const float2 *rope, int P,
-                                  const int *depth, __nv_bfloat16 *q, int qv_pad, __nv_bfloat16 *kc,
-                                  __nv_bfloat16 *vc, int layer, int seq, cudaStream_t s);
 template <typename T>
 cudaError_t resid_norm_launch(float *h, const float *part, const int *planes, long long sstride, int ldp, int d,
                               const T *gain, float eps, const int *row_map, int nrows, T *xout, long long lo_off,
@@ -149,8 +138,8 @@ constexpr int kAttnChunk = 64;
 // fp32 models: SIMT split-KV (64-key chunks) + per-row in-step pass.
 cudaError_t attention_launch(const AttnArgs &a, cudaStream_t s);
 
-// bf16 models: tcgen05 attention over the plane layouts qkv_rope_split
-// writes.  One thread-block cluster per (KV head, tile of 128 query
+// bf16 models: tcgen05 attention that first sums, rotates and splits the
+// QKV projection of its own KV head (see the prologue fields below).  One thread-block cluster per (KV head, tile of 128 query
 // vectors); its CTAs split the keys [0, P + nrows) in 128-key chunks and
 // merge their partial softmax sums through distributed shared memory.
 struct AttnUmmaParams {
@@ -163,6 +152,21 @@ struct AttnUmmaParams {
     __nv_bfloat16 *out;         // [nrows][nh * hd] hi plane; lo plane out_lo_off later
     long long out_lo_off;
     unsigned *err;
+    // Prologue inputs: the QKV GEMM's partial planes ([plane][rows][ldp], q |
+    // k | v columns, planes[tile] planes per 128-column tile), the rotary
+    // table [pos][hd/2] of (cos, sin) and the step rows' depths (nullptr:
+    // row r sits at P + r).  Outputs, all (hi, lo) plane pairs:
+    //   q  [2][nkv][qv_pad][hd]   query vector v = row * gq + j of KV head g
+    //                             is q head g * gq + j, scaled by 1/sqrt(hd)
+    //   kc [L][2][nkv][seq][hd]   rows P + r of layer `layer`
+    //   vc [L][2][nkv][hd][seq]   V transposed: columns P + r
+    const float *part;
+    const int *planes;
+    long long sstride;
+    int ldp, k_off, v_off, qkv_tiles;   // qkv_tiles: entries of `planes`
+    const float2 *rope;
+    const int *depth;
+    __nv_bfloat16 *q, *kc, *vc;
 };
 // Fills the tensor maps; false if the driver rejects one.
 bool attention_umma_maps(AttnUmmaParams &p, const void *q, const void *kc, const void *vc, int L);
