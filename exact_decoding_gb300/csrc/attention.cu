@@ -310,8 +310,12 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     const uint32_t rank = cluster_ctarank();
     const int cs = static_cast<int>(gridDim.x);   // the cluster spans x
     const int g = static_cast<int>(blockIdx.y) / p.mtiles, qt = static_cast<int>(blockIdx.y) % p.mtiles;
-    const int c_beg = static_cast<int>(static_cast<long long>(rank) * p.nchunks / cs);
-    const int c_end = static_cast<int>(static_cast<long long>(rank + 1) * p.nchunks / cs);
+    // Prefix length: from the device step state when given (a captured step
+    // graph), else the launch parameter.  Written before this step began.
+    const int P = p.P_dev ? *p.P_dev : p.P;
+    const int nchunks = (P + p.nrows + kUKeys - 1) / kUKeys;
+    const int c_beg = static_cast<int>(static_cast<long long>(rank) * nchunks / cs);
+    const int c_end = static_cast<int>(static_cast<long long>(rank + 1) * nchunks / cs);
     // bar_ld: Q (first chunk) and K landed; bar_v: V landed; bar_s / bar_pv: MMAs done.
     const uint32_t bar_ld = smem_u32(&bars[0]), bar_s = smem_u32(&bars[1]), bar_pv = smem_u32(&bars[2]);
     const uint32_t bar_v = smem_u32(&bars[3]);
@@ -390,11 +394,11 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
                 } else {
                     r = u / Q4;
                     col0 = p.k_off + g * HD;
-                    it.dst = ((static_cast<long long>(p.layer) * 2 * p.nkv + g) * p.seq + p.P + r) * HD;
+                    it.dst = ((static_cast<long long>(p.layer) * 2 * p.nkv + g) * p.seq + P + r) * HD;
                     it.lo = static_cast<long long>(p.nkv) * p.seq * HD;
                 }
                 it.kind = isq ? 0 : 1;
-                const float2 *rr = p.rope + static_cast<long long>(p.P + sdep[r]) * half + 4 * it.j;
+                const float2 *rr = p.rope + static_cast<long long>(P + sdep[r]) * half + 4 * it.j;
                 it.c01 = *reinterpret_cast<const float4 *>(rr);
                 it.c23 = *reinterpret_cast<const float4 *>(rr + 2);
                 const int np = nplanes(col0);
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
                 sum_planes4x2(pr, np, pr + 4, np, p.sstride, it.a, it.b);
                 it.kind = 2;
                 it.lo = static_cast<long long>(p.nkv) * HD * p.seq;
-                it.dst = ((static_cast<long long>(p.layer) * 2 * p.nkv + g) * HD + 8 * d8) * p.seq + p.P + r;
+                it.dst = ((static_cast<long long>(p.layer) * 2 * p.nkv + g) * HD + 8 * d8) * p.seq + P + r;
             }
         };
         auto store = [&](const Item &it) {
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     // Visibility of keys [k0, k0 + 32) for this query vector, bit j = key k0 + j.
     auto vis_word = [&](int k0) -> uint32_t {
         if (!valid) return 0u;
-        const int s0 = k0 - p.P;   // step index of bit 0 (negative: cached prefix)
+        const int s0 = k0 - P;   // step index of bit 0 (negative: cached prefix)
         uint32_t pre = 0u;
         if (s0 <= -32) return 0xffffffffu;
         if (s0 < 0) pre = (1u << (-s0)) - 1u;
@@ -786,12 +790,12 @@ bool attention_umma_maps(AttnUmmaParams &p, const void *q, const void *kc, const
     return true;
 }
 
-cudaError_t attention_umma_launch(AttnUmmaParams p, int nsm, cudaStream_t s) {
-    p.nchunks = (p.P + p.nrows + kUKeys - 1) / kUKeys;
+cudaError_t attention_umma_launch(AttnUmmaParams p, int nsm, int P_max, cudaStream_t s) {
+    const int nchunks = (std::max(P_max, p.P) + p.nrows + kUKeys - 1) / kUKeys;
     p.mtiles = (p.nrows * p.gq + kUQ - 1) / kUQ;
     const int units = p.nkv * p.mtiles;
     // One chunk per CTA where the SMs allow it (clusters of up to 8 CTAs).
-    int cs = std::min(std::min(8, p.nchunks), std::max(1, nsm / units));
+    int cs = std::min(std::min(8, nchunks), std::max(1, nsm / units));
     if (p.hd == 128) return attention_umma_hd<128>(p, cs, s);
     if (p.hd == 64) return attention_umma_hd<64>(p, cs, s);
     return cudaErrorInvalidValue;

@@ -120,6 +120,12 @@ struct la_handle {
     int64_t prof_launches[4] = {0, 0, 0, 0};
     int64_t launches = 0;
 
+    // Captured step (non-profiled steps after the first): every launch of
+    // la_step plus the state read-back, replayed with one cudaGraphLaunch.
+    cudaGraphExec_t step_graph = nullptr;
+    bool graph_off = false;      // capture failed once: launch directly
+    int64_t graph_launches = 0;  // kernels per replay
+
     // host-side bookkeeping
     bool prefilled = false;
     int P = 0;
@@ -127,6 +133,7 @@ struct la_handle {
     int last_A = 0, last_g = 0, logits_rows = 0;
 
     ~la_handle() {
+        if (step_graph) cudaGraphExecDestroy(step_graph);
         for (cudaEvent_t e : ev) cudaEventDestroy(e);
         for (void *p : allocs) cudaFree(p);
         if (st_host) cudaFreeHost(st_host);
@@ -377,13 +384,14 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
             ap.sstride = ss_qkv;
             ap.ldp = h->ldo[QKV];
             ap.depth = mode == STEP ? h->depth : nullptr;
+            ap.P_dev = mode == STEP ? &h->st->P : nullptr;   // steps may replay from a captured graph
             ap.layer = l;
             ap.P = P;
             ap.nrows = nrows;
             ap.vis_bits = mode == STEP ? h->vis_bits : nullptr;
             ap.out_lo_off = bh * h->qd;
             pe = mode == STEP ? h->prof_begin() : -1;
-            CK(attention_umma_launch(ap, h->nsm, s));
+            CK(attention_umma_launch(ap, h->nsm, mode == STEP ? h->max_seq : P, s));
             h->prof_end(pe, 1, attn_bytes);
             h->launches += 1;   // attention (rotary prologue included)
         } else {
@@ -997,11 +1005,12 @@ struct NvtxRange {
 };
 }  // namespace
 
-int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
-    NvtxRange range("la_step");
-    if (!h || !out_tokens || !out_n) return fail(LA_ERR_INVALID_ARG, "null argument");
-    if (!h->prefilled) return fail(LA_ERR_STATE, "la_step before la_prefill");
-    if (h->P + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "max_seq reached");
+}  // extern "C"
+
+namespace {
+
+// Every launch of one step, then the read-back of the step state.
+int enqueue_step(la_handle *h) {
     cudaStream_t s = h->stream;
     int pe = h->prof_begin();
     CK(build_rows_launch(h->spec(), s));
@@ -1018,6 +1027,54 @@ int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     h->prof_end(pe, 3, 0.0);
     h->launches += 4;   // build_rows, argmax, finish_step, kv_commit
     CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
+    return LA_OK;
+}
+
+// Capture enqueue_step into h->step_graph.  Every kernel argument of a step
+// is fixed except the prefix length, which the attention reads from the
+// device step state, so the graph replays for every later step.  On any
+// failure the handle falls back to direct launches for good.
+void capture_step(la_handle *h) {
+    cudaStream_t s = h->stream;
+    if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        h->graph_off = true;
+        return;
+    }
+    const int64_t l0 = h->launches;
+    const int rc = enqueue_step(h);
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(s, &g);
+    h->graph_launches = h->launches - l0;
+    h->launches = l0;
+    if (rc != LA_OK || e != cudaSuccess || !g || cudaGraphInstantiate(&h->step_graph, g, 0) != cudaSuccess) {
+        cudaGetLastError();
+        h->step_graph = nullptr;
+        h->graph_off = true;
+    }
+    if (g) cudaGraphDestroy(g);
+}
+
+}  // namespace
+
+extern "C" {
+
+int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
+    NvtxRange range("la_step");
+    if (!h || !out_tokens || !out_n) return fail(LA_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled) return fail(LA_ERR_STATE, "la_step before la_prefill");
+    if (h->P + h->M + h->N + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "max_seq reached");
+    cudaStream_t s = h->stream;
+    int rc;
+    // The first step of a handle runs directly (one-time kernel attributes are
+    // set outside any capture); later non-profiled steps replay a graph.
+    if (h->bf16 && !h->prof_on && !h->graph_off && h->steps > 0 && !h->step_graph) capture_step(h);
+    if (h->step_graph) {
+        CK(cudaGraphLaunch(h->step_graph, s));
+        h->launches += h->graph_launches;
+    } else if ((rc = enqueue_step(h)) != LA_OK) {
+        return rc;
+    }
     CK(cudaStreamSynchronize(s));
     if ((rc = check_device_error(h)) != LA_OK) return rc;
     h->prof_collect();

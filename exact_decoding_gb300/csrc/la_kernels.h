@@ -147,7 +147,8 @@ struct AttnUmmaParams {
     CUtensorMap tk;        // K cache as [L * 2 * nkv * seq][hd], box 64 x 128
     CUtensorMap tv;        // V^T cache as [L * 2 * nkv * hd][seq], box 64 x hd
     int layer, nh, nkv, gq, hd, qv_pad, seq;
-    int P, nrows, nchunks, mtiles;
+    int P, nrows, mtiles;
+    const int *P_dev;           // if set, P is read from here (device step state) instead
     const uint32_t *vis_bits;   // [nrows][8] in-step visibility bits, or nullptr (causal)
     __nv_bfloat16 *out;         // [nrows][nh * hd] hi plane; lo plane out_lo_off later
     long long out_lo_off;
@@ -170,9 +171,11 @@ struct AttnUmmaParams {
 };
 // Fills the tensor maps; false if the driver rejects one.
 bool attention_umma_maps(AttnUmmaParams &p, const void *q, const void *kc, const void *vc, int L);
-// Launch for the current P / nrows (fields P, nrows, layer, vis_bits set by
-// the caller); picks the cluster size from the SM count.
-cudaError_t attention_umma_launch(AttnUmmaParams p, int nsm, cudaStream_t s);
+// Launch for nrows rows (fields P or P_dev, nrows, layer, vis_bits set by
+// the caller).  The cluster size is picked from the SM count and the largest
+// prefix the launch may see (P_max), so one launch configuration serves
+// every step of a captured graph.
+cudaError_t attention_umma_launch(AttnUmmaParams p, int nsm, int P_max, cudaStream_t s);
 
 // ------------------------------------------------------------------ speculation state
 struct SpecState {
