@@ -347,6 +347,34 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     const bool valid = qv < QV;
     const int r = valid ? qv / p.gq : 0;
 
+    const long long krows_plane = static_cast<long long>(p.nkv) * p.seq;   // K rows from hi to lo plane
+    const int vrows_plane = p.nkv * HD;
+    const int ky0 = (p.layer * 2 * p.nkv + g) * p.seq;
+    const int vy0 = (p.layer * 2 * p.nkv + g) * HD;
+    // K of chunk c completes on bar_ld, V on bar_v (S can start while V lands).
+    auto issue_kv = [&](int c, uint64_t pol) {
+        const int key0 = c * kUKeys;
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int db = 0; db < HD / 64; ++db)
+                tma_load_2d(s_kp + (pl * (HD / 64) + db) * kUBox, &p.tk, db * 64,
+                            static_cast<int>(ky0 + pl * krows_plane + key0), bar_ld, pol);
+        mbar_arrive_expect_tx(bar_v, Lay::v_bytes);
+#pragma unroll
+        for (int pl = 0; pl < 2; ++pl)
+#pragma unroll
+            for (int kb = 0; kb < kUKeys / 64; ++kb)
+                tma_load_2d(s_v + (pl * (kUKeys / 64) + kb) * Lay::vbox, &p.tv, key0 + kb * 64, vy0 + pl * vrows_plane,
+                            bar_v, pol);
+    };
+    // Cached-prefix chunk first in line: its K/V were written before this
+    // launch began, so they load while the prologue runs.
+    const bool early = p.prefix_early && c_beg < c_end && (c_beg + 1) * kUKeys <= P;
+    if (tid == 0 && early) {
+        mbar_expect_tx(bar_ld, Lay::k_bytes);
+        issue_kv(c_beg, policy_evict_normal());
+    }
     // Tables written once at create time (safe to read before the wait):
     // the step rows' depths and the QKV tiles' partial-plane counts.
     int *sdep = reinterpret_cast<int *>(smem + Lay::tab_off);
@@ -482,38 +510,17 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
         return pre | (st & live & ~pre);
     };
 
-    const long long krows_plane = static_cast<long long>(p.nkv) * p.seq;   // K rows from hi to lo plane
-    const int vrows_plane = p.nkv * HD;
-    const int ky0 = (p.layer * 2 * p.nkv + g) * p.seq;
-    const int vy0 = (p.layer * 2 * p.nkv + g) * HD;
-    // K of chunk c completes on bar_ld, V on bar_v (S can start while V lands).
-    auto issue_kv = [&](int c, uint64_t pol) {
-        const int key0 = c * kUKeys;
-#pragma unroll
-        for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-            for (int db = 0; db < HD / 64; ++db)
-                tma_load_2d(s_kp + (pl * (HD / 64) + db) * kUBox, &p.tk, db * 64,
-                            static_cast<int>(ky0 + pl * krows_plane + key0), bar_ld, pol);
-        mbar_arrive_expect_tx(bar_v, Lay::v_bytes);
-#pragma unroll
-        for (int pl = 0; pl < 2; ++pl)
-#pragma unroll
-            for (int kb = 0; kb < kUKeys / 64; ++kb)
-                tma_load_2d(s_v + (pl * (kUKeys / 64) + kb) * Lay::vbox, &p.tv, key0 + kb * 64, vy0 + pl * vrows_plane,
-                            bar_v, pol);
-    };
     if (tid == 0 && c_beg < c_end) {
         asm volatile("fence.proxy.async.global;" ::: "memory");
         const uint64_t pol = policy_evict_normal();   // other query tiles of this KV head read the same chunks
-        mbar_arrive_expect_tx(bar_ld, Lay::q_bytes + Lay::k_bytes);
+        mbar_arrive_expect_tx(bar_ld, early ? Lay::q_bytes : Lay::q_bytes + Lay::k_bytes);
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
 #pragma unroll
             for (int db = 0; db < HD / 64; ++db)
                 tma_load_2d(s_q + (pl * (HD / 64) + db) * kUBox, &p.tq, db * 64, (pl * p.nkv + g) * p.qv_pad + qt * kUQ,
                             bar_ld, pol);
-        issue_kv(c_beg, pol);
+        if (!early) issue_kv(c_beg, pol);
     }
 
     const uint32_t idesc_s = umma_idesc_bf16(kUQ, kUKeys), idesc_o = umma_idesc_bf16(kUQ, HD);

@@ -385,6 +385,7 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
             ap.ldp = h->ldo[QKV];
             ap.depth = mode == STEP ? h->depth : nullptr;
             ap.P_dev = mode == STEP ? &h->st->P : nullptr;   // steps may replay from a captured graph
+            ap.prefix_early = mode == STEP ? 1 : 0;
             ap.layer = l;
             ap.P = P;
             ap.nrows = nrows;

@@ -149,6 +149,8 @@ struct AttnUmmaParams {
     int layer, nh, nkv, gq, hd, qv_pad, seq;
     int P, nrows, mtiles;
     const int *P_dev;           // if set, P is read from here (device step state) instead
+    int prefix_early;           // cache slots < P were written before this launch began (a step,
+                                // not a prefill chunk): their K/V loads may start before the wait
     const uint32_t *vis_bits;   // [nrows][8] in-step visibility bits, or nullptr (causal)
     __nv_bfloat16 *out;         // [nrows][nh * hd] hi plane; lo plane out_lo_off later
     long long out_lo_off;
