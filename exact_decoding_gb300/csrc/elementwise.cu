@@ -318,7 +318,9 @@ __global__ void __launch_bounds__(1024) k_argmax(const float *part, const int *p
     __syncthreads();
     best = sv[0];
     if (threadIdx.x == 0) {
-        amax[r] = si[0];
+        // All-NaN logits leave no index: report token 0 rather than an id
+        // outside the vocabulary (the step's tokens index the embedding).
+        amax[r] = si[0] < V ? si[0] : 0;
         lmax[r] = best;
     }
     if (invT > 0.f) {
