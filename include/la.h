@@ -47,8 +47,9 @@ extern "C" {
 
 /* Weight / activation element types. */
 #define LA_F32   0   /* fp32 weights, fp32 activations and KV cache (SIMT GEMMs) */
-#define LA_BF16  1   /* bf16 weights, bf16 GEMM inputs and KV cache, fp32 accumulation
-                        and fp32 residual stream (tcgen05 tensor-core GEMMs) */
+#define LA_BF16  1   /* bf16 weights; GEMM inputs, KV cache, q and attention probabilities
+                        as (hi, lo) bf16 pairs (about 16 mantissa bits), fp32 accumulation
+                        and fp32 residual stream (tcgen05 tensor-core GEMMs and attention) */
 
 /* Model shape of a LLaMA-style decoder (the pages run LLaMA-2 / CodeLlama,
  * paper-graph-ui page, section 5 "Experimental setup"). */
@@ -145,8 +146,9 @@ typedef struct la_state_t {
                                keys ascending, each key's suffixes oldest first */
 } la_state_t;
 
-/* Create a decoder for the given weights.  Allocates the KV cache
- * ([n_layers][2][n_kv_heads][max_seq][head_dim]), activations, the n-gram pool
+/* Create a decoder for the given weights.  Allocates the KV cache (fp32
+ * [n_layers][K, V][n_kv_heads][max_seq][head_dim]; bf16 models: K and V as
+ * (hi, lo) bf16 plane pairs, V transposed), activations, the n-gram pool
  * and the window on the current device; no weight is copied.
  * Errors: INVALID_ARG (shapes, alignment, options), UNSUPPORTED, OOM, CUDA. */
 int la_create(const la_model_dims *dims, const la_weights *weights, const la_opts *opts,
@@ -161,6 +163,11 @@ int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_to
 
 /* One lookahead step.  Writes the A accepted tokens (1 <= A <= N) to host
  * out_tokens (capacity >= N) and A to *out_n.  Synchronous.
+ * bf16 models without la_opts.profile: the first step of a handle launches
+ * its kernels directly and captures them, with the state read-back, into a
+ * CUDA graph on the handle's stream; later steps replay that graph (one
+ * launch per step; results equal to direct launches bit for bit).  If the
+ * capture fails the handle keeps launching directly.
  * Errors: STATE (no prefill), CAPACITY (max_seq reached), CUDA, DEVICE_TIMEOUT. */
 int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n);
 
