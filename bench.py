@@ -308,6 +308,23 @@ def run_ours(args, wl, rank, world, local_rank):
     log(f"timed: {args.steps} steps, {total_ms / args.steps:.3f} ms/step, {accepted} tokens")
     launches += dec.stats()["kernel_launches"] - launches0
 
+    # ---- autoregressive baseline on this GPU: la_ar_step, same model and prompt
+    ar_ms = None
+    if not args.ncu:
+        fresh()
+        for _ in range(3):
+            dec.ar_step()
+        n_ar = 64
+        ev_ar = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ar)]
+        sync()
+        for i in range(n_ar):
+            ev_ar[i][0].record(stream)
+            dec.ar_step()
+            ev_ar[i][1].record(stream)
+        sync()
+        ar_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_ar)
+        log(f"autoregressive baseline: {ar_ms:.3f} ms/token")
+
     # ---- profiled pass (events around every GEMM / attention launch)
     pdec = e.Decoder(dw, wl.N, wl.W, wl.G, max_seq, stream=stream, profile=True, **kw)
     if not args.ncu:
@@ -367,6 +384,12 @@ def run_ours(args, wl, rank, world, local_rank):
         "attention": {"achieved": attn_gbs, "unit": "GB/s",
                       "ms_per_step": pst["attn_ms"] / max(pst["steps"], 1)},
         "breakdown_ms_per_step": {k: pst[k + "_ms"] / max(pst["steps"], 1) for k in ("gemm", "attn", "elem", "spec")},
+        "ar_baseline": None if ar_ms is None else {
+            "ms_per_token": ar_ms, "tokens_per_s": 1e3 / ar_ms,
+            "lookahead_over_ar": (accepted_all / (max_ms * 1e-3)) / (1e3 / ar_ms),
+            "note": "la_ar_step (one row per forward, same kernels and weights) timed on this GPU; random weights "
+                    "accept A = 1 token per lookahead step, so the ratio is the step cost ratio, not the pages' "
+                    "speedup on trained models"},
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and not args.ncu and world == 1:

@@ -1095,6 +1095,30 @@ int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     return LA_OK;
 }
 
+int la_ar_step(la_handle *h, int32_t *token) {
+    NvtxRange range("la_ar_step");
+    if (!h || !token) return fail(LA_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled) return fail(LA_ERR_STATE, "la_ar_step before la_prefill");
+    if (h->P + 2 > h->max_seq) return fail(LA_ERR_CAPACITY, "max_seq reached");
+    cudaStream_t s = h->stream;
+    const int P = h->P;   // tokens_log[P] is the last committed token, at position P
+    int rc = forward_any(h, PREFILL, h->tokens_log + P, 1, P, true);
+    if (rc != LA_OK) return rc;
+    if ((rc = run_lm_head(h, 1, false)) != LA_OK) return rc;
+    CK(argmax_launch(h->lm_part, h->planes_lm, h->lm_stride, h->ldo_lm, h->logits, 1, h->V,
+                     h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax, h->lmax, h->lsum, s));
+    CK(first_token_launch(h->spec(), P + 1, s));
+    h->launches += 2;
+    CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+    if ((rc = check_device_error(h)) != LA_OK) return rc;
+    *token = h->st_host->o;
+    h->P = P + 1;
+    h->generated += 1;
+    h->logits_rows = 1;
+    return LA_OK;
+}
+
 int la_generate(la_handle *h, const int32_t *prompt, int32_t n, int32_t max_new, int32_t *out, int32_t *out_n,
                 int32_t *n_steps) {
     if (!h || !prompt || !out || max_new < 1) return fail(LA_ERR_INVALID_ARG, "bad argument");

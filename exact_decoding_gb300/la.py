@@ -79,6 +79,7 @@ def load_library():
                               ctypes.POINTER(H)]
     lib.la_prefill.argtypes = [H, _I32P, ctypes.c_int32, _I32P]
     lib.la_step.argtypes = [H, _I32P, _I32P]
+    lib.la_ar_step.argtypes = [H, _I32P]
     lib.la_generate.argtypes = [H, _I32P, ctypes.c_int32, ctypes.c_int32, _I32P, _I32P, _I32P]
     lib.la_stats.argtypes = [H, ctypes.POINTER(la_stats_t)]
     lib.la_export_state.argtypes = [H, ctypes.POINTER(la_state_t)]
@@ -94,7 +95,7 @@ def load_library():
     lib.la_strerror.restype = ctypes.c_char_p
     lib.la_last_error.argtypes = []
     lib.la_last_error.restype = ctypes.c_char_p
-    for name in ("la_create", "la_prefill", "la_step", "la_generate", "la_stats", "la_export_state",
+    for name in ("la_create", "la_prefill", "la_step", "la_ar_step", "la_generate", "la_stats", "la_export_state",
                  "la_import_state", "la_debug_logits", "la_gemm_bf16", "la_gemm_bf16_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -135,6 +136,12 @@ def la_step(h, N: int) -> List[int]:
     n = np.zeros(1, dtype=np.int32)
     _check(load_library().la_step(h, _i32(out), _i32(n)), "la_step")
     return out[: int(n[0])].tolist()
+
+
+def la_ar_step(h) -> int:
+    tok = np.zeros(1, dtype=np.int32)
+    _check(load_library().la_ar_step(h, _i32(tok)), "la_ar_step")
+    return int(tok[0])
 
 
 def la_generate(h, prompt, max_new: int) -> Tuple[List[int], int]:
@@ -263,6 +270,9 @@ class Decoder:
 
     def step(self) -> List[int]:
         return la_step(self.h, self.N)
+
+    def ar_step(self) -> int:
+        return la_ar_step(self.h)
 
     def generate(self, prompt, max_new: int):
         return la_generate(self.h, prompt, max_new)

@@ -171,6 +171,16 @@ int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_to
  * Errors: STATE (no prefill), CAPACITY (max_seq reached), CUDA, DEVICE_TIMEOUT. */
 int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n);
 
+/* One plain autoregressive decoding step (the baseline lookahead decoding is
+ * measured against; paper-graph-ui page, section 3.4 "The autoregressive
+ * system"): one forward row for the last committed token, which commits its
+ * KV, then argmax (or a draw at temperature > 0, keyed like the first token)
+ * over the vocabulary.  Writes the new token to *token (host).  Uses the same
+ * kernels as la_prefill; leaves the window and the pool untouched, so it can
+ * be interleaved with la_step on one handle.
+ * Errors: STATE (no prefill), CAPACITY (max_seq reached), CUDA, DEVICE_TIMEOUT. */
+int la_ar_step(la_handle *h, int32_t *token);
+
 /* Prefill, then steps until max_new tokens are produced (the prefill's first
  * token counts; the last step is truncated).  Host out[max_new]; *out_n =
  * tokens written; *n_steps = la_step calls.  Any of out_n / n_steps may be NULL. */

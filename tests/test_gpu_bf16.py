@@ -112,3 +112,24 @@ def test_graph_replay_matches_direct_launches(lib):
     assert outs[0][0] == outs[1][0]
     for a, b in zip(outs[0][1], outs[1][1]):
         assert np.array_equal(a, b)
+
+
+def test_ar_step_bf16_matches_oracle(lib):
+    """la_ar_step on a bf16 decoder: each step's logits within 2e-2 of the
+    oracle's last-row logits, tokens equal where the margin exceeds 0.05."""
+    from oracle import decoder
+    dims = SMALL["gqa-hd128"]
+    w = synth.model_weights(dims, 13)
+    p = [int(t) for t in synth.uniform_tokens(40, dims.vocab, 13, 7)]
+    dec = lib.Decoder(w, 4, 5, 4, 256)
+    toks = list(p) + [dec.prefill(p)]
+    for _ in range(6):
+        y = dec.ar_step()
+        ref, _ = decoder.forward(w, toks, np.arange(len(toks)), decoder.causal_mask(0, len(toks)),
+                                 logit_rows=[len(toks) - 1])
+        err = float(np.max(np.abs(dec.debug_logits()[0] - ref[0])))
+        assert err <= LOGIT_TOL_BF16, f"logits max-abs {err}"
+        if top2_margin(ref[0]) > MARGIN:
+            assert y == la.argmax_lowest(ref[0])
+        toks.append(y)
+    dec.close()

@@ -183,3 +183,23 @@ def test_error_paths(lib, tiny_model):
             dec.step()
     assert e.value.code == -3            # max_seq reached, reported before any launch
     dec.close()
+
+
+def test_ar_step_equals_oracle_autoregressive(lib, tiny_model):
+    """la_ar_step (the plain autoregressive baseline) reproduces the oracle's
+    greedy AR stream, and interleaving it with lookahead steps keeps the
+    stream on the same greedy trajectory."""
+    wl, w, p = tiny_model
+    ar, margins = ar_with_margins(w, p, 40)
+    dec = make(lib, w, 3, 4, 4)
+    out = [dec.prefill(p)]
+    for _ in range(20):
+        out.append(dec.ar_step())
+    while len(out) < 40:
+        out.extend(dec.step())
+    for _ in range(3):
+        out.append(dec.ar_step())
+    out = out[:40]
+    upto = compare_stream(out, ar, margins, MARGIN)
+    assert upto >= 16, f"first low-margin decision at {upto}"
+    dec.close()
