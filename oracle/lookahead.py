@@ -48,6 +48,13 @@ Readings taken where the pages are open:
      none is accepted, or after N-1 accepted tokens, one token is drawn from
      dist by inverse CDF (smallest id whose ascending cumulative mass exceeds
      u * total).  Draw index counts draws at the same position.
+  R14 Top-k / top-p (the pages name them for sampling without an order or a
+     tie rule): temperature first, then top-k, then top-p on the renormalised
+     top-k distribution.  Tokens are ranked by probability, ties to the lower
+     id; top-k keeps the first k; top-p keeps the shortest ranked prefix whose
+     mass reaches p (the token that crosses p included).  Algorithm 4 then
+     runs on the filtered distributions unchanged, so its output follows the
+     filtered distribution exactly.
 """
 from __future__ import annotations
 
@@ -321,6 +328,25 @@ def softmax(logits: np.ndarray, T: float) -> np.ndarray:
     return e / e.sum()
 
 
+def filter_top(dist: np.ndarray, top_k: int = 0, top_p: float = 1.0) -> np.ndarray:
+    """Reading R14: zero every token outside the top-k, then outside the
+    top-p prefix of what is left; ranking by probability, ties to the lower
+    id.  top_k <= 0 or >= V and top_p >= 1 leave the distribution whole."""
+    p = np.array(dist, dtype=np.float64)
+    order = sorted(range(len(p)), key=lambda v: (-p[v], v))
+    keep = list(order)
+    if 0 < top_k < len(p):
+        keep = keep[:top_k]
+    if top_p < 1.0:
+        mass = np.array([p[v] for v in keep])
+        cum = np.cumsum(mass) / mass.sum()
+        n = int(np.searchsorted(cum, top_p, side="left")) + 1   # first prefix with cum >= top_p
+        keep = keep[:min(n, len(keep))]
+    out = np.zeros_like(p)
+    out[keep] = p[keep]
+    return out
+
+
 # --------------------------------------------------------------------------
 # Generation (autoregressive reference and lookahead)
 # --------------------------------------------------------------------------
@@ -359,10 +385,11 @@ class Lookahead:
 
     def __init__(self, weights, N: int, W: int, G: int, temperature: float = 0.0, seed: int = 0,
                  prompt_as_reference: bool = False, pool_cap: int = 0, dtype=np.float64,
-                 keep_logits: bool = False):
+                 keep_logits: bool = False, top_k: int = 0, top_p: float = 1.0):
         assert N >= 2 and W >= 1 and G >= 0
         self.w, self.N, self.W, self.G = weights, N, W, G
         self.T, self.seed = temperature, seed
+        self.top_k, self.top_p = top_k, top_p
         self.par = prompt_as_reference
         self.dtype = dtype
         self.keep_logits = keep_logits
@@ -375,6 +402,10 @@ class Lookahead:
         self.window = None
         self.history: List[StepRecord] = []
 
+    def dist(self, logits: np.ndarray) -> np.ndarray:
+        """A row's sampling distribution: softmax at T, then top-k / top-p (R14)."""
+        return filter_top(softmax(logits, self.T), self.top_k, self.top_p)
+
     # state ------------------------------------------------------------
     @property
     def P(self) -> int:
@@ -386,7 +417,7 @@ class Lookahead:
         logits, self.cache = decoder.forward(self.w, prompt, np.arange(s), decoder.causal_mask(0, s),
                                              dtype=self.dtype, logit_rows=[s - 1])
         if self.T > 0:
-            y1 = inverse_cdf(softmax(logits[0], self.T), philox.uniform(self.seed, s, 0))
+            y1 = inverse_cdf(self.dist(logits[0]), philox.uniform(self.seed, s, 0))
         else:
             y1 = argmax_lowest(logits[0])
         self.tokens = prompt + [y1]
@@ -436,8 +467,8 @@ class Lookahead:
         if self.T > 0:
             trace = []
             acc, winner = sampling_verify(
-                cands, softmax(lrow[0], self.T),
-                lambda c, m: softmax(lrow[cand_row(N, W, c, m)], self.T),
+                cands, self.dist(lrow[0]),
+                lambda c, m: self.dist(lrow[cand_row(N, W, c, m)]),
                 P, self.seed, N, trace)
         else:
             acc, winner = greedy_verify(cands, argmax_lowest(lrow[0]),

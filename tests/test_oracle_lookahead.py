@@ -259,3 +259,46 @@ def test_sampling_progress_bounds(tiny):
     assert len(out) == 32
     for rec in o.history:
         assert 1 <= len(rec.accepted) <= 3
+
+
+# ---------------------------------------------------------------- top-k / top-p (reading R14)
+def test_filter_top_hand_examples():
+    """Hand-worked cases on binary fractions: ranking by probability with ties
+    to the lower id, top-k keeps the first k, top-p keeps the prefix whose
+    mass first reaches p (crossing token included), top-p acts on the
+    renormalised top-k set."""
+    d = np.array([0.125, 0.375, 0.25, 0.125, 0.125])   # ranked ids: 1, 2, 0, 3, 4
+    keep = lambda out: [v for v in range(len(out)) if out[v] > 0]
+    assert keep(la.filter_top(d, 1)) == [1]
+    assert keep(la.filter_top(d, 3)) == [0, 1, 2]                 # tie 0/3/4 at 0.125: id 0
+    assert keep(la.filter_top(d, 4)) == [0, 1, 2, 3]
+    assert keep(la.filter_top(d, 0, 0.375)) == [1]                # reaches p exactly
+    assert keep(la.filter_top(d, 0, 0.376)) == [1, 2]             # crossing token kept
+    assert keep(la.filter_top(d, 0, 0.75)) == [0, 1, 2]
+    assert keep(la.filter_top(d, 0, 0.76)) == [0, 1, 2, 3]
+    assert keep(la.filter_top(d, 2, 0.61)) == [1, 2]              # renormalised top-2: 0.6, 0.4
+    assert keep(la.filter_top(d, 2, 0.59)) == [1]
+    assert np.array_equal(la.filter_top(d, 0, 1.0), d)
+    assert np.array_equal(la.filter_top(d, 5, 1.0), d)
+
+
+@pytest.mark.parametrize("top_k,top_p,tokens", [(3, 1.0, [4, 7, 2]), (0, 0.5, [7, 6, 0]), (5, 0.8, [1, 7, 6, 5])])
+def test_sampling_rule_preserves_filtered_distribution_exactly(top_k, top_p, tokens):
+    """With top-k / top-p the rejection chain runs on the filtered
+    distribution, so the output follows that distribution exactly."""
+    p = [Fraction(k, 36) for k in (1, 2, 3, 4, 5, 6, 7, 8)]
+    f = la.filter_top(np.array([float(x) for x in p]), top_k, top_p)
+    pf = [p[v] if f[v] > 0 else Fraction(0) for v in range(8)]
+    tot = sum(pf)
+    got = _exact_rejection_chain(pf, tokens)
+    assert all(got[x] == pf[x] / tot for x in range(8))
+
+
+def test_top_k1_sampling_equals_greedy(tiny):
+    """top_k = 1 leaves one token per row: lookahead sampling at T = 1 must
+    reproduce greedy autoregressive decoding token for token."""
+    wl, w, p = tiny
+    ref = la.generate_ar(w, p, 20)
+    o = la.Lookahead(w, 3, 4, 4, temperature=1.0, seed=5, top_k=1)
+    out, _ = o.generate(p, 20)
+    assert out == ref
