@@ -4,6 +4,7 @@
 //   SwiGLU, and the vocabulary argmax (with softmax statistics for sampling).
 // The residual stream h stays fp32; T is the GEMM-input / KV-cache type.
 #include <algorithm>
+#include <climits>
 
 #include "la_kernels.h"
 
@@ -260,11 +261,165 @@ cudaError_t swiglu_launch(const float *part, const int *planes, long long sstrid
 }
 
 // ------------------------------------------------------------------ argmax / softmax stats
+// Exclusive prefix over the block's threads in thread order (fixed order, so
+// the float version is deterministic); total in *tot.
+template <typename X>
+__device__ __forceinline__ X block_excl_scan(X v, X *wtot, X *tot) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    X incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const X y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wtot[w] = incl;
+    __syncthreads();
+    if (w == 0) {
+        X x = lane < 32 ? wtot[lane] : X(0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const X y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        wtot[lane] = x;
+    }
+    __syncthreads();
+    const X excl = (w > 0 ? wtot[w - 1] : X(0)) + incl - v;
+    *tot = wtot[31];
+    __syncthreads();
+    return excl;
+}
+
+// Keep rule of one row's sampling distribution (top-k, then top-p on what
+// top-k keeps; ranking by logit, ties to the lower id).  Thread t owns the
+// contiguous ids [a, b).  top-k: 4-pass radix select of the k-th largest
+// key with integer histograms, then the lowest ids among the tied keys;
+// top-p: 32-step bisection on the key with fixed-order mass sums, then the
+// tied keys in id order until the mass is reached.  Returns the kept mass.
+__device__ float row_keep_rule(const float *l, int V, float mx, float invT, int top_k, float top_p, unsigned *thr_out,
+                               int *cut_out) {
+    __shared__ unsigned s_hist[256];
+    __shared__ unsigned s_pref, s_rem;
+    __shared__ int s_cut;
+    __shared__ int s_wi[32];
+    __shared__ float s_wf[32];
+    const int tid = threadIdx.x;
+    const int per = (V + 1023) / 1024, a = min(V, tid * per), b = min(V, a + per);
+    unsigned thr = 0u;
+    int cut = INT_MAX;
+    if (top_k > 0 && top_k < V) {
+        unsigned pref = 0u, pmask = 0u, rem = static_cast<unsigned>(top_k);
+        for (int sh = 24; sh >= 0; sh -= 8) {
+            for (int i = tid; i < 256; i += 1024) s_hist[i] = 0u;
+            __syncthreads();
+            for (int v = a; v < b; ++v) {
+                const unsigned k = order_key(l[v]);
+                if ((k & pmask) == pref) atomicAdd(&s_hist[(k >> sh) & 255u], 1u);
+            }
+            __syncthreads();
+            if (tid == 0) {
+                unsigned acc = 0u;
+                for (int dd = 255; dd >= 0; --dd) {
+                    if (acc + s_hist[dd] >= rem) {
+                        s_pref = pref | (static_cast<unsigned>(dd) << sh);
+                        s_rem = rem - acc;
+                        break;
+                    }
+                    acc += s_hist[dd];
+                }
+            }
+            __syncthreads();
+            pref = s_pref;
+            rem = s_rem;
+            pmask |= 0xFFu << sh;
+        }
+        // the rem lowest ids among keys equal to pref
+        int cnt = 0;
+        for (int v = a; v < b; ++v) cnt += order_key(l[v]) == pref;
+        int tot;
+        const int excl = block_excl_scan<int>(cnt, s_wi, &tot);
+        if (tid == 0) s_cut = INT_MAX;
+        __syncthreads();
+        if (cnt > 0 && excl < static_cast<int>(rem) && static_cast<int>(rem) <= excl + cnt) {
+            int c = excl;
+            for (int v = a; v < b; ++v)
+                if (order_key(l[v]) == pref && ++c == static_cast<int>(rem)) {
+                    s_cut = v;
+                    break;
+                }
+        }
+        __syncthreads();
+        thr = pref;
+        cut = s_cut;
+    }
+    if (top_p > 0.f && top_p < 1.f) {
+        const unsigned thrk = thr;
+        const int cutk = cut;
+        float z = 0.f;
+        for (int v = a; v < b; ++v)
+            if (keep_token(l[v], v, thrk, cutk)) z += expf((l[v] - mx) * invT);
+        float zk;
+        block_excl_scan<float>(z, s_wf, &zk);
+        const float target = top_p * zk;
+        unsigned long long lo = 0ull, hi = 1ull << 32;   // largest key K with mass(key >= K) >= target
+        for (int it = 0; it < 32; ++it) {
+            const unsigned long long mid = (lo + hi) >> 1;
+            float sm = 0.f;
+            for (int v = a; v < b; ++v)
+                if (keep_token(l[v], v, thrk, cutk) && order_key(l[v]) >= mid) sm += expf((l[v] - mx) * invT);
+            float S;
+            block_excl_scan<float>(sm, s_wf, &S);
+            if (S >= target) lo = mid;
+            else hi = mid;
+        }
+        const unsigned kp = static_cast<unsigned>(lo);
+        float gt = 0.f, tie = 0.f;
+        for (int v = a; v < b; ++v) {
+            if (!keep_token(l[v], v, thrk, cutk)) continue;
+            const unsigned k = order_key(l[v]);
+            if (k > kp) gt += expf((l[v] - mx) * invT);
+            else if (k == kp) tie += expf((l[v] - mx) * invT);
+        }
+        float Sgt, Stie;
+        block_excl_scan<float>(gt, s_wf, &Sgt);
+        const float excl = block_excl_scan<float>(tie, s_wf, &Stie);
+        const float need = target - Sgt;   // tied mass still needed, in id order
+        if (tid == 0) s_cut = INT_MIN;
+        __syncthreads();
+        if (tie > 0.f && excl < need && need <= excl + tie) {
+            float c = excl;
+            for (int v = a; v < b; ++v) {
+                if (!keep_token(l[v], v, thrk, cutk) || order_key(l[v]) != kp) continue;
+                c += expf((l[v] - mx) * invT);
+                if (c >= need) {
+                    atomicMax(&s_cut, -v);   // rounding may let two ranges claim: the lower id wins
+                    break;
+                }
+            }
+        }
+        __syncthreads();
+        int cp = s_cut == INT_MIN ? INT_MAX : -s_cut;   // no claim (rounding at the end): every tied token
+        if (kp == thrk) cp = min(cp, cutk);
+        thr = kp;
+        cut = cp;
+    }
+    // kept mass, in the fixed order of the unfiltered sum
+    float s = 0.f;
+    for (int v = tid; v < V; v += 1024)
+        if (keep_token(l[v], v, thr, cut)) s += expf((l[v] - mx) * invT);
+    __syncthreads();
+    *thr_out = thr;
+    *cut_out = cut;
+    return s;
+}
+
 // Per row: index of the largest logit (lowest index among equals), the max,
-// and sum_v exp((l_v - max) * invT) when invT > 0.
+// and, when invT > 0, the row's top-k / top-p keep rule and the sum of
+// exp((l_v - max) * invT) over the kept tokens.
 __global__ void __launch_bounds__(1024) k_argmax(const float *part, const int *planes, long long sstride, int ldp,
                                                  float *logits, int V, float invT, int *amax, float *lmax,
-                                                 float *lsum) {
+                                                 float *lsum, int top_k, float top_p, unsigned *thr_key,
+                                                 int *thr_cut) {
     pdl_trigger();
     pdl_wait();
     __shared__ float sv[32];
@@ -324,16 +479,24 @@ __global__ void __launch_bounds__(1024) k_argmax(const float *part, const int *p
         lmax[r] = best;
     }
     if (invT > 0.f) {
-        float s = 0.f;
-        for (int v = threadIdx.x; v < V; v += 1024) s += expf((l[v] - best) * invT);
+        __syncthreads();   // this CTA's logits stores are visible to all its threads
+        unsigned thr;
+        int cut;
+        float s = row_keep_rule(l, V, best, invT, top_k, top_p, &thr, &cut);
         s = block_sum<1024>(s, red);
-        if (threadIdx.x == 0) lsum[r] = s;
+        if (threadIdx.x == 0) {
+            lsum[r] = s;
+            thr_key[r] = thr;
+            thr_cut[r] = cut;
+        }
     }
 }
 
 cudaError_t argmax_launch(const float *part, const int *planes, long long sstride, int ldp, float *logits, int rows,
-                          int V, float invT, int *amax, float *lmax, float *lsum, cudaStream_t s) {
-    launch_k(k_argmax, dim3(rows), dim3(1024), 0, s, part, planes, sstride, ldp, logits, V, invT, amax, lmax, lsum);
+                          int V, float invT, int *amax, float *lmax, float *lsum, int top_k, float top_p,
+                          unsigned *thr_key, int *thr_cut, cudaStream_t s) {
+    launch_k(k_argmax, dim3(rows), dim3(1024), 0, s, part, planes, sstride, ldp, logits, V, invT, amax, lmax, lsum,
+             top_k, top_p, thr_key, thr_cut);
     return cudaGetLastError();
 }
 

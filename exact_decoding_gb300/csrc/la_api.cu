@@ -82,6 +82,8 @@ struct la_handle {
     AttnUmmaParams attn_proto{};
     float2 *rope = nullptr;
     int *amax = nullptr, *tok = nullptr, *depth = nullptr, *anc = nullptr, *anc_cnt = nullptr, *used = nullptr;
+    unsigned *thr_key = nullptr;   // [U] sampling keep rule of each used row (top-k / top-p)
+    int *thr_cut = nullptr;
     int *iota = nullptr;
     uint32_t *vis_bits = nullptr;   // [M][8] in-step visibility bits
     int anc_stride = 0;
@@ -170,6 +172,8 @@ struct la_handle {
         s.logits = logits;
         s.lmax = lmax;
         s.lsum = lsum;
+        s.thr_key = thr_key;
+        s.thr_cut = thr_cut;
         s.V = V;
         s.pkeys = pkeys;
         s.pcnt = pcnt;
@@ -492,7 +496,7 @@ int run_prefix(la_handle *h, int n, bool want_logits) {
         if (rc != LA_OK) return rc;
         CK(argmax_launch(h->lm_part, h->planes_lm, h->lm_stride, h->ldo_lm, h->logits, 1, h->V,
                          h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
-                         h->lmax, h->lsum, h->stream));
+                         h->lmax, h->lsum, h->opts.top_k, h->opts.top_p, h->thr_key, h->thr_cut, h->stream));
     }
     return LA_OK;
 }
@@ -694,8 +698,9 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         return fail(LA_ERR_UNSUPPORTED, "d_model, ffn and n_heads*head_dim must be multiples of 8");
     const la_opts &O = *opts;
     if (O.N < 2 || O.N > 8 || O.W < 1 || O.G < 0 || O.G > 32 || O.pool_cap < 0 || O.pool_cap > 32 ||
-        !(O.temperature >= 0.f))
-        return fail(LA_ERR_INVALID_ARG, "bad options (N 2..8, W >= 1, G 0..32, pool_cap 0..32, temperature >= 0)");
+        !(O.temperature >= 0.f) || O.top_k < 0 || O.top_p != O.top_p)
+        return fail(LA_ERR_INVALID_ARG,
+                    "bad options (N 2..8, W >= 1, G 0..32, pool_cap 0..32, temperature >= 0, top_k >= 0, top_p a number)");
     const int M = 1 + (O.W + O.G) * (O.N - 1);
     if (M > 256) return fail(LA_ERR_UNSUPPORTED, "1 + (W+G)(N-1) must be <= 256");
     if (O.max_seq < O.N + M + 2) return fail(LA_ERR_INVALID_ARG, "max_seq too small");
@@ -794,6 +799,8 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     A(h->alloc(&h->amax, std::max(h->U, 1)));
     A(h->alloc(&h->lmax, std::max(h->U, 1)));
     A(h->alloc(&h->lsum, std::max(h->U, 1)));
+    A(h->alloc(&h->thr_key, std::max(h->U, 1)));
+    A(h->alloc(&h->thr_cut, std::max(h->U, 1)));
     const size_t cache_bytes = static_cast<size_t>(h->L) * 2 * h->nkv * h->seq * h->hd * sizeof(float);
     if (h->bf16) {
         A(h->alloc(&h->attn_ws, 1));
@@ -1022,7 +1029,7 @@ int enqueue_step(la_handle *h) {
     pe = h->prof_begin();
     CK(argmax_launch(h->lm_part, h->planes_lm, h->lm_stride, h->ldo_lm, h->logits, h->U, h->V,
                      h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax,
-                     h->lmax, h->lsum, s));
+                     h->lmax, h->lsum, h->opts.top_k, h->opts.top_p, h->thr_key, h->thr_cut, s));
     CK(finish_step_launch(h->spec(), s));
     if ((rc = kv_commit(h)) != LA_OK) return rc;
     h->prof_end(pe, 3, 0.0);
@@ -1106,7 +1113,8 @@ int la_ar_step(la_handle *h, int32_t *token) {
     if (rc != LA_OK) return rc;
     if ((rc = run_lm_head(h, 1, false)) != LA_OK) return rc;
     CK(argmax_launch(h->lm_part, h->planes_lm, h->lm_stride, h->ldo_lm, h->logits, 1, h->V,
-                     h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax, h->lmax, h->lsum, s));
+                     h->opts.temperature > 0.f ? 1.f / h->opts.temperature : 0.f, h->amax, h->lmax, h->lsum,
+                     h->opts.top_k, h->opts.top_p, h->thr_key, h->thr_cut, s));
     CK(first_token_launch(h->spec(), P + 1, s));
     h->launches += 2;
     CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));

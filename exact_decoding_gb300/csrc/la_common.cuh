@@ -385,6 +385,19 @@ __device__ __forceinline__ void sum_planes4x2(const float *pa, int na, const flo
     }
 }
 
+// Unsigned key that orders floats like their values (for radix selection).
+__device__ __forceinline__ unsigned order_key(float f) {
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+// Sampling keep rule of one row: token v (logit l) survives top-k / top-p
+// iff its key is above thr, or equal to thr with v <= cut.  thr = 0 and cut
+// = INT_MAX keep everything.
+__device__ __forceinline__ bool keep_token(float l, int v, unsigned thr, int cut) {
+    const unsigned k = order_key(l);
+    return k > thr || (k == thr && v <= cut);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

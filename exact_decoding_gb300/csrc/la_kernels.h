@@ -114,7 +114,8 @@ cudaError_t swiglu_launch(const float *part, const int *planes, long long sstrid
 // Sums the lm_head planes into logits[rows][V], then per row the argmax
 // (lowest id among equals), the max, and sum exp((l - max) * invT) if invT > 0.
 cudaError_t argmax_launch(const float *part, const int *planes, long long sstride, int ldp, float *logits, int rows,
-                          int V, float invT, int *amax, float *lmax, float *lsum, cudaStream_t s);
+                          int V, float invT, int *amax, float *lmax, float *lsum, int top_k, float top_p,
+                          unsigned *thr_key, int *thr_cut, cudaStream_t s);
 
 // ------------------------------------------------------------------ attention
 // Keys of row r: the cached prefix [0, P) plus in-step rows.  In tree mode the
@@ -202,7 +203,9 @@ struct SpecDev {
     const int *amax;      // [U] argmax of used rows
     const float *logits;  // [U][V]
     const float *lmax;    // [U] row max
-    const float *lsum;    // [U] sum of exp((l - max) / T)
+    const float *lsum;    // [U] sum of exp((l - max) / T) over the tokens kept by top-k / top-p
+    const unsigned *thr_key;  // [U] keep rule of each row's sampling distribution (keep_token)
+    const int *thr_cut;
     int V;
     int *pkeys, *pcnt, *phead, *pent;  // pool: open-addressed table keyed by first token
     int nslots_log2;

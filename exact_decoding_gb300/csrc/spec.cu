@@ -163,9 +163,11 @@ __global__ void __launch_bounds__(256) k_build_rows(SpecDev d) {
 
 // ------------------------------------------------------------------ inverse CDF (one block)
 // Smallest id whose ascending cumulative weight exceeds u * total, with
-// weight exp((l_v - mx) * invT) and the ids in rej[0..nrej) removed.
+// weight exp((l_v - mx) * invT) for the tokens the row's keep rule (thr,
+// cut) keeps and the ids in rej[0..nrej) removed.
 template <int NT>
-__device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, const int *rej, int nrej, float u) {
+__device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, const int *rej, int nrej, float u,
+                                 unsigned thr, int cut) {
     __shared__ float s_part[NT];
     __shared__ float s_warp[NT / 32];
     __shared__ int s_ans;
@@ -176,7 +178,7 @@ __device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, co
     for (int v = a; v < b; ++v) {
         bool r = false;
         for (int i = 0; i < nrej; ++i) r = r || (rej[i] == v);
-        part += r ? 0.f : expf((l[v] - mx) * invT);
+        part += (r || !keep_token(l[v], v, thr, cut)) ? 0.f : expf((l[v] - mx) * invT);
     }
     // inclusive warp scan, then across warps (fixed order)
     float incl = part;
@@ -209,7 +211,7 @@ __device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, co
         for (int v = a; v < b; ++v) {
             bool r = false;
             for (int i = 0; i < nrej; ++i) r = r || (rej[i] == v);
-            s += r ? 0.f : expf((l[v] - mx) * invT);
+            s += (r || !keep_token(l[v], v, thr, cut)) ? 0.f : expf((l[v] - mx) * invT);
             if (excl + s > t) {
                 ans = v;
                 break;
@@ -226,7 +228,7 @@ __device__ int block_inverse_cdf(const float *l, int V, float mx, float invT, co
                 for (int v = bb - 1; v >= aa; --v) {
                     bool r = false;
                     for (int k = 0; k < nrej; ++k) r = r || (rej[k] == v);
-                    if (!r && expf((l[v] - mx) * invT) > 0.f) {
+                    if (!r && keep_token(l[v], v, thr, cut) && expf((l[v] - mx) * invT) > 0.f) {
                         s_ans = v;
                         break;
                     }
@@ -286,7 +288,9 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
                 int nd = 0, accepted = -1, nrej = 0;
                 float rej_mass = 0.f;
                 const float *lr = d.logits + static_cast<long long>(dist_u) * d.V;
-                const float mx = d.lmax[dist_u], Z = d.lsum[dist_u];
+                const float mx = d.lmax[dist_u], Z = d.lsum[dist_u];   // Z: mass the keep rule keeps
+                const unsigned thr = d.thr_key[dist_u];
+                const int cut = d.thr_cut[dist_u];
                 if (depth <= L && surv) {
                     for (int c = 0; c < g; ++c) {
                         if (!((surv >> c) & 1u)) continue;
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
                         for (int i = 0; i < nrej; ++i) seen = seen || (s_rej[i] == x);
                         if (seen) continue;
                         const float r = draw_uniform(d.seed, pos, nd++);
-                        const float ex = expf((lr[x] - mx) * invT);
+                        const float ex = keep_token(lr[x], x, thr, cut) ? expf((lr[x] - mx) * invT) : 0.f;
                         const float px = ex / (Z - rej_mass);
                         if (r <= px) {
                             accepted = x;
@@ -330,7 +334,7 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
     if (s_need_draw) {
         const int u = s_dist_u;
         const int x = block_inverse_cdf<kFinishThreads>(d.logits + static_cast<long long>(u) * d.V, d.V, d.lmax[u],
-                                                        1.f / d.T, s_rej, s_nrej, s_u);
+                                                        1.f / d.T, s_rej, s_nrej, s_u, d.thr_key[u], d.thr_cut[u]);
         if (tid == 0) {
             s_acc[s_A] = x;
             s_A = s_A + 1;
@@ -433,7 +437,8 @@ __global__ void __launch_bounds__(kFinishThreads) k_first_token(SpecDev d, int n
         y = d.amax[0];
     } else {
         const float u = draw_uniform(d.seed, n, 0);
-        y = block_inverse_cdf<kFinishThreads>(d.logits, d.V, d.lmax[0], 1.f / d.T, nullptr, 0, u);
+        y = block_inverse_cdf<kFinishThreads>(d.logits, d.V, d.lmax[0], 1.f / d.T, nullptr, 0, u, d.thr_key[0],
+                                              d.thr_cut[0]);
     }
     if (threadIdx.x == 0) {
         d.tokens_log[n] = y;

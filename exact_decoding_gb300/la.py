@@ -46,7 +46,7 @@ class la_opts(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int32), ("W", ctypes.c_int32), ("G", ctypes.c_int32), ("max_seq", ctypes.c_int32),
                 ("prompt_as_reference", ctypes.c_int32), ("pool_cap", ctypes.c_int32),
                 ("temperature", ctypes.c_float), ("seed", ctypes.c_uint64), ("cuda_stream", ctypes.c_void_p),
-                ("profile", ctypes.c_int32)]
+                ("profile", ctypes.c_int32), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
 
 
 class la_stats_t(ctypes.Structure):
@@ -257,12 +257,13 @@ class Decoder:
 
     def __init__(self, weights, N: int, W: int, G: int, max_seq: int, temperature: float = 0.0,
                  seed: int = 0, prompt_as_reference: bool = False, pool_cap: int = 0, stream=None, device="cuda",
-                 profile: bool = False):
+                 profile: bool = False, top_k: int = 0, top_p: float = 1.0):
         self.weights = weights if isinstance(weights, DeviceWeights) else DeviceWeights(weights, device)
         self.dims, self.N, self.W, self.G = self.weights.dims, N, W, G
         self.stream = stream
         sp = stream.cuda_stream if stream is not None else None
-        o = la_opts(N, W, G, max_seq, int(prompt_as_reference), pool_cap, temperature, seed, sp, int(profile))
+        o = la_opts(N, W, G, max_seq, int(prompt_as_reference), pool_cap, temperature, seed, sp, int(profile),
+                    top_k, top_p)
         self.h = la_create(self.weights.dims_struct, self.weights.struct, o)
 
     def prefill(self, prompt) -> int:

@@ -106,6 +106,11 @@ typedef struct la_opts {
     int32_t profile;              /* 1: bracket every GEMM and attention launch of la_step with CUDA
                                      events and accumulate their device time in la_stats (adds two
                                      event records per launch) */
+    int32_t top_k;                /* temperature > 0: keep only the top_k most probable tokens of every
+                                     sampling distribution (ties to the lower id); 0: off */
+    float   top_p;                /* temperature > 0: then keep the shortest most-probable prefix whose
+                                     renormalised mass reaches top_p (the crossing token included);
+                                     <= 0 or >= 1: off.  Order: temperature, top_k, top_p */
 } la_opts;
 
 typedef struct la_handle la_handle;

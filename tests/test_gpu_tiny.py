@@ -203,3 +203,64 @@ def test_ar_step_equals_oracle_autoregressive(lib, tiny_model):
     upto = compare_stream(out, ar, margins, MARGIN)
     assert upto >= 16, f"first low-margin decision at {upto}"
     dec.close()
+
+
+def test_sampling_top_k1_equals_greedy(lib, tiny_model):
+    """top_k = 1 keeps one token per distribution: lookahead sampling at T = 1
+    on the GPU reproduces the greedy autoregressive stream."""
+    wl, w, p = tiny_model
+    ar, margins = ar_with_margins(w, p, 40)
+    dec = make(lib, w, 3, 4, 4, temperature=1.0, seed=77, top_k=1)
+    out, _ = dec.generate(p, 40)
+    upto = compare_stream(out, ar, margins, MARGIN)
+    assert upto >= 16, f"first low-margin decision at {upto}"
+    dec.close()
+
+
+def _keep_sets_safe(orc_logits_rows, T, top_k, top_p, eps=1e-4):
+    """True when no top-k / top-p boundary of these rows lies within eps (in
+    logit for top-k, in renormalised mass for top-p) of a flip, so fp32 and
+    fp64 must keep the same tokens."""
+    for l in orc_logits_rows:
+        l = np.asarray(l, dtype=np.float64)
+        order = sorted(range(len(l)), key=lambda v: (-l[v], v))
+        if 0 < top_k < len(l) and l[order[top_k - 1]] - l[order[top_k]] <= eps:
+            return False
+        if 0 < top_p < 1:
+            kept = order[:top_k] if 0 < top_k < len(l) else order
+            q = np.exp((l[kept] - l[kept[0]]) / T)
+            c = np.cumsum(q) / q.sum()
+            if np.min(np.abs(c - top_p)) <= eps:
+                return False
+    return True
+
+
+@pytest.mark.parametrize("top_k,top_p", [(8, 1.0), (0, 0.9), (6, 0.8)])
+def test_step_teacher_forced_sampling_top_k_top_p(lib, tiny_model, top_k, top_p):
+    """Algorithm 4 on top-k / top-p filtered distributions: same Philox draws
+    on both sides; a step may differ only where a draw sits within 1e-3 of
+    its threshold or a filter boundary within 1e-4 of a flip."""
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(8, wl.dims.vocab, seed=19), 5)
+    N, W, G = 4, 3, 4
+    T = 0.7
+    dec = make(lib, w, N, W, G, temperature=T, seed=4321, prompt_as_reference=True, top_k=top_k, top_p=top_p)
+    dec.prefill(p)
+    orc = la.Lookahead(w, N, W, G, temperature=T, seed=4321, prompt_as_reference=True, keep_logits=True,
+                       top_k=top_k, top_p=top_p)
+    exact = 0
+    for t in range(10):
+        s0 = dec.export_state()
+        orc.load_state(s0["tokens"], s0["window"], s0["records"])
+        acc_ref = orc.step()
+        rec = orc.history[-1]
+        acc = dec.step()
+        if acc == acc_ref:
+            exact += 1
+            continue
+        near = [d for d in rec.trace if abs(d.value) <= 1e-3]
+        rows = [rec.logits[0]] + [rec.logits[1 + W + i] for i in range(G * (N - 1))]
+        assert near or not _keep_sets_safe(rows, T, top_k, top_p), \
+            f"step {t}: gpu {acc} vs oracle {acc_ref} with no near-threshold decision"
+    assert exact >= 7
+    dec.close()
