@@ -124,20 +124,30 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def gemm_source_fp(read=None) -> str:
+    """Fingerprint of the GEMM kernel sources with comments and blank lines
+    removed, so that only a code change voids a traffic record."""
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "exact_decoding_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "la_common.cuh", "la_kernels.h"):
+        text = read(f) if read else open(os.path.join(csrc, f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(text.encode())
+    return h.hexdigest()[:16]
+
+
 def gemm_traffic():
     """DRAM bytes per k_gemm_tc2 launch from the committed ncu summary, or None
-    when the kernel sources changed since those counters were taken."""
-    import hashlib
+    when the kernel code changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", "k_gemm_tc2_traffic.txt")
     if not os.path.exists(path):
         return None
     rec = dict(line.split() for line in open(path) if line.strip())
-    csrc = os.path.join(ROOT, "exact_decoding_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in ("gemm.cu", "la_common.cuh", "la_kernels.h"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest()[:16] != rec.get("gemm_source_fp"):
+    if gemm_source_fp() != rec.get("gemm_source_fp"):
         return None
     return float(rec["traffic_bytes_per_launch"])
 

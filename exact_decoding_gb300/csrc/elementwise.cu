@@ -1,7 +1,9 @@
 // Row-wise kernels between the projection GEMMs of one decoder layer:
 //   embedding gather + RMSNorm, split-K reduction + rotary embedding + KV
-//   write, split-K reduction + residual add + RMSNorm, split-K reduction +
-//   SwiGLU, and the vocabulary argmax (with softmax statistics for sampling).
+//   write (fp32 models; bf16 models do this in the attention kernel's
+//   prologue), split-K reduction + residual add + RMSNorm, split-K
+//   reduction + SwiGLU, and the vocabulary argmax with, for sampling, each
+//   row's top-k / top-p keep rule and kept softmax mass.
 // The residual stream h stays fp32; T is the GEMM-input / KV-cache type.
 #include <algorithm>
 #include <climits>

@@ -4,13 +4,17 @@
 // on the same weight stream).
 //
 // bf16 path -- tcgen05 tensor cores, swap-AB: the weight matrix [out][K] is
-// the UMMA A operand (128 output features per tile, K-major), the step rows
-// [rows][K] are the B operand (N = rows padded to 16), the fp32 accumulator
-// lives in TMEM (128 lanes x N columns).  One warp issues TMA loads into a
-// shared-memory ring, one thread issues UMMAs, four warps drain TMEM.  Small
-// projections are split along K so that every SM streams weights; partial
-// sums go to a workspace and are added in a fixed order by the consumer
-// kernel, so results are deterministic.
+// the UMMA A operand (K-major), the step rows [rows][K] are the B operand as
+// bf16 (hi, lo) pairs stacked along N, the fp32 accumulator lives in TMEM.
+// k_gemm_tc2 (the step's GEMMs) runs one 2-SM UMMA (cta_group::2, M = 256
+// features, N = 256 = hi rows + lo rows) per CTA pair of a thread-block
+// cluster: each CTA streams its 128 weight rows and its half of the input
+// rows through a TMA ring, the pair leader issues the UMMAs, four warps per
+// CTA drain TMEM and add the hi and lo columns.  k_gemm_tc is the 1-SM form
+// (M = 128), used by la_gemm_bf16.  The flattened tile x k-block work is
+// split evenly over the SMs (stream-K); partial sums go to a workspace and
+// are added in a fixed order by the consumer kernel, so results are
+// deterministic.
 //
 // fp32 path -- a plain SIMT kernel (fp32 FMA, no tf32) for fp32 models.
 #include <algorithm>

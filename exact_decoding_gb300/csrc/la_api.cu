@@ -3,7 +3,8 @@
 // (paper-graph-ui page, section 3.4: lookahead branch + verification branch
 // + pool update in one forward pass).  Everything that touches step data
 // runs in the kernels of this library on the caller's stream; the host only
-// sequences launches and copies the step's accepted tokens back.
+// sequences launches (after the first step: replays one captured CUDA graph
+// per step) and copies the step's accepted tokens back.
 #include <algorithm>
 #include <cmath>
 #include <cstdarg>
