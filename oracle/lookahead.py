@@ -55,6 +55,16 @@ Readings taken where the pages are open:
      mass reaches p (the token that crosses p included).  Algorithm 4 then
      runs on the filtered distributions unchanged, so its output follows the
      filtered distribution exactly.
+  R15 LRU pool (section 7, "Follow-Up Research This Work Enables", names
+     LRU next to FIFO as an eviction policy the paper leaves open).  Each
+     key's list is kept least recently used first.  An entry is used when a
+     step accepts at least one of its tokens as the winning candidate, or
+     when the harvest meets it again; a use moves it to the most recent
+     end.  The winner's use is recorded after verification and before the
+     harvest.  A new suffix is appended at the most recent end, and when
+     the list is full the least recently used entry is dropped.  Lookup
+     returns the G most recently used entries, most recent first.  Under
+     FIFO (R6) neither a use nor a repeated harvest changes the order.
 """
 from __future__ import annotations
 
@@ -146,37 +156,57 @@ def step_mask(N: int, W: int, G: int) -> np.ndarray:
 # n-gram pool (reading R6)
 # --------------------------------------------------------------------------
 
-class Pool:
-    """First token -> FIFO list of distinct (N-1)-token suffixes."""
+FIFO, LRU = "fifo", "lru"
 
-    def __init__(self, cap: int):
+
+class Pool:
+    """First token -> list of distinct (N-1)-token suffixes, in eviction
+    order (the next to be dropped first): oldest first under FIFO (R6),
+    least recently used first under LRU (R15)."""
+
+    def __init__(self, cap: int, policy: str = FIFO):
+        assert policy in (FIFO, LRU)
         self.cap = cap
+        self.policy = policy
         self.lists: Dict[int, List[Tuple[int, ...]]] = {}
 
     def insert(self, key: int, suffix: Sequence[int]) -> None:
         suffix = tuple(int(t) for t in suffix)
         lst = self.lists.setdefault(int(key), [])
         if suffix in lst:
+            self.use(key, suffix)
             return
         lst.append(suffix)
         if len(lst) > self.cap:
             lst.pop(0)
 
+    def use(self, key: int, suffix: Sequence[int]) -> None:
+        """LRU: move a present suffix to the most recent end (FIFO: no-op)."""
+        if self.policy != LRU:
+            return
+        suffix = tuple(int(t) for t in suffix)
+        lst = self.lists[int(key)]
+        lst.remove(suffix)
+        lst.append(suffix)
+
     def lookup(self, key: int, G: int) -> List[Tuple[int, ...]]:
-        return list(self.lists.get(int(key), []))[:G]
+        lst = list(self.lists.get(int(key), []))
+        if self.policy == LRU:
+            lst.reverse()
+        return lst[:G]
 
     def records(self) -> List[Tuple[int, Tuple[int, ...]]]:
-        """Canonical form: keys ascending, each key's suffixes oldest first."""
+        """Canonical form: keys ascending, each key's suffixes in eviction order."""
         return [(k, s) for k in sorted(self.lists) for s in self.lists[k]]
 
     def copy(self) -> "Pool":
-        p = Pool(self.cap)
+        p = Pool(self.cap, self.policy)
         p.lists = {k: list(v) for k, v in self.lists.items()}
         return p
 
     @staticmethod
-    def from_records(cap: int, records) -> "Pool":
-        p = Pool(cap)
+    def from_records(cap: int, records, policy: str = FIFO) -> "Pool":
+        p = Pool(cap, policy)
         for k, s in records:
             p.insert(k, s)
         return p
@@ -385,7 +415,7 @@ class Lookahead:
 
     def __init__(self, weights, N: int, W: int, G: int, temperature: float = 0.0, seed: int = 0,
                  prompt_as_reference: bool = False, pool_cap: int = 0, dtype=np.float64,
-                 keep_logits: bool = False, top_k: int = 0, top_p: float = 1.0):
+                 keep_logits: bool = False, top_k: int = 0, top_p: float = 1.0, pool_policy: str = FIFO):
         assert N >= 2 and W >= 1 and G >= 0
         self.w, self.N, self.W, self.G = weights, N, W, G
         self.T, self.seed = temperature, seed
@@ -393,7 +423,7 @@ class Lookahead:
         self.par = prompt_as_reference
         self.dtype = dtype
         self.keep_logits = keep_logits
-        self.pool = Pool(pool_cap if pool_cap > 0 else max(G, 1))
+        self.pool = Pool(pool_cap if pool_cap > 0 else max(G, 1), pool_policy)
         self.rows = step_rows(N, W, G)
         self.used = used_rows(N, W, G)
         self.mask = step_mask(N, W, G)
@@ -435,7 +465,7 @@ class Lookahead:
         _, self.cache = decoder.forward(self.w, self.tokens[:P], np.arange(P), decoder.causal_mask(0, P),
                                         dtype=self.dtype, logit_rows=[P - 1])
         self.window = np.array(window, dtype=np.int64).reshape(self.N - 1, self.W)
-        self.pool = Pool.from_records(self.pool.cap, pool_records)
+        self.pool = Pool.from_records(self.pool.cap, pool_records, self.pool.policy)
 
     # one step -----------------------------------------------------------
     def step_inputs(self):
@@ -480,6 +510,8 @@ class Lookahead:
         self.cache = decoder.concat_cache(self.cache, [(k[keep], v[keep]) for k, v in kv])
         rec = StepRecord(P, o, cands, acc, winner, new, self.window.copy(),
                          logits if self.keep_logits else None, trace)
+        if winner >= 0:
+            self.pool.use(o, cands[winner])
         for key, suf in harvest(self.window, new):
             self.pool.insert(key, suf)
         self.window = shift(self.window, new)

@@ -96,6 +96,96 @@ def test_pool_fifo_and_dedup():
     assert p.lookup(99, 4) == []
 
 
+def test_pool_lru_hand_example():
+    """Reading R15 worked by hand: a repeated harvest and a use move an entry
+    to the most recent end; a full list drops its least recently used entry;
+    lookup is most recent first."""
+    p = la.Pool(cap=3, policy=la.LRU)
+    p.insert(7, (1, 2))
+    p.insert(7, (3, 4))
+    p.insert(7, (5, 6))
+    p.insert(7, (1, 2))            # met again: (1, 2) becomes the most recent
+    assert p.records() == [(7, (3, 4)), (7, (5, 6)), (7, (1, 2))]
+    p.insert(7, (8, 9))            # full: the least recently used (3, 4) leaves
+    assert p.lookup(7, 10) == [(8, 9), (1, 2), (5, 6)]
+    assert p.lookup(7, 2) == [(8, 9), (1, 2)]
+    p.use(7, (5, 6))
+    assert p.lookup(7, 10) == [(5, 6), (8, 9), (1, 2)]
+    p.insert(7, (0, 1))            # now (1, 2) is the least recently used
+    assert p.lookup(7, 10) == [(0, 1), (5, 6), (8, 9)]
+    # the same operations under FIFO: neither the repeat nor the use reorders
+    f = la.Pool(cap=3)
+    for suf in [(1, 2), (3, 4), (5, 6), (1, 2), (8, 9)]:
+        f.insert(7, suf)
+    f.use(7, (5, 6))
+    f.insert(7, (0, 1))
+    assert f.lookup(7, 10) == [(5, 6), (8, 9), (0, 1)]
+
+
+class _StampLRU:
+    """LRU written another way: every entry carries the time of its last
+    use; the list is the entries by ascending time, and a full key drops the
+    entry with the smallest time."""
+
+    def __init__(self, cap):
+        self.cap, self.t, self.stamp = cap, 0, {}
+
+    def touch(self, key, suf):
+        self.t += 1
+        ent = self.stamp.setdefault(key, {})
+        if suf not in ent and len(ent) == self.cap:
+            del ent[min(ent, key=ent.get)]
+        ent[suf] = self.t
+
+    def records(self):
+        return [(k, s) for k in sorted(self.stamp) for s in sorted(self.stamp[k], key=self.stamp[k].get)]
+
+
+@pytest.mark.parametrize("cap,seed", [(1, 0), (2, 1), (3, 2), (5, 3)])
+def test_pool_lru_equals_timestamp_model(cap, seed):
+    rng = np.random.default_rng(seed)
+    p, ref = la.Pool(cap, la.LRU), _StampLRU(cap)
+    for _ in range(400):
+        key, suf = int(rng.integers(0, 3)), (int(rng.integers(0, 4)), int(rng.integers(0, 3)))
+        if rng.random() < 0.3 and p.lists.get(key):
+            suf = p.lists[key][int(rng.integers(0, len(p.lists[key])))]
+            p.use(key, suf)
+        else:
+            p.insert(key, suf)
+        ref.touch(key, suf)
+        assert p.records() == ref.records()
+    for key in range(3):
+        assert p.lookup(key, 2) == [s for k, s in reversed(ref.records()) if k == key][:2]
+
+
+@pytest.mark.parametrize("N,W,G,cap", [(4, 3, 4, 0), (3, 4, 2, 3), (5, 2, 3, 2)])
+def test_lru_pool_lossless_and_replay(tiny, N, W, G, cap):
+    """With the LRU pool greedy lookahead still equals greedy autoregressive
+    decoding, and the pool after the run equals the timestamp model fed the
+    prompt's n-grams, then per step the winner's use and the harvest."""
+    wl, w, _ = tiny
+    chunk = synth.uniform_tokens(6, wl.dims.vocab, seed=4)
+    p = np.tile(chunk, 5)
+    ar = la.generate_ar(w, p, 40)
+    o = la.Lookahead(w, N, W, G, prompt_as_reference=True, pool_cap=cap, pool_policy=la.LRU)
+    out, _ = o.generate(p, 40)
+    assert out == ar
+    ref = _StampLRU(o.pool.cap)
+    for i in range(len(p) - N + 1):
+        ref.touch(int(p[i]), tuple(int(t) for t in p[i + 1:i + N]))
+    used = 0
+    for rec in o.history:
+        assert rec.cands == [s for k, s in reversed(ref.records()) if k == rec.o][:G]
+        if rec.winner >= 0:
+            ref.touch(rec.o, rec.cands[rec.winner])
+            used += 1
+        for j in range(W):
+            ref.touch(int(rec.window_before[0, j]),
+                      tuple(int(rec.window_before[k, j]) for k in range(1, N - 1)) + (rec.new[j],))
+    assert used > 0
+    assert o.pool.records() == ref.records()
+
+
 @pytest.mark.parametrize("N,W,G,par", [(3, 4, 4, False), (2, 3, 3, False), (4, 2, 5, False),
                                        (5, 3, 0, False), (3, 1, 2, True), (4, 4, 4, True)])
 def test_lossless_vs_autoregressive(tiny, N, W, G, par):
