@@ -182,6 +182,7 @@ struct la_handle {
         s.pent = pent;
         s.nslots_log2 = nslots_log2;
         s.cap = cap;
+        s.lru = opts.pool_policy == LA_POOL_LRU;
         s.N = N;
         s.W = W;
         s.G = G;
@@ -699,9 +700,11 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         return fail(LA_ERR_UNSUPPORTED, "d_model, ffn and n_heads*head_dim must be multiples of 8");
     const la_opts &O = *opts;
     if (O.N < 2 || O.N > 8 || O.W < 1 || O.G < 0 || O.G > 32 || O.pool_cap < 0 || O.pool_cap > 32 ||
-        !(O.temperature >= 0.f) || O.top_k < 0 || O.top_p != O.top_p)
+        !(O.temperature >= 0.f) || O.top_k < 0 || O.top_p != O.top_p ||
+        (O.pool_policy != LA_POOL_FIFO && O.pool_policy != LA_POOL_LRU))
         return fail(LA_ERR_INVALID_ARG,
-                    "bad options (N 2..8, W >= 1, G 0..32, pool_cap 0..32, temperature >= 0, top_k >= 0, top_p a number)");
+                    "bad options (N 2..8, W >= 1, G 0..32, pool_cap 0..32, temperature >= 0, top_k >= 0, "
+                    "top_p a number, pool_policy FIFO or LRU)");
     const int M = 1 + (O.W + O.G) * (O.N - 1);
     if (M > 256) return fail(LA_ERR_UNSUPPORTED, "1 + (W+G)(N-1) must be <= 256");
     if (O.max_seq < O.N + M + 2) return fail(LA_ERR_INVALID_ARG, "max_seq too small");

@@ -210,6 +210,7 @@ struct SpecDev {
     int *pkeys, *pcnt, *phead, *pent;  // pool: open-addressed table keyed by first token
     int nslots_log2;
     int cap;
+    int lru;              // 1: LRU pool order (uses move entries to the most recent end); 0: FIFO
     int N, W, G, M, U;
     float T;
     unsigned long long seed;

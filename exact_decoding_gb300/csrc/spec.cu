@@ -14,11 +14,15 @@
 //
 // n-gram pool: open-addressed hash table keyed by the n-gram's first token
 // (Fibonacci hashing, linear probing, >= 2x as many slots as the vocabulary
-// so it never fills).  Each slot keeps a FIFO ring of up to `cap` distinct
-// (N-1)-token suffixes, oldest first; inserting a suffix that is present
-// does nothing, inserting into a full ring drops the oldest.  All pool
-// operations run in one warp: lanes probe 32 slots, or compare 32 ring
-// entries, at once; inserts keep their sequential order.
+// so it never fills).  Each slot keeps a ring of up to `cap` distinct
+// (N-1)-token suffixes in eviction order (the next to be dropped at the
+// head); a new suffix goes to the tail, and into a full ring it replaces
+// the head.  FIFO: a suffix that is present stays where it is, candidates
+// are read from the head.  LRU (section 7 of the same page leaves the
+// eviction policy open): a suffix harvested again, or the step's winning
+// candidate, moves to the tail, and candidates are read from the tail.  All
+// pool operations run in one warp: lanes probe 32 slots, or compare 32
+// ring entries, at once; inserts keep their sequential order.
 #include <climits>
 
 #include "la_kernels.h"
@@ -77,6 +81,46 @@ __device__ int pool_find(const SpecDev &d, int key, int lane) {
     return INT_MIN;
 }
 
+// Ring entry `i` (0 = head) of `slot` moves to the tail; entries i+1..cnt-1
+// move one place towards the head.  Lane l holds list entry l (cap <= 32).
+__device__ void pool_move_to_tail_warp(const SpecDev &d, int slot, int i, int lane) {
+    const int L = d.N - 1, cap = d.cap;
+    const int cnt = d.pcnt[slot], head = d.phead[slot];
+    if (i < 0 || i >= cnt - 1) return;   // absent, or already at the tail
+    int *ring = d.pent + static_cast<long long>(slot) * cap * L;
+    int e[7];
+#pragma unroll
+    for (int m = 0; m < 7; ++m) e[m] = (lane < cnt && m < L) ? ring[((head + lane) % cap) * L + m] : 0;
+    const int src = lane < i ? lane : (lane < cnt - 1 ? lane + 1 : i);
+#pragma unroll
+    for (int m = 0; m < 7; ++m) e[m] = __shfl_sync(FULL, e[m], src & 31);
+    __syncwarp();
+    if (lane < cnt)
+        for (int m = 0; m < L; ++m) ring[((head + lane) % cap) * L + m] = e[m];
+    __syncwarp();
+}
+
+// List index of the entry of `slot` equal to suf, or -1 (every lane gets it).
+__device__ int pool_index_warp(const SpecDev &d, int slot, const int *suf, int lane) {
+    const int L = d.N - 1, cap = d.cap;
+    const int cnt = d.pcnt[slot], head = d.phead[slot];
+    bool same = false;
+    if (lane < cnt) {
+        const int *e = d.pent + (static_cast<long long>(slot) * cap + (head + lane) % cap) * L;
+        same = true;
+        for (int m = 0; m < L; ++m) same = same && (e[m] == suf[m]);
+    }
+    const unsigned hit = __ballot_sync(FULL, same);
+    return hit ? __ffs(hit) - 1 : -1;
+}
+
+// LRU: the suffix `suf` of `key` (if present) moves to the tail.
+__device__ void pool_use_warp(const SpecDev &d, int key, const int *suf, int lane) {
+    const int f = pool_find(d, key, lane);
+    if (f < 0) return;
+    pool_move_to_tail_warp(d, f, pool_index_warp(d, f, suf, lane), lane);
+}
+
 // suf: N-1 tokens, identical in every lane.
 __device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int lane) {
     const int L = d.N - 1, cap = d.cap;
@@ -96,13 +140,11 @@ __device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int 
         __syncwarp();
     }
     const int cnt = d.pcnt[slot], head = d.phead[slot];
-    bool same = false;
-    if (lane < cnt) {
-        const int *e = d.pent + (static_cast<long long>(slot) * cap + (head + lane) % cap) * L;
-        same = true;
-        for (int m = 0; m < L; ++m) same = same && (e[m] == suf[m]);
+    const int present = pool_index_warp(d, slot, suf, lane);
+    if (present >= 0) {
+        if (d.lru) pool_move_to_tail_warp(d, slot, present, lane);
+        return;
     }
-    if (__any_sync(FULL, same)) return;
     if (lane == 0) {
         int pos;
         if (cnt < cap) {
@@ -136,7 +178,8 @@ __global__ void __launch_bounds__(256) k_build_rows(SpecDev d) {
                 g = min(cnt, d.G);
                 for (int t = lane; t < g * L; t += 32) {
                     const int c = t / L, m = t % L;
-                    s_c[t] = d.pent[(static_cast<long long>(f) * d.cap + (head + c) % d.cap) * L + m];
+                    const int li = d.lru ? cnt - 1 - c : c;   // LRU: most recent first
+                    s_c[t] = d.pent[(static_cast<long long>(f) * d.cap + (head + li) % d.cap) * L + m];
                 }
             }
         }
@@ -341,9 +384,14 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
         }
         __syncthreads();
     }
-    // Harvest the window's n-grams (column order), then slide it.
+    // LRU: the winning candidate was used (before the harvest); then harvest
+    // the window's n-grams (column order) and slide the window.
     if (tid < 32) {
         int suf[8];
+        if (d.lru && s_win >= 0) {
+            for (int m = 0; m < L; ++m) suf[m] = d.cands[s_win * L + m];
+            pool_use_warp(d, d.st->o, suf, tid);
+        }
         for (int j = 0; j < d.W; ++j) {
             for (int k = 1; k < L; ++k) suf[k - 1] = d.window[k * d.W + j];
             suf[L - 1] = d.amax[1 + j];

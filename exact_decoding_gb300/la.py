@@ -17,6 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libla.so")
 
 LA_F32, LA_BF16 = 0, 1
+LA_POOL_FIFO, LA_POOL_LRU = 0, 1
 _lib = None
 
 
@@ -46,7 +47,8 @@ class la_opts(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int32), ("W", ctypes.c_int32), ("G", ctypes.c_int32), ("max_seq", ctypes.c_int32),
                 ("prompt_as_reference", ctypes.c_int32), ("pool_cap", ctypes.c_int32),
                 ("temperature", ctypes.c_float), ("seed", ctypes.c_uint64), ("cuda_stream", ctypes.c_void_p),
-                ("profile", ctypes.c_int32), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+                ("profile", ctypes.c_int32), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("pool_policy", ctypes.c_int32)]
 
 
 class la_stats_t(ctypes.Structure):
@@ -257,13 +259,16 @@ class Decoder:
 
     def __init__(self, weights, N: int, W: int, G: int, max_seq: int, temperature: float = 0.0,
                  seed: int = 0, prompt_as_reference: bool = False, pool_cap: int = 0, stream=None, device="cuda",
-                 profile: bool = False, top_k: int = 0, top_p: float = 1.0):
+                 profile: bool = False, top_k: int = 0, top_p: float = 1.0, pool_policy: str = "fifo"):
         self.weights = weights if isinstance(weights, DeviceWeights) else DeviceWeights(weights, device)
         self.dims, self.N, self.W, self.G = self.weights.dims, N, W, G
         self.stream = stream
         sp = stream.cuda_stream if stream is not None else None
+        policies = {"fifo": LA_POOL_FIFO, "lru": LA_POOL_LRU}
+        if pool_policy not in policies:
+            raise ValueError(f"pool_policy must be 'fifo' or 'lru', not {pool_policy!r}")
         o = la_opts(N, W, G, max_seq, int(prompt_as_reference), pool_cap, temperature, seed, sp, int(profile),
-                    top_k, top_p)
+                    top_k, top_p, policies[pool_policy])
         self.h = la_create(self.weights.dims_struct, self.weights.struct, o)
 
     def prefill(self, prompt) -> int:

@@ -51,6 +51,16 @@ extern "C" {
                         as (hi, lo) bf16 pairs (about 16 mantissa bits), fp32 accumulation
                         and fp32 residual stream (tcgen05 tensor-core GEMMs and attention) */
 
+/* n-gram pool eviction policies (la_opts.pool_policy).  The pages keep the
+ * pool's management open (paper-graph-ui page, section 7, "Follow-Up
+ * Research This Work Enables": LRU, FIFO or frequency-based eviction). */
+#define LA_POOL_FIFO 0   /* each key's suffixes in insertion order; a full list drops the oldest;
+                            candidates are the oldest G */
+#define LA_POOL_LRU  1   /* least recently used first; a use (the step's winning candidate, when it
+                            contributed an accepted token, or a suffix harvested again) moves an
+                            entry to the most recent end; a full list drops the least recently used;
+                            candidates are the G most recently used, most recent first */
+
 /* Model shape of a LLaMA-style decoder (the pages run LLaMA-2 / CodeLlama,
  * paper-graph-ui page, section 5 "Experimental setup"). */
 typedef struct la_model_dims {
@@ -99,7 +109,7 @@ typedef struct la_opts {
     int32_t G;                    /* candidates per step, 0..32 */
     int32_t max_seq;              /* KV capacity in tokens: prompt + generated + step rows */
     int32_t prompt_as_reference;  /* 1: seed the pool with the prompt's n-grams after prefill */
-    int32_t pool_cap;             /* suffixes kept per first token (FIFO); 0 -> G (min 1); <= 32 */
+    int32_t pool_cap;             /* suffixes kept per first token; 0 -> G (min 1); <= 32 */
     float   temperature;          /* 0: greedy (Algorithm 3); > 0: sampling (Algorithm 4) */
     uint64_t seed;                /* window initialisation and sampling draws */
     void   *cuda_stream;          /* cudaStream_t or NULL */
@@ -111,6 +121,7 @@ typedef struct la_opts {
     float   top_p;                /* temperature > 0: then keep the shortest most-probable prefix whose
                                      renormalised mass reaches top_p (the crossing token included);
                                      <= 0 or >= 1: off.  Order: temperature, top_k, top_p */
+    int32_t pool_policy;          /* LA_POOL_FIFO (0) or LA_POOL_LRU (1) */
 } la_opts;
 
 typedef struct la_handle la_handle;
@@ -148,7 +159,9 @@ typedef struct la_state_t {
     int32_t  n_records;     /* pool entries */
     int32_t  records_cap;
     int32_t *records;       /* [records_cap][N]: first token, then the N-1 suffix tokens;
-                               keys ascending, each key's suffixes oldest first */
+                               keys ascending, each key's suffixes in eviction order (the next
+                               to be dropped first: oldest under FIFO, least recently used
+                               under LRU); la_import_state rebuilds the same order */
 } la_state_t;
 
 /* Create a decoder for the given weights.  Allocates the KV cache (fp32

@@ -59,10 +59,13 @@ def test_generate_equals_autoregressive(lib, tiny_model, N, W, G, par):
     dec.close()
 
 
-def _teacher_forced(lib, w, p, N, W, G, steps, temperature=0.0, seed=0, par=False, tol=LOGIT_TOL_F32):
-    dec = make(lib, w, N, W, G, temperature=temperature, seed=seed, prompt_as_reference=par)
+def _teacher_forced(lib, w, p, N, W, G, steps, temperature=0.0, seed=0, par=False, tol=LOGIT_TOL_F32,
+                    pool_policy=la.FIFO, pool_cap=0, hits=None):
+    dec = make(lib, w, N, W, G, temperature=temperature, seed=seed, prompt_as_reference=par, pool_policy=pool_policy,
+               pool_cap=pool_cap)
     dec.prefill(p)
-    orc = la.Lookahead(w, N, W, G, temperature=temperature, seed=seed, prompt_as_reference=par, keep_logits=True)
+    orc = la.Lookahead(w, N, W, G, temperature=temperature, seed=seed, prompt_as_reference=par, keep_logits=True,
+                       pool_policy=pool_policy, pool_cap=pool_cap)
     checked = 0
     for t in range(steps):
         s0 = dec.export_state()
@@ -88,8 +91,16 @@ def _teacher_forced(lib, w, p, N, W, G, steps, temperature=0.0, seed=0, par=Fals
                 assert gnew == rec.new[j], f"step {t} column {j}"
             else:
                 assert lr[gnew] >= lr.max() - MARGIN
-        # pool: the oracle replays the GPU's own new tokens from the same start
-        pool = la.Pool.from_records(orc.pool.cap, s0["records"])
+        # pool: the oracle replays the GPU's own decisions from the same start:
+        # the winner (first candidate whose prefix is the accepted candidate
+        # tokens; candidates in the oracle's lookup order), then the harvest
+        pool = la.Pool.from_records(orc.pool.cap, s0["records"], orc.pool.policy)
+        a = len(acc) - 1
+        win = next((c for c, cand in enumerate(rec.cands) if a > 0 and list(cand[:a]) == acc[:a]), -1)
+        if win >= 0:
+            pool.use(s0["tokens"][-1], rec.cands[win])
+            if hits is not None:
+                hits.append(t)
         for key, suf in la.harvest(np.asarray(s0["window"]), [int(x) for x in s1["window"][N - 2]]):
             pool.insert(key, suf)
         assert pool.records() == s1["records"], f"step {t}: pool"
@@ -109,6 +120,30 @@ def test_step_teacher_forced_repetitive_prompt(lib, tiny_model):
     wl, w, _ = tiny_model
     p = np.tile(synth.uniform_tokens(8, wl.dims.vocab, seed=9), 5)
     assert _teacher_forced(lib, w, p, 4, 3, 4, steps=10, par=True) == 10
+
+
+@pytest.mark.parametrize("N,W,G,cap", [(4, 3, 4, 0), (4, 3, 2, 5), (3, 4, 3, 3)])
+def test_step_teacher_forced_lru_pool(lib, tiny_model, N, W, G, cap):
+    """LRU pool: candidates most recent first, the winner and repeated
+    harvests move to the most recent end; the pool after every step equals
+    the oracle's replay, and some steps do accept a candidate."""
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(6, wl.dims.vocab, seed=4), 6)
+    hits = []
+    assert _teacher_forced(lib, w, p, N, W, G, steps=12, par=True, pool_policy=la.LRU, pool_cap=cap, hits=hits) == 12
+    assert hits
+
+
+def test_generate_lru_pool_equals_autoregressive(lib, tiny_model):
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(6, wl.dims.vocab, seed=4), 6)
+    ar, margins = ar_with_margins(w, p, wl.new_tokens)
+    dec = make(lib, w, 4, 3, 2, prompt_as_reference=True, pool_policy=la.LRU, pool_cap=5)
+    out, steps = dec.generate(p, wl.new_tokens)
+    upto = compare_stream(out, ar, margins, MARGIN)
+    assert upto >= 16, f"first low-margin decision at {upto}"
+    assert steps < wl.new_tokens - 1     # some steps accepted more than one token
+    dec.close()
 
 
 def test_step_teacher_forced_sampling(lib, tiny_model):
