@@ -133,6 +133,9 @@ def gemm_source_fp(read=None) -> str:
     h = hashlib.sha256()
     for f in ("gemm.cu", "la_common.cuh", "la_kernels.h"):
         text = read(f) if read else open(os.path.join(csrc, f)).read()
+        if f == "la_kernels.h":
+            # the shared header's GEMM section only (the rest declares other kernels)
+            text = text[text.index("// " + "-" * 66 + " GEMMs"):text.index("// " + "-" * 66 + " elementwise")]
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
         text = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
