@@ -338,6 +338,22 @@ def run_ours(args, wl, rank, world, local_rank):
         ar_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_ar)
         log(f"autoregressive baseline: {ar_ms:.3f} ms/token")
 
+    # ---- prefill, reported on its own: la_prefill of the host prompt (prompt
+    # copy in, KV of every prompt token in 128-row chunks, first token back)
+    prefill_ms = None
+    if not args.ncu:
+        fresh()
+        n_pf = 3
+        ev_pf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_pf)]
+        sync()
+        for i in range(n_pf):
+            ev_pf[i][0].record(stream)
+            fresh()
+            ev_pf[i][1].record(stream)
+        sync()
+        prefill_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_pf)
+        log(f"prefill: {len(prompt)} tokens in {prefill_ms:.3f} ms")
+
     # ---- profiled pass (events around every GEMM / attention launch)
     pdec = e.Decoder(dw, wl.N, wl.W, wl.G, max_seq, stream=stream, profile=True, **kw)
     if not args.ncu:
@@ -403,6 +419,10 @@ def run_ours(args, wl, rank, world, local_rank):
             "note": "la_ar_step (one row per forward, same kernels and weights) timed on this GPU; random weights "
                     "accept A = 1 token per lookahead step, so the ratio is the step cost ratio, not the pages' "
                     "speedup on trained models"},
+        "prefill": None if prefill_ms is None else {
+            "tokens": len(prompt), "ms": prefill_ms, "tokens_per_s": len(prompt) / (prefill_ms * 1e-3),
+            "note": "la_prefill from a host prompt (copy in, 128-row chunks through the step kernels, each chunk "
+                    "streaming every weight once, first token read back); not part of value or ms_per_step"},
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and not args.ncu and world == 1:
