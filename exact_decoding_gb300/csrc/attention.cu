@@ -15,6 +15,7 @@
 //   in fixed order, then adds the row's in-step keys with an online softmax
 //   (warp-shuffle dot products) and writes the normalised output.
 #include <algorithm>
+#include <atomic>
 
 #include "la_kernels.h"
 
@@ -201,18 +202,32 @@ __global__ void __launch_bounds__(256) k_attn_final(const float *q, const T *kc,
     for (int j = 0; j < DPL; ++j) orow[j] = from_f32<T>(o[j] * inv);
 }
 
+// Kernel attributes are per device: bit d of `mask` says they are set on
+// device d.  True (with *bit = the current device's bit) while they still
+// have to be set there; a device index past 63 sets them on every call.
+static bool attrs_needed(const std::atomic<unsigned long long> &mask, unsigned long long *bit) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *bit = 0;
+        return true;
+    }
+    *bit = 1ull << dev;
+    return !(mask.load() & *bit);
+}
+
 template <typename T, int HD>
 static cudaError_t attention_launch_hd(const AttnArgs &a, cudaStream_t s) {
     constexpr int CH = kAttnChunk;
     if (a.nch > 0) {
         const size_t smem = (static_cast<size_t>(HD) * (CH + 4) + CH * HD + 32 * (HD + 1) + 32 * (CH + 1) + 64) *
                             sizeof(float);
-        static bool configured = false;
-        if (!configured) {
+        static std::atomic<unsigned long long> configured{0};
+        unsigned long long bit = 0;
+        if (attrs_needed(configured, &bit)) {
             cudaError_t e = cudaFuncSetAttribute(k_attn_prefix<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));
             if (e != cudaSuccess) return e;
-            configured = true;
+            configured.fetch_or(bit);
         }
         dim3 grid(a.nkv, a.nch);
         launch_k(k_attn_prefix<T, HD>, dim3(grid), dim3(256), smem, s, a.q, a.kc, a.vc,
@@ -757,14 +772,15 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
 template <int HD>
 static cudaError_t attention_umma_hd(const AttnUmmaParams &p, int cs, cudaStream_t s) {
     using Lay = AttnLayout<HD>;
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<unsigned long long> configured{0};
+    unsigned long long bit = 0;
+    if (attrs_needed(configured, &bit)) {
         cudaError_t e = cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(Lay::bytes));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(k_attn_umma<HD>, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured.fetch_or(bit);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cs, p.nkv * p.mtiles);

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -1069,6 +1070,29 @@ void capture_step(la_handle *h) {
 
 }  // namespace
 
+namespace {
+
+// Error word of la_gemm_bf16's kernels on the current device: one per device,
+// allocated on the first call there and kept until the process exits (a
+// kernel may only write its own device's word).
+cudaError_t gemm_err_word(unsigned **out) {
+    static std::mutex mu;
+    static unsigned *words[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!words[dev]) {
+        e = cudaMalloc(&words[dev], sizeof(unsigned));
+        if (e != cudaSuccess) return e;
+    }
+    *out = words[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
 extern "C" {
 
 int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
@@ -1279,8 +1303,8 @@ int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t o
     const int n_kb = (k + kBlockK - 1) / kBlockK;
     if (splits > n_kb) return fail(LA_ERR_INVALID_ARG, "splits > k / 64");
     if (splits > 1 && !workspace) return fail(LA_ERR_INVALID_ARG, "workspace required when splits > 1");
-    static unsigned *err = nullptr;
-    if (!err) CK(cudaMalloc(&err, sizeof(unsigned)));
+    unsigned *err = nullptr;
+    CK(gemm_err_word(&err));
     TcGemm g;
     std::memset(&g.p, 0, sizeof(g.p));
     const int bn = round_up(rows, 16);
