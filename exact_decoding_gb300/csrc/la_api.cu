@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -18,6 +19,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "../../include/la.h"
+#include "abi_guard.h"
 #include "la_kernels.h"
 
 using namespace la;
@@ -688,7 +690,7 @@ const char *la_last_error(void) { return g_last_error.c_str(); }
 
 static int la_prefill_impl(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token);
 
-int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opts, la_handle **out) {
+static int la_create_body(const la_model_dims *dims, const la_weights *w, const la_opts *opts, la_handle **out) {
     if (!dims || !w || !opts || !out) return fail(LA_ERR_INVALID_ARG, "null argument");
     *out = nullptr;
     const la_model_dims &D = *dims;
@@ -713,7 +715,8 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         !w->ffn_norm || !w->w_gate || !w->w_up || !w->w_down)
         return fail(LA_ERR_INVALID_ARG, "null weight pointer");
 
-    la_handle *h = new la_handle();
+    std::unique_ptr<la_handle> owner(new la_handle());   // freed on every early return
+    la_handle *h = owner.get();
     h->dims = D;
     h->opts = O;
     h->stream = static_cast<cudaStream_t>(O.cuda_stream);
@@ -763,7 +766,6 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     h->ldo_lm = h->tv * kTileM;
     h->lm_stride = static_cast<long long>(std::max(h->U, 1)) * h->ldo_lm;
     if (h->bf16 && M > kPrefillRows) {
-        delete h;
         return fail(LA_ERR_UNSUPPORTED, "bf16 models need 1 + (W+G)(N-1) <= 128");
     }
     h->embed = w->embed;
@@ -778,12 +780,10 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     if (!grab(h->attn_norm, w->attn_norm) || !grab(h->wq, w->wq) || !grab(h->wk, w->wk) || !grab(h->wv, w->wv) ||
         !grab(h->wo, w->wo) || !grab(h->ffn_norm, w->ffn_norm) || !grab(h->wg, w->w_gate) || !grab(h->wu, w->w_up) ||
         !grab(h->wd, w->w_down)) {
-        delete h;
         return fail(LA_ERR_INVALID_ARG, "null or misaligned per-layer weight pointer");
     }
     for (const void *p : {w->embed, w->final_norm, w->lm_head})
         if (reinterpret_cast<uintptr_t>(p) & 15) {
-            delete h;
             return fail(LA_ERR_INVALID_ARG, "weights must be 16-byte aligned");
         }
 
@@ -838,10 +838,7 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     A(h->alloc(&h->pent, nslots * h->cap * (h->N - 1)));
     if (rc == LA_OK && cudaMallocHost(&h->st_host, sizeof(SpecState)) != cudaSuccess)
         rc = fail(LA_ERR_OOM, "pinned host allocation failed");
-    if (rc != LA_OK) {
-        delete h;
-        return rc;
-    }
+    if (rc != LA_OK) return rc;
     cudaStream_t s = h->stream;
     // Static tables: rotary angles, step-row depths and in-step key lists.
     {
@@ -883,7 +880,6 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
             cudaMemcpy(h->vis_bits, bits.data(), bits.size() * sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess ||
             cudaMemcpy(h->used, used.data(), used.size() * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
             cudaMemcpy(h->iota, iota.data(), R * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
-            delete h;
             return fail(LA_ERR_CUDA, "uploading static tables failed");
         }
     }
@@ -893,7 +889,6 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         cudaMemsetAsync(h->fa, 0, ar * h->F * act, s) != cudaSuccess ||
         cudaMemsetAsync(h->xu, 0, ar * h->d * act, s) != cudaSuccess ||
         cudaMemsetAsync(h->st, 0, sizeof(SpecState), s) != cudaSuccess) {
-        delete h;
         return fail(LA_ERR_CUDA, "memset failed");
     }
     if (h->bf16) {
@@ -904,13 +899,11 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         h->vcs = h->kcs + static_cast<size_t>(h->L) * 2 * h->nkv * h->seq * h->hd;
         if (cudaMemsetAsync(h->cache, 0, cache_bytes, s) != cudaSuccess ||
             cudaMemsetAsync(h->qs, 0, static_cast<size_t>(2) * h->nkv * h->qv_pad * h->hd * 2, s) != cudaSuccess) {
-            delete h;
             return fail(LA_ERR_CUDA, "memset failed");
         }
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&h->nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            delete h;
             return fail(LA_ERR_CUDA, "device query failed");
         }
         AttnUmmaParams &ap = h->attn_proto;
@@ -930,7 +923,6 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
         ap.kc = h->kcs;
         ap.vc = h->vcs;
         if (!attention_umma_maps(ap, h->qs, h->kcs, h->vcs, h->L)) {
-            delete h;
             return fail(LA_ERR_CUDA, "tensor maps for the attention failed");
         }
     }
@@ -950,11 +942,8 @@ int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opt
     }
     if (rc == LA_OK) rc = reset_pool(h);
     if (rc == LA_OK && cudaStreamSynchronize(s) != cudaSuccess) rc = fail(LA_ERR_CUDA, "create sync failed");
-    if (rc != LA_OK) {
-        delete h;
-        return rc;
-    }
-    *out = h;
+    if (rc != LA_OK) return rc;
+    *out = owner.release();
     return LA_OK;
 }
 
@@ -965,7 +954,7 @@ void la_destroy(la_handle *h) {
     delete h;
 }
 
-int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token) {
+static int la_prefill_body(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token) {
     nvtxRangePushA("la_prefill");
     const int rc = la_prefill_impl(h, prompt, n, first_token);
     nvtxRangePop();
@@ -1095,7 +1084,7 @@ cudaError_t gemm_err_word(unsigned **out) {
 
 extern "C" {
 
-int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
+static int la_step_body(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     NvtxRange range("la_step");
     if (!h || !out_tokens || !out_n) return fail(LA_ERR_INVALID_ARG, "null argument");
     if (!h->prefilled) return fail(LA_ERR_STATE, "la_step before la_prefill");
@@ -1130,7 +1119,7 @@ int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     return LA_OK;
 }
 
-int la_ar_step(la_handle *h, int32_t *token) {
+static int la_ar_step_body(la_handle *h, int32_t *token) {
     NvtxRange range("la_ar_step");
     if (!h || !token) return fail(LA_ERR_INVALID_ARG, "null argument");
     if (!h->prefilled) return fail(LA_ERR_STATE, "la_ar_step before la_prefill");
@@ -1155,8 +1144,8 @@ int la_ar_step(la_handle *h, int32_t *token) {
     return LA_OK;
 }
 
-int la_generate(la_handle *h, const int32_t *prompt, int32_t n, int32_t max_new, int32_t *out, int32_t *out_n,
-                int32_t *n_steps) {
+static int la_generate_body(la_handle *h, const int32_t *prompt, int32_t n, int32_t max_new, int32_t *out,
+                            int32_t *out_n, int32_t *n_steps) {
     if (!h || !prompt || !out || max_new < 1) return fail(LA_ERR_INVALID_ARG, "bad argument");
     int32_t first = 0;
     int rc = la_prefill(h, prompt, n, &first);
@@ -1195,7 +1184,7 @@ int la_stats(const la_handle *h, la_stats_t *o) {
     return LA_OK;
 }
 
-int la_export_state(la_handle *h, la_state_t *stt) {
+static int la_export_state_body(la_handle *h, la_state_t *stt) {
     if (!h || !stt || !stt->tokens || !stt->window || (!stt->records && stt->records_cap > 0))
         return fail(LA_ERR_INVALID_ARG, "null argument");
     if (!h->prefilled) return fail(LA_ERR_STATE, "no state before la_prefill");
@@ -1236,7 +1225,7 @@ int la_export_state(la_handle *h, la_state_t *stt) {
     return LA_OK;
 }
 
-int la_import_state(la_handle *h, const la_state_t *stt) {
+static int la_import_state_body(la_handle *h, const la_state_t *stt) {
     if (!h || !stt || !stt->tokens || !stt->window || (stt->n_records > 0 && !stt->records))
         return fail(LA_ERR_INVALID_ARG, "null argument");
     const int n = stt->n_tokens;
@@ -1284,7 +1273,7 @@ int la_import_state(la_handle *h, const la_state_t *stt) {
     return LA_OK;
 }
 
-int la_debug_logits(la_handle *h, float *host, int32_t *rows, int32_t *vocab) {
+static int la_debug_logits_body(la_handle *h, float *host, int32_t *rows, int32_t *vocab) {
     if (!h || !rows || !vocab) return fail(LA_ERR_INVALID_ARG, "null argument");
     *rows = h->logits_rows;
     *vocab = h->V;
@@ -1296,8 +1285,8 @@ int la_debug_logits(la_handle *h, float *host, int32_t *rows, int32_t *vocab) {
     return LA_OK;
 }
 
-int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k, int32_t splits,
-                 float *workspace, void *stream) {
+static int la_gemm_bf16_body(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
+                             int32_t splits, float *workspace, void *stream) {
     if (!x || !w || !y || rows < 1 || rows > 256 || out < 1 || k < 8 || k % 8 || splits < 1)
         return fail(LA_ERR_INVALID_ARG, "bad GEMM arguments");
     const int n_kb = (k + kBlockK - 1) / kBlockK;
@@ -1330,6 +1319,47 @@ int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t o
     CK(tc_gemm_launch(g, s));
     if (splits > 1) CK(reduce_splits_launch(workspace, splits, g.p.split_stride, rows, out, y, s));
     return LA_OK;
+}
+
+// Exported entry points: each runs its body under abi_guard, so no C++
+// exception crosses the C ABI.
+int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opts, la_handle **out) {
+    return abi_guard("la_create", [&] { return la_create_body(dims, w, opts, out); });
+}
+
+int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token) {
+    return abi_guard("la_prefill", [&] { return la_prefill_body(h, prompt, n, first_token); });
+}
+
+int la_step(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
+    return abi_guard("la_step", [&] { return la_step_body(h, out_tokens, out_n); });
+}
+
+int la_ar_step(la_handle *h, int32_t *token) {
+    return abi_guard("la_ar_step", [&] { return la_ar_step_body(h, token); });
+}
+
+int la_generate(la_handle *h, const int32_t *prompt, int32_t n, int32_t max_new, int32_t *out, int32_t *out_n,
+                int32_t *n_steps) {
+    return abi_guard("la_generate", [&] { return la_generate_body(h, prompt, n, max_new, out, out_n, n_steps); });
+}
+
+int la_export_state(la_handle *h, la_state_t *stt) {
+    return abi_guard("la_export_state", [&] { return la_export_state_body(h, stt); });
+}
+
+int la_import_state(la_handle *h, const la_state_t *stt) {
+    return abi_guard("la_import_state", [&] { return la_import_state_body(h, stt); });
+}
+
+int la_debug_logits(la_handle *h, float *host, int32_t *rows, int32_t *vocab) {
+    return abi_guard("la_debug_logits", [&] { return la_debug_logits_body(h, host, rows, vocab); });
+}
+
+int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k, int32_t splits,
+                 float *workspace, void *stream) {
+    return abi_guard("la_gemm_bf16",
+                     [&] { return la_gemm_bf16_body(x, w, y, rows, out, k, splits, workspace, stream); });
 }
 
 }  // extern "C"

@@ -25,6 +25,7 @@
 #include <mutex>
 
 #include "../../include/la.h"
+#include "abi_guard.h"
 #include "la_kernels.h"
 
 static __device__ __align__(256) float g_noalloc_scratch[LA_NOALLOC_SCRATCH_FLOATS];
@@ -64,8 +65,8 @@ cudaError_t symbol_ptrs(DevicePtrs *out) {
 
 }  // namespace
 
-extern "C" int la_gemm_bf16_noalloc(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
-                                    int32_t splits, void *stream) {
+static int gemm_noalloc_body(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
+                             int32_t splits, void *stream) {
     using namespace la;
     if (!x || !w || !y || rows < 1 || rows > 256 || out < 1 || k < 8 || k % 8 || splits < 1)
         return set_last_error(LA_ERR_INVALID_ARG, "la_gemm_bf16_noalloc: bad arguments");
@@ -103,4 +104,10 @@ extern "C" int la_gemm_bf16_noalloc(const void *x, const void *w, float *y, int3
     if (splits > 1 && reduce_splits_launch(p.scratch, splits, g.p.split_stride, rows, out, y, s) != cudaSuccess)
         return set_last_error(LA_ERR_CUDA, "la_gemm_bf16_noalloc: reduce launch failed");
     return LA_OK;
+}
+
+extern "C" int la_gemm_bf16_noalloc(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
+                                    int32_t splits, void *stream) {
+    return la::abi_guard("la_gemm_bf16_noalloc",
+                         [&] { return gemm_noalloc_body(x, w, y, rows, out, k, splits, stream); });
 }
