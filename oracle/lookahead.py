@@ -65,6 +65,13 @@ Readings taken where the pages are open:
      the list is full the least recently used entry is dropped.  Lookup
      returns the G most recently used entries, most recent first.  Under
      FIFO (R6) neither a use nor a repeated harvest changes the order.
+  R16 LFU pool (the same passage names frequency-based eviction).  The uses
+     are R15's.  Each entry carries a use count (0 when it enters) and the
+     time of its last use or entry; each key's list is ordered by (count,
+     time) ascending.  A new suffix into a full list first drops the head
+     (fewest uses, the oldest among equals), then enters.  Lookup returns
+     the G entries at the tail end, highest (count, time) first.  The counts
+     are part of the pool's state, so a snapshot carries them.
 """
 from __future__ import annotations
 
@@ -156,42 +163,62 @@ def step_mask(N: int, W: int, G: int) -> np.ndarray:
 # n-gram pool (reading R6)
 # --------------------------------------------------------------------------
 
-FIFO, LRU = "fifo", "lru"
+FIFO, LRU, LFU = "fifo", "lru", "lfu"
 
 
 class Pool:
     """First token -> list of distinct (N-1)-token suffixes, in eviction
     order (the next to be dropped first): oldest first under FIFO (R6),
-    least recently used first under LRU (R15)."""
+    least recently used first under LRU (R15), fewest uses first under LFU
+    (R16)."""
 
     def __init__(self, cap: int, policy: str = FIFO):
-        assert policy in (FIFO, LRU)
+        assert policy in (FIFO, LRU, LFU)
         self.cap = cap
         self.policy = policy
         self.lists: Dict[int, List[Tuple[int, ...]]] = {}
+        self.clock = 0                                            # LFU: event counter
+        self.meta: Dict[Tuple[int, Tuple[int, ...]], List[int]] = {}   # LFU: (key, suffix) -> [count, time]
 
-    def insert(self, key: int, suffix: Sequence[int]) -> None:
-        suffix = tuple(int(t) for t in suffix)
-        lst = self.lists.setdefault(int(key), [])
+    def _lfu_order(self, key: int) -> None:
+        self.lists[key].sort(key=lambda s: tuple(self.meta[(key, s)]))
+
+    def insert(self, key: int, suffix: Sequence[int], uses: int = 0) -> None:
+        key, suffix = int(key), tuple(int(t) for t in suffix)
+        lst = self.lists.setdefault(key, [])
         if suffix in lst:
             self.use(key, suffix)
+            return
+        if self.policy == LFU:
+            self.clock += 1
+            if len(lst) == self.cap:
+                del self.meta[(key, lst.pop(0))]
+            lst.append(suffix)
+            self.meta[(key, suffix)] = [uses, self.clock]
+            self._lfu_order(key)
             return
         lst.append(suffix)
         if len(lst) > self.cap:
             lst.pop(0)
 
     def use(self, key: int, suffix: Sequence[int]) -> None:
-        """LRU: move a present suffix to the most recent end (FIFO: no-op)."""
-        if self.policy != LRU:
-            return
-        suffix = tuple(int(t) for t in suffix)
-        lst = self.lists[int(key)]
-        lst.remove(suffix)
-        lst.append(suffix)
+        """LRU: move a present suffix to the most recent end.  LFU: count the
+        use and re-order.  FIFO: no-op."""
+        key, suffix = int(key), tuple(int(t) for t in suffix)
+        lst = self.lists[key]
+        if self.policy == LRU:
+            lst.remove(suffix)
+            lst.append(suffix)
+        elif self.policy == LFU:
+            self.clock += 1
+            m = self.meta[(key, suffix)]
+            m[0] += 1
+            m[1] = self.clock
+            self._lfu_order(key)
 
     def lookup(self, key: int, G: int) -> List[Tuple[int, ...]]:
         lst = list(self.lists.get(int(key), []))
-        if self.policy == LRU:
+        if self.policy in (LRU, LFU):
             lst.reverse()
         return lst[:G]
 
@@ -199,16 +226,24 @@ class Pool:
         """Canonical form: keys ascending, each key's suffixes in eviction order."""
         return [(k, s) for k in sorted(self.lists) for s in self.lists[k]]
 
+    def use_counts(self) -> List[int]:
+        """LFU: the use count of each entry of records(), in the same order."""
+        return [self.meta[(k, s)][0] for k, s in self.records()]
+
     def copy(self) -> "Pool":
         p = Pool(self.cap, self.policy)
         p.lists = {k: list(v) for k, v in self.lists.items()}
+        p.clock = self.clock
+        p.meta = {k: list(v) for k, v in self.meta.items()}
         return p
 
     @staticmethod
-    def from_records(cap: int, records, policy: str = FIFO) -> "Pool":
+    def from_records(cap: int, records, policy: str = FIFO, uses=None) -> "Pool":
+        """Rebuild a pool from records in eviction order (LFU: with their use
+        counts; entry times follow the record order, which keeps it)."""
         p = Pool(cap, policy)
-        for k, s in records:
-            p.insert(k, s)
+        for i, (k, s) in enumerate(records):
+            p.insert(k, s, uses[i] if uses is not None else 0)
         return p
 
 
@@ -457,15 +492,15 @@ class Lookahead:
                 self.pool.insert(key, suf)
         return y1
 
-    def load_state(self, tokens: Sequence[int], window: np.ndarray, pool_records) -> None:
-        """Start from a given committed sequence, window and pool; the prefix
-        KV is recomputed from the tokens."""
+    def load_state(self, tokens: Sequence[int], window: np.ndarray, pool_records, pool_uses=None) -> None:
+        """Start from a given committed sequence, window and pool (LFU: with
+        the entries' use counts); the prefix KV is recomputed from the tokens."""
         self.tokens = [int(t) for t in tokens]
         P = self.P
         _, self.cache = decoder.forward(self.w, self.tokens[:P], np.arange(P), decoder.causal_mask(0, P),
                                         dtype=self.dtype, logit_rows=[P - 1])
         self.window = np.array(window, dtype=np.int64).reshape(self.N - 1, self.W)
-        self.pool = Pool.from_records(self.pool.cap, pool_records, self.pool.policy)
+        self.pool = Pool.from_records(self.pool.cap, pool_records, self.pool.policy, pool_uses)
 
     # one step -----------------------------------------------------------
     def step_inputs(self):

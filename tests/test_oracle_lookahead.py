@@ -186,6 +186,115 @@ def test_lru_pool_lossless_and_replay(tiny, N, W, G, cap):
     assert o.pool.records() == ref.records()
 
 
+def test_pool_lfu_hand_example():
+    """Reading R16 worked by hand: uses raise an entry's count; a full list
+    drops the entry with the fewest uses (the oldest among equals) before the
+    new one enters; lookup is most used first."""
+    p = la.Pool(cap=3, policy=la.LFU)
+    p.insert(7, (1, 2))
+    p.insert(7, (3, 4))
+    p.insert(7, (5, 6))
+    p.insert(7, (1, 2))            # met again: (1, 2) has 1 use
+    p.use(7, (3, 4))
+    p.use(7, (3, 4))               # (3, 4) has 2 uses
+    assert p.records() == [(7, (5, 6)), (7, (1, 2)), (7, (3, 4))]
+    assert p.use_counts() == [0, 1, 2]
+    p.insert(7, (8, 9))            # full: (5, 6) (no uses) leaves, (8, 9) enters with none
+    assert p.lookup(7, 10) == [(3, 4), (1, 2), (8, 9)]
+    p.insert(7, (0, 1))            # (8, 9) is now the least used: it leaves at once
+    assert p.lookup(7, 10) == [(3, 4), (1, 2), (0, 1)]
+    p.use(7, (0, 1))               # one use each for (0, 1) and (1, 2); (0, 1) more recent
+    assert p.lookup(7, 2) == [(3, 4), (0, 1)]
+    p.insert(7, (2, 2))            # (1, 2): 1 use, older than (0, 1)
+    assert p.records() == [(7, (2, 2)), (7, (0, 1)), (7, (3, 4))]
+    assert p.use_counts() == [0, 1, 2]
+
+
+class _StampLFU:
+    """LFU written another way: every entry carries (uses, time of last use
+    or entry); a full key drops the entry with the smallest pair, found by a
+    search, and the list is the entries by ascending pair."""
+
+    def __init__(self, cap):
+        self.cap, self.t, self.ent = cap, 0, {}
+
+    def touch(self, key, suf):
+        self.t += 1
+        ent = self.ent.setdefault(key, {})
+        if suf in ent:
+            ent[suf] = (ent[suf][0] + 1, self.t)
+            return
+        if len(ent) == self.cap:
+            del ent[min(ent, key=ent.get)]
+        ent[suf] = (0, self.t)
+
+    def records(self):
+        return [(k, s) for k in sorted(self.ent) for s in sorted(self.ent[k], key=self.ent[k].get)]
+
+    def uses(self):
+        return [self.ent[k][s][0] for k, s in self.records()]
+
+
+@pytest.mark.parametrize("cap,seed", [(1, 0), (2, 1), (3, 2), (5, 3)])
+def test_pool_lfu_equals_search_model(cap, seed):
+    rng = np.random.default_rng(seed)
+    p, ref = la.Pool(cap, la.LFU), _StampLFU(cap)
+    for _ in range(400):
+        key, suf = int(rng.integers(0, 3)), (int(rng.integers(0, 4)), int(rng.integers(0, 3)))
+        if rng.random() < 0.3 and p.lists.get(key):
+            suf = p.lists[key][int(rng.integers(0, len(p.lists[key])))]
+            p.use(key, suf)
+        else:
+            p.insert(key, suf)
+        ref.touch(key, suf)
+        assert p.records() == ref.records()
+        assert p.use_counts() == ref.uses()
+    # a snapshot (records in eviction order with their counts) rebuilds the same pool
+    q = la.Pool.from_records(cap, p.records(), la.LFU, p.use_counts())
+    assert q.records() == p.records() and q.use_counts() == p.use_counts()
+    for key in range(3):
+        assert q.lookup(key, 2) == p.lookup(key, 2)
+
+
+def test_pool_policies_agree_at_cap_one():
+    """With one suffix per key every policy keeps the last suffix seen."""
+    rng = np.random.default_rng(5)
+    pools = [la.Pool(1, pol) for pol in (la.FIFO, la.LRU, la.LFU)]
+    for _ in range(300):
+        key, suf = int(rng.integers(0, 4)), (int(rng.integers(0, 3)),)
+        for p in pools:
+            p.insert(key, suf)
+        assert pools[0].records() == pools[1].records() == pools[2].records()
+
+
+@pytest.mark.parametrize("N,W,G,cap", [(4, 3, 4, 0), (4, 3, 2, 5), (3, 4, 3, 3)])
+def test_lfu_pool_lossless_and_replay(tiny, N, W, G, cap):
+    """With the LFU pool greedy lookahead still equals greedy autoregressive
+    decoding, and the pool after the run equals the search model fed the
+    prompt's n-grams, then per step the winner's use and the harvest."""
+    wl, w, _ = tiny
+    chunk = synth.uniform_tokens(6, wl.dims.vocab, seed=4)
+    p = np.tile(chunk, 5)
+    ar = la.generate_ar(w, p, 40)
+    o = la.Lookahead(w, N, W, G, prompt_as_reference=True, pool_cap=cap, pool_policy=la.LFU)
+    out, _ = o.generate(p, 40)
+    assert out == ar
+    ref = _StampLFU(o.pool.cap)
+    for i in range(len(p) - N + 1):
+        ref.touch(int(p[i]), tuple(int(t) for t in p[i + 1:i + N]))
+    used = 0
+    for rec in o.history:
+        assert rec.cands == [s for k, s in reversed(ref.records()) if k == rec.o][:G]
+        if rec.winner >= 0:
+            ref.touch(rec.o, rec.cands[rec.winner])
+            used += 1
+        for j in range(W):
+            ref.touch(int(rec.window_before[0, j]),
+                      tuple(int(rec.window_before[k, j]) for k in range(1, N - 1)) + (rec.new[j],))
+    assert used > 0
+    assert o.pool.records() == ref.records() and o.pool.use_counts() == ref.uses()
+
+
 @pytest.mark.parametrize("N,W,G,par", [(3, 4, 4, False), (2, 3, 3, False), (4, 2, 5, False),
                                        (5, 3, 0, False), (3, 1, 2, True), (4, 4, 4, True)])
 def test_lossless_vs_autoregressive(tiny, N, W, G, par):
