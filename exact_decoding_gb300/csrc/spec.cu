@@ -82,7 +82,9 @@ __device__ int pool_find(const SpecDev &d, int key, int lane) {
 }
 
 // Ring entry `i` (0 = head) of `slot` moves to the tail; entries i+1..cnt-1
-// move one place towards the head.  Lane l holds list entry l (cap <= 32).
+// move one place towards the head.  Lane l holds list entry l (cap <= 32)
+// in registers (N - 1 <= 7 tokens); `i` and the counts are warp-uniform, so
+// the early return leaves no lane behind in the shuffles.
 __device__ void pool_move_to_tail_warp(const SpecDev &d, int slot, int i, int lane) {
     const int L = d.N - 1, cap = d.cap;
     const int cnt = d.pcnt[slot], head = d.phead[slot];
