@@ -208,21 +208,27 @@ def run_reference(args, wl):
     import synth
     weights = synth.model_weights(wl.dims, wl.seed, layers=list(range(min(wl.dims.n_layers, args.steps + args.warmup))))
     prompt = synth.prompt(wl)
-    times = []
+    times, walls = [], []
     for i in range(args.warmup + args.steps):
         layer = i % wl.dims.n_layers
         if weights["layers"][layer] is None:
             weights["layers"][layer] = synth.layer_weights(wl.dims, layer, wl.seed)
+        tw = time.perf_counter()
         t1, t0 = oracle_step_sample(weights, wl, prompt, layer)
+        tw = time.perf_counter() - tw
         if i >= args.warmup:
             times.append(extrapolated_step_seconds(t1, t0, wl.dims.n_layers))
+            walls.append(tw)
     step_s = statistics.mean(times)
     # Tokens per step: a sampled step does not verify, so count the floor the
-    # method guarantees (A = 1 committed token per step).
+    # method guarantees (A = 1 committed token per step).  ms_per_step is the
+    # wall time a sampled step really took here; the value scales the sample
+    # to a whole step (all layers), reported as extrapolated_ms_per_step.
     value = 1.0 / step_s
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "committed tokens/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": statistics.mean(walls) * 1e3, "extrapolated_ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl.name, "prompt_len": wl.prompt_len, "N": wl.N, "W": wl.W,
                                         "G": wl.G, "rows_per_step": wl.M},
@@ -262,10 +268,10 @@ def run_ours(args, wl, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     t = time.perf_counter()
-    weights = synth.model_weights(wl.dims, wl.seed)
+    weights = synth.lazy_model_weights(wl.dims, wl.seed)   # layers generated while they are uploaded
     prompt = synth.prompt(wl)
-    log(f"weights generated in {time.perf_counter() - t:.1f} s")
     dw = e.DeviceWeights(weights)
+    log(f"weights generated and uploaded in {time.perf_counter() - t:.1f} s ({dw.nbytes() / 1e9:.1f} GB)")
     stream = torch.cuda.Stream()
     max_seq = wl.prompt_len + wl.new_tokens + wl.M + 8 * wl.N + 64
     kw = dict(temperature=wl.temperature, seed=wl.seed, prompt_as_reference=wl.prompt_as_reference)
@@ -288,6 +294,7 @@ def run_ours(args, wl, rank, world, local_rank):
         sync()
         e2e_s = time.perf_counter() - t0
         e2e_tps = len(toks) / e2e_s
+        gst = dec.stats()          # bytes the library copied in and out during that generation
     log(f"e2e: {len(toks)} tokens in {gen_steps} steps, {e2e_s:.3f} s")
 
     # ---- device-timed steps
@@ -376,7 +383,9 @@ def run_ours(args, wl, rank, world, local_rank):
     d = wl.dims
     act = 2 if d.dtype == "bf16" else 4
     weight_bytes = sum(t.numel() * t.element_size() for t in dw._keep if hasattr(t, "numel")) - d.vocab * d.d_model * act
-    kv_per_tok = 2 * d.n_layers * d.n_kv_heads * d.head_dim * 4   # K, V as fp32 or bf16 (hi, lo): 4 bytes each
+    # Algorithmic K/V bytes per token: K and V of every layer at the weights'
+    # element size (the cache's extra precision planes are not counted).
+    kv_per_tok = 2 * d.n_layers * d.n_kv_heads * d.head_dim * act
     mean_P = statistics.mean(prefixes)
     step_bytes = weight_bytes + mean_P * kv_per_tok + wl.M * d.d_model * act + wl.N * kv_per_tok
     peak, peak_kind = peaks()
@@ -392,16 +401,21 @@ def run_ours(args, wl, rank, world, local_rank):
         "config": {"workload": wl.name, "prompt_len": wl.prompt_len, "N": wl.N, "W": wl.W, "G": wl.G,
                    "rows_per_step": wl.M, "new_tokens": wl.new_tokens, "temperature": wl.temperature,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (13.2 GB of weights streamed per step)"},
+                   "l2": f"inputs larger than L2 ({weight_bytes / 1e9:.1f} GB of weights streamed per step)"},
         "step_stats": {"accepted_per_step": accepted / args.steps, "p50_ms": statistics.median(step_ms),
                        "p90_ms": sorted(step_ms)[int(0.9 * (len(step_ms) - 1))], "mean_prefix": mean_P,
                        "step_tokens_per_s": wl.M / (ms_per_step * 1e-3)},
-        "e2e": {"value": e2e_tps, "unit": "committed tokens/s (la_generate, prefill included)",
-                "h2d_bytes_per_step": (wl.prompt_len * 4 + (wl.N - 1) * wl.W * 4) / max(gen_steps, 1),
-                "d2h_bytes_per_step": 64.0 * (gen_steps + 1) / max(gen_steps, 1) + 4.0,
-                "tokens": len(toks), "steps": gen_steps, "seconds": e2e_s},
+        "e2e": None if args.ncu else {
+            "value": e2e_tps, "unit": "committed tokens/s (la_generate, prefill included)",
+            "h2d_bytes_per_step": gst["h2d_bytes"] / max(gen_steps, 1),
+            "d2h_bytes_per_step": gst["d2h_bytes"] / max(gen_steps, 1),
+            "bytes_counted_by": "la_stats h2d_bytes / d2h_bytes over the timed la_generate (prompt and initial "
+                                "window in; the step state with the accepted tokens out, once per step and once "
+                                "for the prefill), divided by its steps",
+            "tokens": len(toks), "steps": gen_steps, "seconds": e2e_s},
         "gpu_launches": int(launches),
-        "roofline": {"bound": "hbm", "kernel": "k_gemm_tc2 (2-SM tcgen05 projection GEMM, all launches of a step)",
+        "roofline": {"bound": "hbm", "kernel": "k_gemm_tc2 (2-SM tcgen05 projection GEMM, all launches of a step; "
+                               "algorithmic bytes = the weights each launch streams)",
                      "achieved": gemm_gbs, "peak": peak, "unit": "GB/s",
                      "frac": (gemm_gbs / peak) if gemm_gbs else None, "traffic": gemm_traffic(),
                      "peak_source": peak_kind, "launch_ms": pst["gemm_ms"] / max(pst["gemm_launches"], 1),

@@ -18,6 +18,7 @@
 //
 // fp32 path -- a plain SIMT kernel (fp32 FMA, no tf32) for fp32 models.
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <vector>
 
@@ -419,15 +420,24 @@ int tc_gemm2_stages() {
     return static_cast<int>((200 * 1024) / (2 * kTileM * kBlockK * 2));   // 6
 }
 
-static cudaError_t gemm2_smem_attr() {
-    static int done = 0;
-    if (done) return cudaSuccess;
+// Raise a kernel's dynamic shared-memory limit to the device's opt-in
+// maximum.  Function attributes are per device, so `done` keeps one bit per
+// device index (indices past 63 set the attribute on every call).
+static cudaError_t smem_attr_per_device(const void *fn, std::atomic<unsigned long long> &done) {
     int dev = 0, mx = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc2, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    if (e == cudaSuccess) done = 1;
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load() & bit)) return cudaSuccess;
+    e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) done.fetch_or(bit);
     return e;
+}
+
+static cudaError_t gemm2_smem_attr() {
+    static std::atomic<unsigned long long> done{0};
+    return smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2), done);
 }
 
 int tc_gemm2_max_pairs() {
@@ -510,17 +520,10 @@ int tc_gemm_stages_for(int bn) {
     return s > 8 ? 8 : (s < 2 ? 2 : s);
 }
 
-// Raise the kernel's dynamic shared-memory limit once to the device's opt-in
-// maximum; every plan then launches under it.
+// The 1-SM kernel's limit, per device like the 2-SM kernel's.
 static cudaError_t gemm_smem_attr() {
-    static int done = 0;
-    if (done) return cudaSuccess;
-    int dev = 0, mx = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
-    if (e == cudaSuccess) done = 1;
-    return e;
+    static std::atomic<unsigned long long> done{0};
+    return smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc), done);
 }
 
 int tc_gemm_ctas_per_sm(int bn, int stages) {
@@ -562,6 +565,25 @@ cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s) {
     cudaError_t e = gemm_smem_attr();
     if (e != cudaSuccess) return e;
     launch_k(k_gemm_tc, dim3(g.grid), dim3(192), g.smem, s, g.p);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ bounded-wait self-test
+// One thread waits, through the same mbar_wait as every kernel of the
+// library, on a barrier that nothing arrives at.  The wait gives up after
+// limit_ns, sets ERR_TIMEOUT_SELFTEST in *err (and in *err2 when given) and
+// the kernel returns: the failure path of an in-kernel wait, exercised
+// without a fault or an endless loop.  No TMA or MMA is in flight.
+__global__ void k_wait_selftest(unsigned *err, unsigned *err2, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    if (!mbar_wait(b, 0, err, ERR_TIMEOUT_SELFTEST, limit_ns) && err2) atomicOr(err2, ERR_TIMEOUT_SELFTEST);
+}
+
+cudaError_t wait_selftest_launch(unsigned *err, unsigned *err2, unsigned long long limit_ns, cudaStream_t s) {
+    k_wait_selftest<<<1, 32, 0, s>>>(err, err2, limit_ns);
     return cudaGetLastError();
 }
 

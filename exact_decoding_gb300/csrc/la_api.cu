@@ -136,6 +136,7 @@ struct la_handle {
     bool prefilled = false;
     int P = 0;
     int64_t steps = 0, generated = 0;
+    int64_t h2d_bytes = 0, d2h_bytes = 0;   // host <-> device copies since la_prefill
     int last_A = 0, last_g = 0, logits_rows = 0;
 
     ~la_handle() {
@@ -270,11 +271,14 @@ uint64_t splitmix64(uint64_t x) {
 }
 
 // ------------------------------------------------------------------ GEMM dispatch
+// Algorithmic bytes of one projection launch: its weights, read once.  The
+// input rows and outputs (about 2% of the weight bytes at M = 121) and the
+// extra precision planes are not counted.
 double gemm_bytes(const la_handle *h, Kind kind, int nrows) {
+    (void)nrows;
     const int K = kind == OPROJ ? h->qd : kind == DOWN ? h->F : h->d;
     const int out = kind == QKV ? h->qkv_out : kind == GATEUP ? 2 * h->F : h->d;
-    // weights once + input rows (fp32, or its bf16 hi/lo pair) + fp32 output
-    return static_cast<double>(out) * K * h->act + 4.0 * nrows * K + 4.0 * nrows * out;
+    return static_cast<double>(out) * K * h->act;
 }
 
 int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
@@ -337,7 +341,7 @@ int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
 int run_lm_head(la_handle *h, int nrows, bool step) {
     h->launches += 1;
     const int pe = step ? h->prof_begin() : -1;
-    const double bytes = static_cast<double>(h->V) * h->d * h->act + 4.0 * nrows * h->d + 4.0 * nrows * h->V;
+    const double bytes = static_cast<double>(h->V) * h->d * h->act;   // the lm_head, read once
     if (h->bf16) {
         TcGemm g = h->plan_lm;
         g.p.nrows = nrows;
@@ -384,8 +388,9 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         int rc;
         if ((rc = run_gemm(h, mode, QKV, l, nrows)) != LA_OK) return rc;
         const long long ss_qkv = static_cast<long long>(h->R) * h->ldo[QKV];
-        const double attn_bytes =
-            (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * 4.0 + 4.0 * nrows * h->qd + 4.0 * nrows * h->qd;
+        // Algorithmic bytes of one attention launch: the prefix and step K/V
+        // once at the weights' element size (the hi/lo planes double that).
+        const double attn_bytes = (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * h->act;
         if (h->bf16) {
             AttnUmmaParams ap = h->attn_proto;
             ap.part = h->part;
@@ -997,6 +1002,8 @@ static int la_prefill_impl(la_handle *h, const int32_t *prompt, int32_t n, int32
     h->launches = 0;
     h->ev_used = 0;
     for (int c = 0; c < 4; ++c) h->prof_ms[c] = h->prof_bytes[c] = 0, h->prof_launches[c] = 0;
+    h->h2d_bytes = static_cast<int64_t>(n) * sizeof(int32_t) + static_cast<int64_t>(win.size()) * sizeof(int);
+    h->d2h_bytes = sizeof(SpecState);
     return LA_OK;
 }
 
@@ -1064,17 +1071,24 @@ namespace {
 // Error word of la_gemm_bf16's kernels on the current device: one per device,
 // allocated on the first call there and kept until the process exits (a
 // kernel may only write its own device's word).
-cudaError_t gemm_err_word(unsigned **out) {
+// With create = false, *out stays nullptr while the device has no word yet.
+cudaError_t gemm_err_word(unsigned **out, bool create = true) {
     static std::mutex mu;
     static unsigned *words[64] = {};
+    *out = nullptr;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
-    if (!words[dev]) {
+    if (!words[dev] && create) {
         e = cudaMalloc(&words[dev], sizeof(unsigned));
-        if (e != cudaSuccess) return e;
+        if (e == cudaSuccess) e = cudaMemset(words[dev], 0, sizeof(unsigned));
+        if (e != cudaSuccess) {
+            if (words[dev]) cudaFree(words[dev]);
+            words[dev] = nullptr;
+            return e;
+        }
     }
     *out = words[dev];
     return cudaSuccess;
@@ -1113,6 +1127,7 @@ static int la_step_body(la_handle *h, int32_t *out_tokens, int32_t *out_n) {
     h->P = st.P;
     h->steps += 1;
     h->generated += st.A;
+    h->d2h_bytes += sizeof(SpecState);
     h->last_A = st.A;
     h->last_g = st.g;
     h->logits_rows = h->U;
@@ -1140,6 +1155,7 @@ static int la_ar_step_body(la_handle *h, int32_t *token) {
     *token = h->st_host->o;
     h->P = P + 1;
     h->generated += 1;
+    h->d2h_bytes += sizeof(SpecState);
     h->logits_rows = 1;
     return LA_OK;
 }
@@ -1181,6 +1197,8 @@ int la_stats(const la_handle *h, la_stats_t *o) {
     o->kernel_launches = h->launches;
     o->elem_ms = h->prof_ms[2];
     o->spec_ms = h->prof_ms[3];
+    o->h2d_bytes = h->h2d_bytes;
+    o->d2h_bytes = h->d2h_bytes;
     return LA_OK;
 }
 
@@ -1321,6 +1339,38 @@ static int la_gemm_bf16_body(const void *x, const void *w, float *y, int32_t row
     return LA_OK;
 }
 
+static int la_gemm_status_body(void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned *w = nullptr, bits = 0, bits_na = 0;
+    CK(gemm_err_word(&w, false));
+    if (w) {
+        CK(cudaMemcpyAsync(&bits, w, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+        CK(cudaMemsetAsync(w, 0, sizeof(unsigned), s));
+    }
+    CK(noalloc_err_take(s, &bits_na));
+    CK(cudaStreamSynchronize(s));
+    if (bits | bits_na)
+        return fail(LA_ERR_DEVICE_TIMEOUT,
+                    "a bounded wait of an earlier GEMM call gave up (error bits 0x%x la_gemm_bf16, 0x%x "
+                    "la_gemm_bf16_noalloc); that call's output is void", bits, bits_na);
+    return LA_OK;
+}
+
+static int la_selftest_timeout_body(la_handle *h, int64_t limit_ns, void *stream) {
+    if (limit_ns < 1000 || limit_ns > static_cast<int64_t>(kWaitNs))
+        return fail(LA_ERR_INVALID_ARG, "limit_ns must lie in [1000, %llu]", static_cast<unsigned long long>(kWaitNs));
+    const unsigned long long lim = static_cast<unsigned long long>(limit_ns);
+    if (h) {
+        CK(wait_selftest_launch(&h->st->err, nullptr, lim, h->stream));
+        return LA_OK;
+    }
+    unsigned *w = nullptr, *wna = nullptr;
+    CK(gemm_err_word(&w));
+    CK(noalloc_err_word(&wna));
+    CK(wait_selftest_launch(w, wna, lim, static_cast<cudaStream_t>(stream)));
+    return LA_OK;
+}
+
 // Exported entry points: each runs its body under abi_guard, so no C++
 // exception crosses the C ABI.
 int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opts, la_handle **out) {
@@ -1360,6 +1410,14 @@ int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t o
                  float *workspace, void *stream) {
     return abi_guard("la_gemm_bf16",
                      [&] { return la_gemm_bf16_body(x, w, y, rows, out, k, splits, workspace, stream); });
+}
+
+int la_gemm_status(void *stream) {
+    return abi_guard("la_gemm_status", [&] { return la_gemm_status_body(stream); });
+}
+
+int la_selftest_timeout(la_handle *h, int64_t limit_ns, void *stream) {
+    return abi_guard("la_selftest_timeout", [&] { return la_selftest_timeout_body(h, limit_ns, stream); });
 }
 
 }  // extern "C"

@@ -20,6 +20,7 @@ enum : unsigned {
     ERR_TIMEOUT_ACCUM = 4u,    // epilogue waited too long for the accumulator
     ERR_POOL = 8u,             // pool probe found no slot (table full)
     ERR_TIMEOUT_ATTN = 16u,    // attention waited too long for a TMA load or an MMA
+    ERR_TIMEOUT_SELFTEST = 32u,  // the bounded-wait self-test kernel gave up (as it is meant to)
 };
 
 constexpr int kMaxSeg = 3;           // weight matrices sharing one GEMM launch
@@ -91,14 +92,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: true when the phase completed, false (and err |= bit) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err, unsigned bit) {
+// Bounded wait: true when the phase completed, false (and err |= bit) once
+// limit_ns of wall-clock time have passed without it.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err, unsigned bit,
+                                          uint64_t limit_ns = kWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (;;) {
         for (int i = 0; i < 256; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitNs) {
+        if (globaltimer() - t0 > limit_ns) {
             atomicOr(err, bit);
             return false;
         }

@@ -87,6 +87,14 @@ cudaError_t simt_gemm_launch(const SimtGemmParams &p, int total_f, cudaStream_t 
 cudaError_t reduce_splits_launch(const float *part, int splits, long long stride, int rows, int cols, float *y,
                                  cudaStream_t s);
 
+// One CTA whose bounded mbarrier wait (on a barrier nothing arrives at) gives
+// up after limit_ns and ORs ERR_TIMEOUT_SELFTEST into *err (and *err2 if set).
+cudaError_t wait_selftest_launch(unsigned *err, unsigned *err2, unsigned long long limit_ns, cudaStream_t s);
+// Error word of la_gemm_bf16_noalloc on the current device: its address
+// (nullptr while the device has made no call), or read-and-clear on stream s.
+cudaError_t noalloc_err_word(unsigned **out);
+cudaError_t noalloc_err_take(cudaStream_t s, unsigned *bits);
+
 // ------------------------------------------------------------------ elementwise
 // T is the weight type; activations written as T go through store_act
 // (fp32, or a bf16 hi/lo pair whose lo plane is lo_off elements later).

@@ -20,7 +20,11 @@
 // In host code the symbol names a host-side stand-in, not a device address.
 // So the first call on each device looks the address up with
 // cudaGetSymbolAddress, with that device current, and caches it; that first
-// call should come before any stream capture.
+// call should come before any stream capture.  The cache lives as long as
+// the process: after a cudaDeviceReset the cached addresses are stale.
+//
+// A bounded wait inside the kernel that gives up sets a bit in a second
+// device word of this file; la_gemm_status reads and clears it.
 #include <cstring>
 #include <mutex>
 
@@ -64,6 +68,31 @@ cudaError_t symbol_ptrs(DevicePtrs *out) {
 }
 
 }  // namespace
+
+// Address of this device's error word, or nullptr while the device has made
+// no call (nothing can have set it then).
+cudaError_t la::noalloc_err_word(unsigned **out) {
+    *out = nullptr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mu);
+    *out = g_ptrs[dev].err;
+    return cudaSuccess;
+}
+
+// Read this device's error word into *bits and clear it, both on stream s
+// (the caller synchronises s before reading *bits).  No allocation.
+cudaError_t la::noalloc_err_take(cudaStream_t s, unsigned *bits) {
+    *bits = 0;
+    unsigned *w = nullptr;
+    cudaError_t e = noalloc_err_word(&w);
+    if (e != cudaSuccess || !w) return e;
+    e = cudaMemcpyAsync(bits, w, sizeof(unsigned), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w, 0, sizeof(unsigned), s);
+    return e;
+}
 
 static int gemm_noalloc_body(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
                              int32_t splits, void *stream) {

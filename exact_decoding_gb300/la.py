@@ -56,7 +56,8 @@ class la_stats_t(ctypes.Structure):
                 ("last_candidates", ctypes.c_int32), ("prefix_len", ctypes.c_int32), ("rows", ctypes.c_int32),
                 ("gemm_ms", ctypes.c_double), ("gemm_bytes", ctypes.c_double), ("gemm_launches", ctypes.c_int64),
                 ("attn_ms", ctypes.c_double), ("attn_bytes", ctypes.c_double), ("attn_launches", ctypes.c_int64),
-                ("kernel_launches", ctypes.c_int64), ("elem_ms", ctypes.c_double), ("spec_ms", ctypes.c_double)]
+                ("kernel_launches", ctypes.c_int64), ("elem_ms", ctypes.c_double), ("spec_ms", ctypes.c_double),
+                ("h2d_bytes", ctypes.c_int64), ("d2h_bytes", ctypes.c_int64)]
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -91,6 +92,8 @@ def load_library():
                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
     lib.la_gemm_bf16_noalloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+    lib.la_gemm_status.argtypes = [ctypes.c_void_p]
+    lib.la_selftest_timeout.argtypes = [H, ctypes.c_int64, ctypes.c_void_p]
     lib.la_destroy.argtypes = [H]
     lib.la_destroy.restype = None
     lib.la_strerror.argtypes = [ctypes.c_int]
@@ -98,7 +101,8 @@ def load_library():
     lib.la_last_error.argtypes = []
     lib.la_last_error.restype = ctypes.c_char_p
     for name in ("la_create", "la_prefill", "la_step", "la_ar_step", "la_generate", "la_stats", "la_export_state",
-                 "la_import_state", "la_debug_logits", "la_gemm_bf16", "la_gemm_bf16_noalloc"):
+                 "la_import_state", "la_debug_logits", "la_gemm_bf16", "la_gemm_bf16_noalloc", "la_gemm_status",
+                 "la_selftest_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -208,6 +212,19 @@ def la_gemm_bf16_noalloc(x_ptr: int, w_ptr: int, y_ptr: int, rows: int, out: int
 
 
 NOALLOC_SCRATCH_FLOATS = 4 * 1024 * 1024
+
+
+def la_gemm_status(stream: Optional[int] = None) -> None:
+    """Raise LaError(-5) if a bounded wait inside an earlier la_gemm_bf16 /
+    la_gemm_bf16_noalloc kernel on this device gave up; clears the status."""
+    _check(load_library().la_gemm_status(stream), "la_gemm_status")
+
+
+def la_selftest_timeout(h, limit_ns: int, stream: Optional[int] = None) -> None:
+    """Launch the bounded-wait self-test kernel (its wait gives up after
+    limit_ns and sets a timeout bit in h's error word, or with h None in the
+    standalone GEMMs' words)."""
+    _check(load_library().la_selftest_timeout(h, limit_ns, stream), "la_selftest_timeout")
 
 
 def la_destroy(h) -> None:

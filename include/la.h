@@ -135,8 +135,8 @@ typedef struct la_stats_t {
     int32_t rows;             /* M = 1 + (W + G)(N - 1) rows per step */
     /* With la_opts.profile = 1, summed over la_step calls since la_prefill:
      * device time (CUDA events on the handle's stream), launch count and
-     * algorithmic bytes of the projection GEMMs (weights + input rows + fp32
-     * output) and of attention (prefix K/V + queries + outputs). */
+     * algorithmic bytes of the projection GEMMs (their weights, read once)
+     * and of attention (prefix and step K/V at the weights' element size). */
     double  gemm_ms;
     double  gemm_bytes;
     int64_t gemm_launches;
@@ -146,6 +146,10 @@ typedef struct la_stats_t {
     int64_t kernel_launches;  /* kernels launched by la_step calls since la_prefill */
     double  elem_ms;          /* profile: row-wise kernels (embedding, norms, rotary/KV write, SwiGLU) */
     double  spec_ms;          /* profile: lookup, argmax, verification/pool/window, KV commit */
+    int64_t h2d_bytes;        /* host-to-device bytes copied by la_prefill and la_step since la_prefill
+                                 (the prompt, the initial window) */
+    int64_t d2h_bytes;        /* device-to-host bytes copied back (the step state with the accepted
+                                 tokens, once per la_prefill and per la_step) */
 } la_stats_t;
 
 /* Host-side snapshot of the decoding state, for resume and for checking a
@@ -176,6 +180,11 @@ int la_create(const la_model_dims *dims, const la_weights *weights, const la_opt
  * causally, commit its KV, produce the first token (argmax, or a draw at
  * temperature > 0) into *first_token (host), initialise the window from the
  * prompt and, if asked, seed the pool.  Resets any previous state.
+ * Passages: the prompt's forward pass and first output of the autoregressive
+ * system (paper-graph-ui page, section 3.4, "The autoregressive system"); the
+ * window's random initialisation from the prompt ("The Lookahead Branch");
+ * prompt-as-reference seeding (section 5, "Ablation Studies (Table 3)",
+ * configurations 2 and 9).
  * Errors: INVALID_ARG, CAPACITY, CUDA, DEVICE_TIMEOUT. */
 int la_prefill(la_handle *h, const int32_t *prompt, int32_t n, int32_t *first_token);
 
@@ -201,23 +210,33 @@ int la_ar_step(la_handle *h, int32_t *token);
 
 /* Prefill, then steps until max_new tokens are produced (the prefill's first
  * token counts; the last step is truncated).  Host out[max_new]; *out_n =
- * tokens written; *n_steps = la_step calls.  Any of out_n / n_steps may be NULL. */
+ * tokens written; *n_steps = la_step calls.  Any of out_n / n_steps may be NULL.
+ * Passage: the generation loop of the autoregressive system that lookahead
+ * decoding replaces (paper-graph-ui page, section 3.4, "The autoregressive
+ * system"), with one lookahead step per iteration. */
 int la_generate(la_handle *h, const int32_t *prompt, int32_t n, int32_t max_new,
                 int32_t *out, int32_t *out_n, int32_t *n_steps);
 
-/* Counters since the last prefill (host struct). */
+/* Counters since the last prefill (host struct).  generated / steps is the
+ * step compression ratio S the pages report (paper-graph-ui page, section 5,
+ * "Ablation Studies (Table 3)": tokens per decoding step); the timing fields
+ * are this library's own instrumentation, with no passage. */
 int la_stats(const la_handle *h, la_stats_t *out);
 
-/* Copy the committed tokens, window and pool to host buffers in *st.
+/* Test and resume utility; the pages have no counterpart.
+ * Copy the committed tokens, window and pool to host buffers in *st.
  * Errors: STATE, CAPACITY (a cap too small; n_tokens / n_records still report
  * the sizes needed), CUDA. */
 int la_export_state(la_handle *h, la_state_t *st);
 
-/* Replace the state with *st (same N, W): recomputes the prefix KV from the
+/* Test and resume utility; the pages have no counterpart.
+ * Replace the state with *st (same N, W): recomputes the prefix KV from the
  * tokens, loads window and pool.  Errors: INVALID_ARG, CAPACITY, CUDA. */
 int la_import_state(la_handle *h, const la_state_t *st);
 
-/* Logits of the last step's used rows, fp32, to host[rows * vocab]: row 0,
+/* Debug utility (no passage): the rows are those the verification and the
+ * lookahead branch read (paper-graph-ui page, section 3.4).
+ * Logits of the last step's used rows, fp32, to host[rows * vocab]: row 0,
  * then the top lookahead level's W rows, then G*(N-1) candidate rows
  * (candidate c, depth m at 1 + W + c*(N-1) + m-1).  After la_prefill it
  * holds the prompt's last row only (rows = 1).  *rows, *vocab receive the
@@ -231,7 +250,8 @@ int la_debug_logits(la_handle *h, float *host, int32_t *rows, int32_t *vocab);
  * across CTAs: partial sums go to `workspace` (device fp32, at least
  * splits*rows*out elements, owned by the caller) and are added in a fixed
  * order, so results are deterministic.  splits == 1 needs no workspace
- * (NULL allowed).  stream: cudaStream_t or NULL.  Asynchronous.
+ * (NULL allowed).  stream: cudaStream_t or NULL.  Asynchronous: a bounded
+ * wait that gives up inside the kernel is reported by la_gemm_status.
  * Errors: INVALID_ARG, CUDA. */
 int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
                  int32_t splits, float *workspace, void *stream);
@@ -249,12 +269,39 @@ int la_gemm_bf16(const void *x, const void *w, float *y, int32_t rows, int32_t o
  * LA_ERR_CAPACITY with nothing launched; other limits as la_gemm_bf16.
  * The first call on each device looks up that array's device address (with
  * the device current); make that first call before any stream capture.
+ * The cached address does not survive a cudaDeviceReset in the same process.
  * All calls share the array: calls whose kernels overlap on the GPU (other
  * streams, other threads on the same device) race and must be serialised by
- * the caller.  Asynchronous on `stream`.  Errors: INVALID_ARG, CAPACITY, CUDA. */
+ * the caller.  Asynchronous on `stream`; a bounded wait that gives up inside
+ * the kernel is reported by la_gemm_status.
+ * Errors: INVALID_ARG, CAPACITY, CUDA. */
 #define LA_NOALLOC_SCRATCH_FLOATS (4 * 1024 * 1024)
 int la_gemm_bf16_noalloc(const void *x, const void *w, float *y, int32_t rows, int32_t out, int32_t k,
                          int32_t splits, void *stream);
+
+/* Error status of the standalone GEMMs (la_gemm_bf16, la_gemm_bf16_noalloc)
+ * on the current device.  Their kernels wait on TMA loads and tensor-core
+ * commits with a bounded wait; one that gives up sets a bit in a per-device
+ * error word and leaves that call's output incomplete.  This call
+ * synchronises `stream` (cudaStream_t or NULL), reads and clears both words,
+ * and returns LA_ERR_DEVICE_TIMEOUT if any bit was set since the last status
+ * call, else LA_OK.  It allocates nothing.  No passage: library plumbing.
+ * Errors: DEVICE_TIMEOUT, CUDA. */
+int la_gemm_status(void *stream);
+
+/* Test support for the failure path (no passage).  Launches one CTA that
+ * waits, through the same bounded mbarrier wait every kernel here uses, on a
+ * barrier that nothing arrives at, with a limit of limit_ns nanoseconds
+ * (1e3 .. 2e9) instead of the usual 2 s.  The wait gives up, sets its
+ * timeout bit and the kernel returns: nothing faults, traps or hangs.
+ *   h != NULL: the bit goes to the handle's error word, on the handle's
+ *     stream; the next la_step / la_ar_step then returns
+ *     LA_ERR_DEVICE_TIMEOUT and the handle needs la_prefill again.
+ *   h == NULL: the bit goes to the error words of la_gemm_bf16 and (once
+ *     this device has called it) la_gemm_bf16_noalloc, on `stream`; the next
+ *     la_gemm_status reports it.
+ * Asynchronous.  Errors: INVALID_ARG (limit), CUDA. */
+int la_selftest_timeout(la_handle *h, int64_t limit_ns, void *stream);
 
 void la_destroy(la_handle *h);
 const char *la_strerror(int code);

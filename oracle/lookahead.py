@@ -174,6 +174,7 @@ class Pool:
 
     def __init__(self, cap: int, policy: str = FIFO):
         assert policy in (FIFO, LRU, LFU)
+        assert cap >= 1, "a key's list holds at least one suffix"
         self.cap = cap
         self.policy = policy
         self.lists: Dict[int, List[Tuple[int, ...]]] = {}
@@ -443,6 +444,7 @@ class StepRecord:
     window_before: np.ndarray
     logits: Optional[np.ndarray] = None   # used-row logits [U, V]
     trace: Optional[List[SampleDecision]] = None
+    decisive: Optional[List[int]] = None   # used-row indices whose argmax / distribution verification read
 
 
 class Lookahead:
@@ -529,22 +531,27 @@ class Lookahead:
         lrow = {r: logits[i] for i, r in enumerate(self.used)}
         new = [argmax_lowest(lrow[look_row(N, W, N - 2, j)]) for j in range(W)]
         trace = None
+        # Bookkeeping for parity checks: which rows' logits the verification
+        # reads (row 0, then the row of each candidate position it consults).
+        read = [0]
+
+        def row_of(c, m):
+            read.append(self.used.index(cand_row(N, W, c, m)))
+            return lrow[cand_row(N, W, c, m)]
+
         if self.T > 0:
             trace = []
             acc, winner = sampling_verify(
-                cands, self.dist(lrow[0]),
-                lambda c, m: self.dist(lrow[cand_row(N, W, c, m)]),
-                P, self.seed, N, trace)
+                cands, self.dist(lrow[0]), lambda c, m: self.dist(row_of(c, m)), P, self.seed, N, trace)
         else:
-            acc, winner = greedy_verify(cands, argmax_lowest(lrow[0]),
-                                        lambda c, m: argmax_lowest(lrow[cand_row(N, W, c, m)]))
+            acc, winner = greedy_verify(cands, argmax_lowest(lrow[0]), lambda c, m: argmax_lowest(row_of(c, m)))
         A = len(acc)
         assert 1 <= A <= N
         # KV of the accepted rows: row 0 and the winner's first A-1 rows.
         keep = [0] + [cand_row(N, W, winner, m) for m in range(1, A)]
         self.cache = decoder.concat_cache(self.cache, [(k[keep], v[keep]) for k, v in kv])
         rec = StepRecord(P, o, cands, acc, winner, new, self.window.copy(),
-                         logits if self.keep_logits else None, trace)
+                         logits if self.keep_logits else None, trace, read)
         if winner >= 0:
             self.pool.use(o, cands[winner])
         for key, suf in harvest(self.window, new):

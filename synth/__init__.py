@@ -154,9 +154,12 @@ def uniform_tokens(n: int, vocab: int, seed: int, stream: int = PROMPT_STREAM) -
 
 
 def model_weights(dims: ModelDims, seed: int = 0, std: float = 0.02,
-                  layers: Optional[List[int]] = None) -> dict:
+                  layers: Optional[List[int]] = None, lm_head_std: Optional[float] = None) -> dict:
     """All weights of a LLaMA-style decoder.  `layers` limits which layers are
-    materialised (the others are None) for callers that stream layer by layer."""
+    materialised (the others are None) for callers that stream layer by layer.
+    `lm_head_std` (default `std`) draws the lm_head with another spread: the
+    final hidden row has RMS 1, so the logits' spread is lm_head_std *
+    sqrt(d_model); small test models use it to get 7B-like logit spreads."""
     dt = dims.dtype
     d, hd, L = dims.d_model, dims.head_dim, dims.n_layers
     w = {"dims": dims, "embed": normal((dims.vocab, d), seed, 0, std, dt), "layers": []}
@@ -166,7 +169,7 @@ def model_weights(dims: ModelDims, seed: int = 0, std: float = 0.02,
             continue
         w["layers"].append(layer_weights(dims, l, seed, std))
     w["final_norm"] = ones((d,), dt)
-    w["lm_head"] = normal((dims.vocab, d), seed, 2 + 9 * L, std, dt)
+    w["lm_head"] = normal((dims.vocab, d), seed, 2 + 9 * L, std if lm_head_std is None else lm_head_std, dt)
     return w
 
 
@@ -185,6 +188,33 @@ def layer_weights(dims: ModelDims, l: int, seed: int = 0, std: float = 0.02) -> 
         "w_up": normal((dims.ffn, d), seed, b + 7, std, dt),
         "w_down": normal((d, dims.ffn), seed, b + 8, std, dt),
     }
+
+
+class LazyLayers:
+    """Per-layer weight dicts generated on access (the same values as
+    model_weights), so models larger than host memory can be streamed to the
+    device or through the CPU oracle one layer at a time."""
+
+    def __init__(self, dims: ModelDims, seed: int = 0, std: float = 0.02):
+        self.dims, self.seed, self.std = dims, seed, std
+
+    def __len__(self):
+        return self.dims.n_layers
+
+    def __getitem__(self, l):
+        if l < 0 or l >= self.dims.n_layers:
+            raise IndexError(l)
+        return layer_weights(self.dims, l, self.seed, self.std)
+
+    def __iter__(self):
+        return (self[l] for l in range(len(self)))
+
+
+def lazy_model_weights(dims: ModelDims, seed: int = 0, std: float = 0.02) -> dict:
+    """model_weights with the layers generated on access (LazyLayers)."""
+    return {"dims": dims, "embed": normal((dims.vocab, dims.d_model), seed, 0, std, dims.dtype),
+            "layers": LazyLayers(dims, seed, std), "final_norm": ones((dims.d_model,), dims.dtype),
+            "lm_head": normal((dims.vocab, dims.d_model), seed, 2 + 9 * dims.n_layers, std, dims.dtype)}
 
 
 def prompt(wl: Workload) -> np.ndarray:

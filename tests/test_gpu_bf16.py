@@ -1,14 +1,19 @@
 """bf16 path (tcgen05 GEMMs, tensor-core lookahead attention) vs the oracle on
 small bf16 decoders: teacher-forced steps, logits within 2e-2, tokens exact
 where the oracle's margin exceeds 0.05, pool exact.  Shapes cover head dim 64
-and 128, grouped-query attention, several prefix chunks and prefill chunks."""
-import dataclasses
+and 128, grouped-query attention, several prefix chunks and prefill chunks.
 
+The lm_head of these models is drawn with std 1.28 / sqrt(d_model), which
+gives the logits the spread of the 7B-shaped model (std 1.28): with the
+default 0.02 a d = 256 model's logits have std 0.32 and nearly half of its
+rows sit within 0.05 of a tie, so the accepted tokens would rarely be
+compared.  Each test counts the steps whose accepted tokens and lookahead
+columns were compared exactly and asserts a floor on them."""
 import numpy as np
 import pytest
 
 import synth
-from helpers import MARGIN, ensure_built, top2_margin
+from helpers import MARGIN, ensure_built, teacher_forced, top2_margin
 from oracle import lookahead as la
 
 pytestmark = pytest.mark.gpu
@@ -21,6 +26,10 @@ SMALL = {
 }
 
 
+def decisive_weights(dims, seed):
+    return synth.model_weights(dims, seed, lm_head_std=1.28 / np.sqrt(dims.d_model))
+
+
 @pytest.fixture(scope="module")
 def lib():
     ensure_built()
@@ -28,68 +37,47 @@ def lib():
     return e
 
 
-def run_teacher_forced(lib, w, prompt, N, W, G, steps, par=False, max_seq=1024):
-    dec = lib.Decoder(w, N, W, G, max_seq, prompt_as_reference=par)
-    dec.prefill(prompt)
-    orc = la.Lookahead(w, N, W, G, prompt_as_reference=par, keep_logits=True)
-    worst = 0.0
-    for t in range(steps):
-        s0 = dec.export_state()
-        orc.load_state(s0["tokens"], s0["window"], s0["records"])
-        acc_ref = orc.step()
-        rec = orc.history[-1]
-        acc = dec.step()
-        logits = dec.debug_logits()
-        err = float(np.max(np.abs(logits - rec.logits)))
-        worst = max(worst, err)
-        assert err <= LOGIT_TOL_BF16, f"step {t}: logits max-abs {err}"
-        decisive = [0] + [1 + W + i for i in range(G * (N - 1))]
-        if not any(top2_margin(rec.logits[i]) <= MARGIN for i in decisive):
-            assert acc == acc_ref, f"step {t}"
-        s1 = dec.export_state()
-        for j in range(W):
-            lr = rec.logits[1 + j]
-            gnew = int(s1["window"][N - 2, j])
-            if top2_margin(lr) > MARGIN:
-                assert gnew == rec.new[j], f"step {t} column {j}"
-        pool = la.Pool.from_records(orc.pool.cap, s0["records"])
-        for key, suf in la.harvest(np.asarray(s0["window"]), [int(x) for x in s1["window"][N - 2]]):
-            pool.insert(key, suf)
-        assert pool.records() == s1["records"]
-        assert s1["tokens"] == s0["tokens"] + acc
-    dec.close()
-    return worst
+def run_teacher_forced(lib, w, prompt, N, W, G, steps, par=False, max_seq=1024, **kw):
+    t = teacher_forced(lib, w, prompt, N, W, G, steps, MARGIN, LOGIT_TOL_BF16, par=par, max_seq=max_seq, **kw)
+    print(t)
+    assert t.steps == steps
+    assert 2 * t.accept_compared >= steps, t        # at least half of the steps compared exactly
+    assert 2 * t.columns_compared >= t.columns, t
+    return t
 
 
 @pytest.mark.parametrize("name", list(SMALL))
 def test_bf16_small_models_teacher_forced(lib, name):
     dims = SMALL[name]
-    w = synth.model_weights(dims, seed=3)
+    w = decisive_weights(dims, seed=3)
     p = synth.uniform_tokens(40, dims.vocab, seed=4)
-    run_teacher_forced(lib, w, p, N=4, W=5, G=3, steps=4)
+    run_teacher_forced(lib, w, p, N=4, W=5, G=3, steps=6)
 
 
 def test_bf16_long_prompt_spans_chunks(lib):
     """300-token prompt: three prefill chunks, three prefix attention chunks."""
     dims = SMALL["gqa-hd128"]
-    w = synth.model_weights(dims, seed=5)
+    w = decisive_weights(dims, seed=5)
     p = synth.uniform_tokens(300, dims.vocab, seed=6)
-    run_teacher_forced(lib, w, p, N=5, W=7, G=7, steps=3)
+    run_teacher_forced(lib, w, p, N=5, W=7, G=7, steps=6)
 
 
 def test_bf16_repetitive_prompt_accepts(lib):
+    """A repeated prompt with prompt-as-reference: candidates hit, and at
+    least one step that accepted more than one token is compared exactly."""
     dims = SMALL["mha-hd64"]
-    w = synth.model_weights(dims, seed=7)
+    w = decisive_weights(dims, seed=7)
     p = np.tile(synth.uniform_tokens(12, dims.vocab, seed=8), 6)
-    run_teacher_forced(lib, w, p, N=4, W=4, G=4, steps=6, par=True)
+    t = run_teacher_forced(lib, w, p, N=4, W=4, G=4, steps=12, par=True)
+    assert t.accept_compared_multi >= 1, t
 
 
 def test_bf16_wide_step_rows(lib):
     """M = 1 + (15 + 15) * 4 = 121 rows (the 7B step's shape) on a small model."""
     dims = SMALL["mha-hd128-3l"]
-    w = synth.model_weights(dims, seed=9)
+    w = decisive_weights(dims, seed=9)
     p = synth.uniform_tokens(64, dims.vocab, seed=10)
-    run_teacher_forced(lib, w, p, N=5, W=15, G=15, steps=2)
+    run_teacher_forced(lib, w, p, N=5, W=15, G=15, steps=4)
 
 
 def test_graph_replay_matches_direct_launches(lib):
@@ -119,10 +107,11 @@ def test_ar_step_bf16_matches_oracle(lib):
     oracle's last-row logits, tokens equal where the margin exceeds 0.05."""
     from oracle import decoder
     dims = SMALL["gqa-hd128"]
-    w = synth.model_weights(dims, 13)
+    w = decisive_weights(dims, 13)
     p = [int(t) for t in synth.uniform_tokens(40, dims.vocab, 13, 7)]
     dec = lib.Decoder(w, 4, 5, 4, 256)
     toks = list(p) + [dec.prefill(p)]
+    compared = 0
     for _ in range(6):
         y = dec.ar_step()
         ref, _ = decoder.forward(w, toks, np.arange(len(toks)), decoder.causal_mask(0, len(toks)),
@@ -131,5 +120,7 @@ def test_ar_step_bf16_matches_oracle(lib):
         assert err <= LOGIT_TOL_BF16, f"logits max-abs {err}"
         if top2_margin(ref[0]) > MARGIN:
             assert y == la.argmax_lowest(ref[0])
+            compared += 1
         toks.append(y)
     dec.close()
+    assert compared >= 3

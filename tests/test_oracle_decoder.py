@@ -104,3 +104,111 @@ def test_tree_rows_equal_their_linear_paths(tiny):
 def test_bf16_widening_is_exact():
     bits = np.array([0x3F80, 0xBF80, 0x0000, 0x4049, 0x3C23], dtype=np.uint16)
     np.testing.assert_array_equal(decoder.as_float(bits), [1.0, -1.0, 0.0, 3.140625, 1.2734375 * 2.0 ** -7])
+
+
+# ---------------------------------------------------------------------------
+# Hand-worked one-layer decoders (d = 4).  Each case zeroes or fixes weights
+# so that the logits have a closed form worked out below with scalars; a
+# wiring mistake in the oracle (SiLU on the wrong projection, a norm moved or
+# skipped, the lm_head reading the raw residual, the FFN norm reading the
+# pre-attention residual) changes the numbers.
+# ---------------------------------------------------------------------------
+import math
+
+
+def _silu(z):
+    return z / (1.0 + math.exp(-z))
+
+
+def _one_layer(**over):
+    dims = synth.ModelDims(1, 4, 1, 1, 4, 2, 3, rms_eps=0.0, dtype="f32")
+    z4, z24, z42 = np.zeros((4, 4)), np.zeros((2, 4)), np.zeros((4, 2))
+    layer = {"attn_norm": np.ones(4), "wq": z4, "wk": z4, "wv": z4, "wo": z4, "ffn_norm": np.ones(4),
+             "w_gate": z24, "w_up": z24, "w_down": z42}
+    w = {"dims": dims, "embed": np.zeros((3, 4)), "layers": [layer], "final_norm": np.ones(4),
+         "lm_head": np.array([[1.0, 0, 0, 0], [0, 1.0, 0, 0], [1.0, 1.0, 1.0, 1.0]])}
+    for k, v in over.items():
+        (layer if k in layer else w)[k] = np.asarray(v, dtype=np.float64)
+    return w
+
+
+def _logits(w, token, position=0):
+    lg, _ = decoder.forward(w, [token], np.array([position]), np.ones((1, 1), bool))
+    return lg[0]
+
+
+def _rms_normed(v, g=(1.0, 1.0, 1.0, 1.0)):
+    r = math.sqrt(sum(x * x for x in v) / len(v))
+    return [x / r * gi for x, gi in zip(v, g)]
+
+
+def test_hand_worked_lm_head_reads_the_final_normed_residual():
+    # No layer contribution: h = E[t] = (3, 4, 0, 0); rms 2.5 -> (1.2, 1.6, 0, 0);
+    # final gain (2, 1, 1, 1) -> (2.4, 1.6, 0, 0); lm_head rows e0, e1, 1.
+    w = _one_layer(embed=[[3.0, 4, 0, 0], [30.0, 40, 0, 0], [0, 0, 0, 1.0]], final_norm=[2.0, 1, 1, 1])
+    np.testing.assert_allclose(_logits(w, 0), [2.4, 1.6, 4.0], rtol=1e-14)
+    np.testing.assert_allclose(_logits(w, 1), [2.4, 1.6, 4.0], rtol=1e-14)   # scale-free: the norm is applied
+
+
+def test_hand_worked_silu_goes_through_the_gate_projection():
+    # Attention zero.  E[0] = (2, 0, 0, 0) has rms 1, so the FFN input is
+    # (2, 0, 0, 0): gate = 1 * 2 = 2, up = 0.5 * 2 = 1, silu(2) * 1 goes to
+    # h[1] through w_down[1][0] = 1.  Swapping gate and up would give silu(1) * 2.
+    w = _one_layer(embed=[[2.0, 0, 0, 0], [0, 0, 0, 1.0], [0, 0, 1.0, 0]],
+                   w_gate=[[1.0, 0, 0, 0], [0, 0, 0, 0]], w_up=[[0.5, 0, 0, 0], [0, 0, 0, 0]],
+                   w_down=[[0, 0], [1.0, 0], [0, 0], [0, 0]])
+    h = [2.0, _silu(2.0) * 1.0, 0.0, 0.0]
+    x = _rms_normed(h)
+    np.testing.assert_allclose(_logits(w, 0), [x[0], x[1], sum(x)], rtol=1e-13)
+    assert abs(_silu(2.0) - _silu(1.0) * 2.0) > 0.25   # the swap is visible
+
+
+def test_hand_worked_strongly_negative_gate_closes_the_ffn():
+    # gate = -50 on the FFN input: silu(-50) * up is below 1e-20 whatever up is.
+    w = _one_layer(embed=[[2.0, 0, 0, 0], [0, 0, 0, 1.0], [0, 0, 1.0, 0]],
+                   w_gate=[[-25.0, 0, 0, 0], [0, 0, 0, 0]], w_up=[[7.0, 0, 0, 0], [0, 0, 0, 0]],
+                   w_down=[[0, 0], [1.0, 0], [0, 0], [0, 0]])
+    np.testing.assert_allclose(_logits(w, 0), [2.0, 0.0, 2.0], atol=1e-18)
+
+
+def test_hand_worked_norm_gains_sit_where_the_decoder_puts_them():
+    # The FFN gain (0.5, 1, 1, 1) halves the FFN input: gate 1, up 0.5,
+    # h[1] = silu(1) * 0.5.  The attention gain (7, ...) changes nothing,
+    # because attention is zero; swapping the two gains would change h[1].
+    w = _one_layer(embed=[[2.0, 0, 0, 0], [0, 0, 0, 1.0], [0, 0, 1.0, 0]], attn_norm=[7.0, 7, 7, 7],
+                   ffn_norm=[0.5, 1, 1, 1],
+                   w_gate=[[1.0, 0, 0, 0], [0, 0, 0, 0]], w_up=[[0.5, 0, 0, 0], [0, 0, 0, 0]],
+                   w_down=[[0, 0], [1.0, 0], [0, 0], [0, 0]])
+    x = _rms_normed([2.0, _silu(1.0) * 0.5, 0.0, 0.0])
+    np.testing.assert_allclose(_logits(w, 0), [x[0], x[1], sum(x)], rtol=1e-13)
+
+
+def test_hand_worked_ffn_norm_reads_the_residual_after_attention():
+    # One row at position 5 sees only itself: softmax weight 1, so the
+    # attention output is v = Wv x_attn whatever the rotation does to q and k.
+    # E[0] = (2, 2, 0, 0): rms 2^0.5, x_attn = (2^0.5, 2^0.5, 0, 0) with gain 1.
+    # Wv = I, and Wo moves component 0 to component 2: h1 = (2, 2, 2^0.5, 0).
+    # The FFN input is
+    # rmsnorm(h1); gate row (1, 0, 0, 0), up row (0, 0, 1, 0), w_down[3][0] = 1:
+    # h2[3] = silu(n0) * n2 with n = rmsnorm(h1).  Reading E[0] instead of h1
+    # would give n2 = 0 and h2[3] = 0.
+    wo = np.zeros((4, 4))
+    wo[2, 0] = 1.0
+    w = _one_layer(embed=[[2.0, 2.0, 0, 0], [0, 0, 0, 1.0], [0, 0, 1.0, 0]], wq=np.eye(4), wk=np.eye(4),
+                   wv=np.eye(4), wo=wo, w_gate=[[1.0, 0, 0, 0], [0, 0, 0, 0]],
+                   w_up=[[0, 0, 1.0, 0], [0, 0, 0, 0]], w_down=[[0, 0], [0, 0], [0, 0], [1.0, 0]])
+    w["lm_head"] = np.array([[1.0, 0, 0, 0], [0, 0, 1.0, 0], [0, 0, 0, 1.0]])
+    h1 = [2.0, 2.0, math.sqrt(2.0), 0.0]
+    n = _rms_normed(h1)
+    h2 = h1[:3] + [_silu(n[0]) * n[2]]
+    x = _rms_normed(h2)
+    np.testing.assert_allclose(_logits(w, 0, position=5), [x[0], x[2], x[3]], rtol=1e-13)
+    assert x[3] > 0.1
+
+
+def test_softmax_temperature_hand_worked():
+    # logits ln(1, 4, 16): T = 1 gives (1, 4, 16) / 21; T = 2 gives (1, 2, 4) / 7.
+    lg = np.log(np.array([1.0, 4.0, 16.0]))
+    np.testing.assert_allclose(la.softmax(lg, 1.0), np.array([1, 4, 16]) / 21.0, rtol=1e-14)
+    np.testing.assert_allclose(la.softmax(lg, 2.0), np.array([1, 2, 4]) / 7.0, rtol=1e-14)
+    np.testing.assert_allclose(la.softmax(lg + 1000.0, 2.0), np.array([1, 2, 4]) / 7.0, rtol=1e-12)

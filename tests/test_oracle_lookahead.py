@@ -501,3 +501,27 @@ def test_top_k1_sampling_equals_greedy(tiny):
     o = la.Lookahead(w, 3, 4, 4, temperature=1.0, seed=5, top_k=1)
     out, _ = o.generate(p, 20)
     assert out == ref
+
+
+def test_verification_reads_the_rows_of_the_matching_candidate(tiny):
+    """A pool candidate equal to the model's greedy continuation is accepted
+    whole (A = N, Algorithm 3 with every token matching), the step's tokens
+    equal plain greedy decoding, and the rows the verification reads are row
+    0 and that candidate's N-1 rows (a non-matching candidate ahead of it is
+    read at depth 1 only through row 0)."""
+    wl, w, p = tiny
+    N, W, G = 4, 2, 3
+    prompt = [int(t) for t in p[:20]]
+    ar = la.generate_ar(w, prompt, N + 1)
+    o = ar[0]
+    good = tuple(ar[1:N])                              # the N-1 tokens greedy decoding emits after o
+    bad = tuple((t + 1) % wl.dims.vocab for t in good)
+    orc = la.Lookahead(w, N, W, G, keep_logits=True)
+    window = la.init_window(prompt, N, W, 0)
+    orc.load_state(prompt + [o], window, [(o, bad), (o, good)])
+    acc = orc.step()
+    rec = orc.history[-1]
+    assert acc == ar[1:N + 1]
+    assert rec.winner == 1
+    used = la.used_rows(N, W, G)
+    assert rec.decisive == [0] + [used.index(la.cand_row(N, W, 1, m)) for m in range(1, N)]
