@@ -94,10 +94,10 @@ struct la_handle {
     SpecState *st = nullptr;
     SpecState *st_host = nullptr;   // pinned
     int *tokens_log = nullptr, *window = nullptr, *cands = nullptr;
-    int *pkeys = nullptr, *pcnt = nullptr, *phead = nullptr, *pent = nullptr;
+    int *pkeys = nullptr, *pcnt = nullptr, *phead = nullptr, *pent = nullptr, *puse = nullptr;
     int nslots_log2 = 0;
-    int *records_dev = nullptr;
-    size_t records_dev_cap = 0;
+    int *records_dev = nullptr, *uses_dev = nullptr;
+    size_t records_dev_cap = 0, uses_dev_cap = 0;
 
     // GEMM plans (bf16): [mode][kind][layer]
     std::vector<TcGemm> plan[2][4];
@@ -186,7 +186,8 @@ struct la_handle {
         s.pent = pent;
         s.nslots_log2 = nslots_log2;
         s.cap = cap;
-        s.lru = opts.pool_policy == LA_POOL_LRU;
+        s.puse = puse;
+        s.policy = opts.pool_policy == LA_POOL_LRU ? kPoolLru : opts.pool_policy == LA_POOL_LFU ? kPoolLfu : kPoolFifo;
         s.N = N;
         s.W = W;
         s.G = G;
@@ -709,10 +710,10 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
     const la_opts &O = *opts;
     if (O.N < 2 || O.N > 8 || O.W < 1 || O.G < 0 || O.G > 32 || O.pool_cap < 0 || O.pool_cap > 32 ||
         !(O.temperature >= 0.f) || O.top_k < 0 || O.top_p != O.top_p ||
-        (O.pool_policy != LA_POOL_FIFO && O.pool_policy != LA_POOL_LRU))
+        (O.pool_policy != LA_POOL_FIFO && O.pool_policy != LA_POOL_LRU && O.pool_policy != LA_POOL_LFU))
         return fail(LA_ERR_INVALID_ARG,
                     "bad options (N 2..8, W >= 1, G 0..32, pool_cap 0..32, temperature >= 0, top_k >= 0, "
-                    "top_p a number, pool_policy FIFO or LRU)");
+                    "top_p a number, pool_policy FIFO, LRU or LFU)");
     const int M = 1 + (O.W + O.G) * (O.N - 1);
     if (M > 256) return fail(LA_ERR_UNSUPPORTED, "1 + (W+G)(N-1) must be <= 256");
     if (O.max_seq < O.N + M + 2) return fail(LA_ERR_INVALID_ARG, "max_seq too small");
@@ -841,6 +842,7 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
     A(h->alloc(&h->pcnt, nslots));
     A(h->alloc(&h->phead, nslots));
     A(h->alloc(&h->pent, nslots * h->cap * (h->N - 1)));
+    A(h->alloc(&h->puse, nslots * h->cap));
     if (rc == LA_OK && cudaMallocHost(&h->st_host, sizeof(SpecState)) != cudaSuccess)
         rc = fail(LA_ERR_OOM, "pinned host allocation failed");
     if (rc != LA_OK) return rc;
@@ -1210,7 +1212,7 @@ static int la_export_state_body(la_handle *h, la_state_t *stt) {
     const int n = h->P + 1;
     const size_t nslots = static_cast<size_t>(1) << h->nslots_log2;
     const int L = h->N - 1;
-    std::vector<int> keys(nslots), cnt(nslots), head(nslots), ent(nslots * h->cap * L);
+    std::vector<int> keys(nslots), cnt(nslots), head(nslots), ent(nslots * h->cap * L), use(nslots * h->cap);
     std::vector<int> toks(n);
     CK(cudaMemcpyAsync(toks.data(), h->tokens_log, n * sizeof(int), cudaMemcpyDeviceToHost, s));
     CK(cudaMemcpyAsync(stt->window, h->window, static_cast<size_t>(L) * h->W * sizeof(int), cudaMemcpyDeviceToHost, s));
@@ -1218,6 +1220,7 @@ static int la_export_state_body(la_handle *h, la_state_t *stt) {
     CK(cudaMemcpyAsync(cnt.data(), h->pcnt, nslots * sizeof(int), cudaMemcpyDeviceToHost, s));
     CK(cudaMemcpyAsync(head.data(), h->phead, nslots * sizeof(int), cudaMemcpyDeviceToHost, s));
     CK(cudaMemcpyAsync(ent.data(), h->pent, ent.size() * sizeof(int), cudaMemcpyDeviceToHost, s));
+    CK(cudaMemcpyAsync(use.data(), h->puse, use.size() * sizeof(int), cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));
     std::map<int, size_t> order;
     for (size_t i = 0; i < nslots; ++i)
@@ -1235,8 +1238,10 @@ static int la_export_state_body(la_handle *h, la_state_t *stt) {
         for (int e = 0; e < cnt[sl]; ++e) {
             int *rec = stt->records + static_cast<size_t>(r) * h->N;
             rec[0] = kv.first;
-            const int *src = ent.data() + (sl * h->cap + (head[sl] + e) % h->cap) * L;
+            const size_t at = sl * h->cap + (head[sl] + e) % h->cap;
+            const int *src = ent.data() + at * L;
             for (int m = 0; m < L; ++m) rec[1 + m] = src[m];
+            if (stt->uses) stt->uses[r] = h->opts.pool_policy == LA_POOL_LFU ? use[at] : 0;
             ++r;
         }
     }
@@ -1280,7 +1285,21 @@ static int la_import_state_body(la_handle *h, const la_state_t *stt) {
             h->records_dev_cap = need;
         }
         CK(cudaMemcpyAsync(h->records_dev, stt->records, need * sizeof(int), cudaMemcpyHostToDevice, s));
-        CK(pool_insert_launch(h->spec(), h->records_dev, stt->n_records, s));
+        const int *uses = nullptr;
+        if (stt->uses && h->opts.pool_policy == LA_POOL_LFU) {
+            for (int i = 0; i < stt->n_records; ++i)
+                if (stt->uses[i] < 0) return fail(LA_ERR_INVALID_ARG, "negative use count");
+            const size_t nu = static_cast<size_t>(stt->n_records);
+            if (nu > h->uses_dev_cap) {
+                int *p = nullptr;
+                if ((rc = h->alloc(&p, nu)) != LA_OK) return rc;
+                h->uses_dev = p;
+                h->uses_dev_cap = nu;
+            }
+            CK(cudaMemcpyAsync(h->uses_dev, stt->uses, nu * sizeof(int), cudaMemcpyHostToDevice, s));
+            uses = h->uses_dev;
+        }
+        CK(pool_insert_launch(h->spec(), h->records_dev, uses, stt->n_records, s));
     }
     CK(cudaMemcpyAsync(h->st_host, h->st, sizeof(SpecState), cudaMemcpyDeviceToHost, s));
     CK(cudaStreamSynchronize(s));

@@ -201,6 +201,8 @@ struct SpecState {
     unsigned err;   // device error bits
 };
 
+enum PoolPolicy { kPoolFifo = 0, kPoolLru = 1, kPoolLfu = 2 };   // la_opts.pool_policy values
+
 struct SpecDev {
     SpecState *st;
     int *tokens_log;      // [max_seq] committed tokens
@@ -216,9 +218,10 @@ struct SpecDev {
     const int *thr_cut;
     int V;
     int *pkeys, *pcnt, *phead, *pent;  // pool: open-addressed table keyed by first token
+    int *puse;            // [slots][cap] use count of each ring entry (LFU order)
     int nslots_log2;
     int cap;
-    int lru;              // 1: LRU pool order (uses move entries to the most recent end); 0: FIFO
+    int policy;           // kPoolFifo, kPoolLru (uses move entries to the most recent end) or kPoolLfu
     int N, W, G, M, U;
     float T;
     unsigned long long seed;
@@ -230,8 +233,9 @@ cudaError_t kv_commit_launch(const SpecDev &d, float *cache, int L, int nkv, int
 // Same for the bf16 plane layouts (K rows, V^T columns).
 cudaError_t kv_commit_split_launch(const SpecDev &d, __nv_bfloat16 *kc, __nv_bfloat16 *vc, int L, int nkv, int hd,
                                    int seq, cudaStream_t s);
-// Insert n records [n][N] (key, suffix) in order, one warp, sequential semantics.
-cudaError_t pool_insert_launch(const SpecDev &d, const int *records, int n, cudaStream_t s);
+// Insert n records [n][N] (key, suffix) in order, one warp, sequential
+// semantics; uses (or nullptr: 0) gives each record's LFU use count.
+cudaError_t pool_insert_launch(const SpecDev &d, const int *records, const int *uses, int n, cudaStream_t s);
 // Insert the prompt's n-grams (tokens_log[0..n)) in ascending start position.
 cudaError_t pool_seed_prompt_launch(const SpecDev &d, int n, cudaStream_t s);
 // Prefill's first token: argmax or a draw at (position n, draw 0); appends to the log.

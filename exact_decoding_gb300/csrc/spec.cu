@@ -20,7 +20,14 @@
 // the head.  FIFO: a suffix that is present stays where it is, candidates
 // are read from the head.  LRU (section 7 of the same page leaves the
 // eviction policy open): a suffix harvested again, or the step's winning
-// candidate, moves to the tail, and candidates are read from the tail.  All
+// candidate, moves to the tail, and candidates are read from the tail.  LFU
+// (frequency-based eviction, the same passage): every ring entry carries a
+// use count, and the ring is kept ordered by (count, time of the last use or
+// entry) ascending; a use adds one to the count and moves the entry behind
+// every entry whose count is not larger, a new suffix enters with count 0
+// behind the count-0 entries after the head has been dropped from a full
+// ring, and candidates are read from the tail.  Since a moved or new entry
+// always carries the newest time, the ring order alone keeps the times.  All
 // pool operations run in one warp: lanes probe 32 slots, or compare 32
 // ring entries, at once; inserts keep their sequential order.
 #include <climits>
@@ -116,15 +123,91 @@ __device__ int pool_index_warp(const SpecDev &d, int slot, const int *suf, int l
     return hit ? __ffs(hit) - 1 : -1;
 }
 
-// LRU: the suffix `suf` of `key` (if present) moves to the tail.
-__device__ void pool_use_warp(const SpecDev &d, int key, const int *suf, int lane) {
-    const int f = pool_find(d, key, lane);
-    if (f < 0) return;
-    pool_move_to_tail_warp(d, f, pool_index_warp(d, f, suf, lane), lane);
+// LFU: entry `i` of `slot` is used: its count grows by one and it moves
+// behind every other entry whose count is at most the new count (they are
+// older).  Lane l holds list entry l; `i` and the counts are warp-uniform.
+__device__ void pool_lfu_use_warp(const SpecDev &d, int slot, int i, int lane) {
+    const int L = d.N - 1, cap = d.cap;
+    const int cnt = d.pcnt[slot], head = d.phead[slot];
+    if (i < 0 || i >= cnt) return;
+    int *ring = d.pent + static_cast<long long>(slot) * cap * L;
+    int *uses = d.puse + static_cast<long long>(slot) * cap;
+    int e[7], u = 0;
+    const int r = (head + lane) % cap;
+#pragma unroll
+    for (int m = 0; m < 7; ++m) e[m] = (lane < cnt && m < L) ? ring[r * L + m] : 0;
+    if (lane < cnt) u = uses[r];
+    const int newc = __shfl_sync(FULL, u, i) + 1;
+    // final index of entry i: behind entries 0..i-1 (counts <= newc - 1) and
+    // behind the run after i whose counts are <= newc
+    const int pos = __popc(__ballot_sync(FULL, lane < cnt && lane != i && u <= newc));
+    const int src = lane < i ? lane : (lane < pos ? lane + 1 : (lane == pos ? i : lane));
+#pragma unroll
+    for (int m = 0; m < 7; ++m) e[m] = __shfl_sync(FULL, e[m], src & 31);
+    u = __shfl_sync(FULL, u, src & 31);
+    if (lane == pos) u = newc;
+    __syncwarp();
+    if (lane < cnt) {
+        for (int m = 0; m < L; ++m) ring[r * L + m] = e[m];
+        uses[r] = u;
+    }
+    __syncwarp();
 }
 
-// suf: N-1 tokens, identical in every lane.
-__device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int lane) {
+// LFU: a new suffix with use count c0 enters `slot` (known absent).  A full
+// ring first drops its head (fewest uses, oldest among equals); the new entry
+// goes behind every entry whose count is at most c0.
+__device__ void pool_lfu_insert_warp(const SpecDev &d, int slot, const int *suf, int c0, int lane) {
+    const int L = d.N - 1, cap = d.cap;
+    int cnt = d.pcnt[slot], head = d.phead[slot];
+    if (cnt == cap) {
+        head = (head + 1) % cap;
+        cnt -= 1;
+    }
+    int *ring = d.pent + static_cast<long long>(slot) * cap * L;
+    int *uses = d.puse + static_cast<long long>(slot) * cap;
+    int e[7], u = 0;
+    const int r = (head + lane) % cap;
+#pragma unroll
+    for (int m = 0; m < 7; ++m) e[m] = (lane < cnt && m < L) ? ring[r * L + m] : 0;
+    if (lane < cnt) u = uses[r];
+    const int pos = __popc(__ballot_sync(FULL, lane < cnt && u <= c0));
+    const int src = lane <= pos ? lane : lane - 1;
+#pragma unroll
+    for (int m = 0; m < 7; ++m) e[m] = __shfl_sync(FULL, e[m], src & 31);
+    u = __shfl_sync(FULL, u, src & 31);
+    if (lane == pos) {
+        for (int m = 0; m < L; ++m) e[m] = suf[m];
+        u = c0;
+    }
+    __syncwarp();
+    if (lane <= cnt) {
+        for (int m = 0; m < L; ++m) ring[r * L + m] = e[m];
+        uses[r] = u;
+    }
+    __syncwarp();
+    if (lane == 0) {
+        d.pcnt[slot] = cnt + 1;
+        d.phead[slot] = head;
+    }
+    __syncwarp();
+}
+
+// A use of the suffix `suf` of `key` (if present): LRU moves it to the tail,
+// LFU counts it and re-orders; FIFO ignores it.
+__device__ void pool_use_warp(const SpecDev &d, int key, const int *suf, int lane) {
+    if (d.policy == kPoolFifo) return;
+    const int f = pool_find(d, key, lane);
+    if (f < 0) return;
+    const int i = pool_index_warp(d, f, suf, lane);
+    if (d.policy == kPoolLru)
+        pool_move_to_tail_warp(d, f, i, lane);
+    else
+        pool_lfu_use_warp(d, f, i, lane);
+}
+
+// suf: N-1 tokens, identical in every lane; c0: LFU use count of a new entry.
+__device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int lane, int c0 = 0) {
     const int L = d.N - 1, cap = d.cap;
     const int f = pool_find(d, key, lane);
     if (f == INT_MIN) {
@@ -144,7 +227,12 @@ __device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int 
     const int cnt = d.pcnt[slot], head = d.phead[slot];
     const int present = pool_index_warp(d, slot, suf, lane);
     if (present >= 0) {
-        if (d.lru) pool_move_to_tail_warp(d, slot, present, lane);
+        if (d.policy == kPoolLru) pool_move_to_tail_warp(d, slot, present, lane);
+        if (d.policy == kPoolLfu) pool_lfu_use_warp(d, slot, present, lane);
+        return;
+    }
+    if (d.policy == kPoolLfu) {
+        pool_lfu_insert_warp(d, slot, suf, c0, lane);
         return;
     }
     if (lane == 0) {
@@ -180,7 +268,7 @@ __global__ void __launch_bounds__(256) k_build_rows(SpecDev d) {
                 g = min(cnt, d.G);
                 for (int t = lane; t < g * L; t += 32) {
                     const int c = t / L, m = t % L;
-                    const int li = d.lru ? cnt - 1 - c : c;   // LRU: most recent first
+                    const int li = d.policy != kPoolFifo ? cnt - 1 - c : c;   // LRU / LFU: from the tail
                     s_c[t] = d.pent[(static_cast<long long>(f) * d.cap + (head + li) % d.cap) * L + m];
                 }
             }
@@ -386,11 +474,11 @@ __global__ void __launch_bounds__(kFinishThreads) k_finish_step(SpecDev d) {
         }
         __syncthreads();
     }
-    // LRU: the winning candidate was used (before the harvest); then harvest
-    // the window's n-grams (column order) and slide the window.
+    // LRU / LFU: the winning candidate was used (before the harvest); then
+    // harvest the window's n-grams (column order) and slide the window.
     if (tid < 32) {
         int suf[8];
-        if (d.lru && s_win >= 0) {
+        if (d.policy != kPoolFifo && s_win >= 0) {
             for (int m = 0; m < L; ++m) suf[m] = d.cands[s_win * L + m];
             pool_use_warp(d, d.st->o, suf, tid);
         }
@@ -463,12 +551,13 @@ __global__ void k_kv_commit_split(SpecDev d, __nv_bfloat16 *kc, __nv_bfloat16 *v
 }
 
 // ------------------------------------------------------------------ pool seeding / import
-__global__ void k_pool_insert(SpecDev d, const int *records, int n) {
+__global__ void k_pool_insert(SpecDev d, const int *records, const int *uses, int n) {
     pdl_trigger();
     pdl_wait();
     const int lane = threadIdx.x;
     const int N = d.N;
-    for (int i = 0; i < n; ++i) pool_insert_warp(d, records[i * N], records + i * N + 1, lane);
+    for (int i = 0; i < n; ++i)
+        pool_insert_warp(d, records[i * N], records + i * N + 1, lane, uses ? uses[i] : 0);
 }
 
 __global__ void k_pool_seed_prompt(SpecDev d, int n) {
@@ -521,9 +610,9 @@ cudaError_t kv_commit_split_launch(const SpecDev &d, __nv_bfloat16 *kc, __nv_bfl
     return cudaGetLastError();
 }
 
-cudaError_t pool_insert_launch(const SpecDev &d, const int *records, int n, cudaStream_t s) {
+cudaError_t pool_insert_launch(const SpecDev &d, const int *records, const int *uses, int n, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    launch_k(k_pool_insert, dim3(1), dim3(32), 0, s, d, records, n);
+    launch_k(k_pool_insert, dim3(1), dim3(32), 0, s, d, records, uses, n);
     return cudaGetLastError();
 }
 cudaError_t pool_seed_prompt_launch(const SpecDev &d, int n, cudaStream_t s) {

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libla.so")
 
 LA_F32, LA_BF16 = 0, 1
-LA_POOL_FIFO, LA_POOL_LRU = 0, 1
+LA_POOL_FIFO, LA_POOL_LRU, LA_POOL_LFU = 0, 1, 2
 _lib = None
 
 
@@ -66,7 +66,7 @@ _I32P = ctypes.POINTER(ctypes.c_int32)
 class la_state_t(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int32), ("tokens_cap", ctypes.c_int32), ("tokens", _I32P),
                 ("window", _I32P), ("n_records", ctypes.c_int32), ("records_cap", ctypes.c_int32),
-                ("records", _I32P)]
+                ("records", _I32P), ("uses", _I32P)]
 
 
 def load_library():
@@ -170,18 +170,22 @@ def la_export_state(h, N: int, W: int, tokens_cap: int = 1 << 16, records_cap: i
     toks = np.zeros(tokens_cap, dtype=np.int32)
     win = np.zeros((N - 1) * W, dtype=np.int32)
     recs = np.zeros(records_cap * N, dtype=np.int32)
-    st = la_state_t(0, tokens_cap, _i32(toks), _i32(win), 0, records_cap, _i32(recs))
+    uses = np.zeros(records_cap, dtype=np.int32)
+    st = la_state_t(0, tokens_cap, _i32(toks), _i32(win), 0, records_cap, _i32(recs), _i32(uses))
     _check(load_library().la_export_state(h, ctypes.byref(st)), "la_export_state")
     r = recs[: st.n_records * N].reshape(st.n_records, N)
     return {"tokens": toks[: st.n_tokens].tolist(), "window": win.reshape(N - 1, W).copy(),
-            "records": [(int(x[0]), tuple(int(t) for t in x[1:])) for x in r]}
+            "records": [(int(x[0]), tuple(int(t) for t in x[1:])) for x in r],
+            "uses": uses[: st.n_records].tolist()}
 
 
-def la_import_state(h, N: int, W: int, tokens, window, records) -> None:
+def la_import_state(h, N: int, W: int, tokens, window, records, uses=None) -> None:
     toks = np.ascontiguousarray(tokens, dtype=np.int32)
     win = np.ascontiguousarray(np.asarray(window).reshape(-1), dtype=np.int32)
     recs = np.ascontiguousarray(np.array([[k, *s] for k, s in records], dtype=np.int32).reshape(-1, N))
-    st = la_state_t(len(toks), len(toks), _i32(toks), _i32(win), len(recs), len(recs), _i32(recs))
+    u = None if uses is None else np.ascontiguousarray(uses, dtype=np.int32)
+    st = la_state_t(len(toks), len(toks), _i32(toks), _i32(win), len(recs), len(recs), _i32(recs),
+                    _i32(u) if u is not None else None)
     _check(load_library().la_import_state(h, ctypes.byref(st)), "la_import_state")
 
 
@@ -281,9 +285,9 @@ class Decoder:
         self.dims, self.N, self.W, self.G = self.weights.dims, N, W, G
         self.stream = stream
         sp = stream.cuda_stream if stream is not None else None
-        policies = {"fifo": LA_POOL_FIFO, "lru": LA_POOL_LRU}
+        policies = {"fifo": LA_POOL_FIFO, "lru": LA_POOL_LRU, "lfu": LA_POOL_LFU}
         if pool_policy not in policies:
-            raise ValueError(f"pool_policy must be 'fifo' or 'lru', not {pool_policy!r}")
+            raise ValueError(f"pool_policy must be 'fifo', 'lru' or 'lfu', not {pool_policy!r}")
         o = la_opts(N, W, G, max_seq, int(prompt_as_reference), pool_cap, temperature, seed, sp, int(profile),
                     top_k, top_p, policies[pool_policy])
         self.h = la_create(self.weights.dims_struct, self.weights.struct, o)
@@ -306,8 +310,8 @@ class Decoder:
     def export_state(self) -> dict:
         return la_export_state(self.h, self.N, self.W)
 
-    def import_state(self, tokens, window, records) -> None:
-        la_import_state(self.h, self.N, self.W, tokens, window, records)
+    def import_state(self, tokens, window, records, uses=None) -> None:
+        la_import_state(self.h, self.N, self.W, tokens, window, records, uses)
 
     def debug_logits(self) -> np.ndarray:
         return la_debug_logits(self.h)

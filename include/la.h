@@ -60,6 +60,11 @@ extern "C" {
                             contributed an accepted token, or a suffix harvested again) moves an
                             entry to the most recent end; a full list drops the least recently used;
                             candidates are the G most recently used, most recent first */
+#define LA_POOL_LFU  2   /* fewest uses first: every entry counts its uses (the same events as LRU) and
+                            each list is ordered by (uses, time of the last use or entry); a full list
+                            drops its head, the fewest-used and oldest among equals, before a new
+                            suffix enters with 0 uses; candidates are the G entries with the most
+                            uses, the most recent first among equals */
 
 /* Model shape of a LLaMA-style decoder (the pages run LLaMA-2 / CodeLlama,
  * paper-graph-ui page, section 5 "Experimental setup"). */
@@ -121,7 +126,7 @@ typedef struct la_opts {
     float   top_p;                /* temperature > 0: then keep the shortest most-probable prefix whose
                                      renormalised mass reaches top_p (the crossing token included);
                                      <= 0 or >= 1: off.  Order: temperature, top_k, top_p */
-    int32_t pool_policy;          /* LA_POOL_FIFO (0) or LA_POOL_LRU (1) */
+    int32_t pool_policy;          /* LA_POOL_FIFO (0), LA_POOL_LRU (1) or LA_POOL_LFU (2) */
 } la_opts;
 
 typedef struct la_handle la_handle;
@@ -165,7 +170,10 @@ typedef struct la_state_t {
     int32_t *records;       /* [records_cap][N]: first token, then the N-1 suffix tokens;
                                keys ascending, each key's suffixes in eviction order (the next
                                to be dropped first: oldest under FIFO, least recently used
-                               under LRU); la_import_state rebuilds the same order */
+                               under LRU, fewest uses then oldest under LFU); la_import_state
+                               rebuilds the same order */
+    int32_t *uses;          /* [records_cap] or NULL: each record's use count (LFU; 0 under FIFO
+                               and LRU).  On import, NULL means 0 uses for every record */
 } la_state_t;
 
 /* Create a decoder for the given weights.  Allocates the KV cache (fp32

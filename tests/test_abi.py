@@ -61,6 +61,6 @@ def test_create_rejects_bad_options_without_touching_the_gpu():
     o.N, o.G = 3, 40
     assert lib.la_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(o), ctypes.byref(h)) == -1
     assert b"G 0..32" in lib.la_last_error()
-    o.G, o.pool_policy = 4, 2
+    o.G, o.pool_policy = 4, 3
     assert lib.la_create(ctypes.byref(d), ctypes.byref(w), ctypes.byref(o), ctypes.byref(h)) == -1
     assert b"pool_policy" in lib.la_last_error()

@@ -104,6 +104,54 @@ def test_generate_lru_pool_equals_autoregressive(lib, tiny_model):
     dec.close()
 
 
+@pytest.mark.parametrize("N,W,G,cap", [(4, 3, 4, 0), (4, 3, 2, 2), (3, 4, 3, 3)])
+def test_step_teacher_forced_lfu_pool(lib, tiny_model, N, W, G, cap):
+    """LFU pool (reading R16): use counts beside the device ring, each key's
+    list ordered by (uses, time); after every step the pool and the counts
+    equal the oracle's replay, and candidates hit.  These shapes end with a
+    pool that differs from the LRU pool's on the same run."""
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(6, wl.dims.vocab, seed=4), 6)
+    t = _teacher_forced(lib, w, p, N, W, G, steps=14, par=True, pool_policy=la.LFU, pool_cap=cap)
+    print(t)
+    assert t.steps == 14 and t.hits >= 2 and t.accept_compared >= 11 and t.accept_compared_multi >= 2
+
+
+def test_generate_lfu_pool_equals_autoregressive(lib, tiny_model):
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(6, wl.dims.vocab, seed=4), 6)
+    ar, margins = ar_with_margins(w, p, wl.new_tokens)
+    dec = make(lib, w, 4, 3, 2, prompt_as_reference=True, pool_policy=la.LFU, pool_cap=2)
+    out, steps = dec.generate(p, wl.new_tokens)
+    upto = compare_stream(out, ar, margins, MARGIN)
+    assert upto >= 16, f"first low-margin decision at {upto}"
+    assert steps < wl.new_tokens - 1
+    dec.close()
+
+
+def test_lfu_state_with_counts_resumes_identically(lib, tiny_model):
+    """An LFU snapshot carries the use counts; a fresh handle that imports it
+    continues exactly like the handle that kept stepping (tokens, pool and
+    counts)."""
+    wl, w, _ = tiny_model
+    p = np.tile(synth.uniform_tokens(6, wl.dims.vocab, seed=4), 6)
+    a = make(lib, w, 3, 4, 3, prompt_as_reference=True, pool_policy=la.LFU, pool_cap=3)
+    a.prefill(p)
+    for _ in range(8):
+        a.step()
+    s = a.export_state()
+    assert max(s["uses"]) >= 2
+    b = make(lib, w, 3, 4, 3, prompt_as_reference=True, pool_policy=la.LFU, pool_cap=3)
+    b.import_state(s["tokens"], s["window"], s["records"], s["uses"])
+    assert b.export_state()["uses"] == s["uses"]
+    for _ in range(6):
+        assert a.step() == b.step()
+    sa, sb = a.export_state(), b.export_state()
+    assert sa["records"] == sb["records"] and sa["uses"] == sb["uses"]
+    a.close()
+    b.close()
+
+
 def test_step_teacher_forced_sampling(lib, tiny_model):
     """Algorithm 4: same Philox draws on both sides; decisions within 1e-3 of
     a threshold may differ (fp32 vs fp64), everything else must match."""
