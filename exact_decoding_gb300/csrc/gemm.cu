@@ -421,16 +421,21 @@ int tc_gemm2_stages() {
 }
 
 // Raise a kernel's dynamic shared-memory limit to the device's opt-in
-// maximum.  Function attributes are per device, so `done` keeps one bit per
-// device index (indices past 63 set the attribute on every call).
+// maximum less its static shared memory.  Function attributes are per
+// device, so `done` keeps one bit per device index (indices past 63 set the
+// attribute on every call).
 static cudaError_t smem_attr_per_device(const void *fn, std::atomic<unsigned long long> &done) {
     int dev = 0, mx = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
     if (bit && (done.load() & bit)) return cudaSuccess;
+    cudaFuncAttributes fa;
     e = cudaDeviceGetAttribute(&mx, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, fn);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mx - static_cast<int>(fa.sharedSizeBytes));
     if (e == cudaSuccess) done.fetch_or(bit);
     return e;
 }

@@ -68,10 +68,10 @@ def teacher_forced_step(lib, wl, w, prompt, steps_before=1, max_tries=1, device_
         if not greedy and acc != acc_ref:
             assert any(abs(d.value) <= 1e-3 for d in rec.trace), "sampling decision differs away from any threshold"
         print(tally)
-        if not greedy or tally.accept_compared:
+        if tally.accept_compared:
             break
     dec.close()
-    if greedy:
+    if greedy or max_tries > 1:
         assert tally.accept_compared >= 1, tally
     assert 2 * tally.columns_compared >= tally.columns, tally
     return tally
@@ -80,7 +80,7 @@ def teacher_forced_step(lib, wl, w, prompt, steps_before=1, max_tries=1, device_
 def test_7b_sampling_step_matches_oracle(lib):
     wl = synth.WORKLOADS["llama7b-bf16-sampling"]
     w = synth.model_weights(wl.dims, wl.seed)
-    teacher_forced_step(lib, wl, w, synth.prompt(wl), steps_before=2)
+    teacher_forced_step(lib, wl, w, synth.prompt(wl), steps_before=2, max_tries=2)
 
 
 @pytest.mark.parametrize("name", ["codellama13b-bf16-greedy", "llama70b-bf16-greedy"])
