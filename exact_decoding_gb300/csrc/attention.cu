@@ -441,7 +441,9 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
                     it.lo = static_cast<long long>(p.nkv) * p.seq * HD;
                 }
                 it.kind = isq ? 0 : 1;
-                const float2 *rr = p.rope + static_cast<long long>(P + sdep[r]) * half + 4 * it.j;
+                // step rows sit at P + depth (the table covers a step's <= 128
+                // rows); prefill rows at P + r
+                const float2 *rr = p.rope + static_cast<long long>(P + (p.depth ? sdep[r] : r)) * half + 4 * it.j;
                 it.c01 = *reinterpret_cast<const float4 *>(rr);
                 it.c23 = *reinterpret_cast<const float4 *>(rr + 2);
                 const int np = nplanes(col0);

@@ -232,23 +232,69 @@ cudaError_t resid_norm_launch(float *h, const float *part, const int *planes, lo
 // ------------------------------------------------------------------ SwiGLU
 // part columns: gate [0, F) | up [up_off, up_off + F).  out[r][f] = silu(gate) * up.
 // Items of four columns, grid-stride over a grid sized to the SMs; F % 4 == 0.
+// A thread takes its items kSwigluBatch at a time and issues the plane loads
+// of all of them before it adds any (the loads are L2 hits whose latency,
+// not bandwidth, sets the kernel's time).
+constexpr int kSwigluBatch = 3;
+
 template <typename T>
-__global__ void __launch_bounds__(256) k_swiglu(const float *part, const int *planes, long long sstride, int ldp,
-                                                int nrows, int F, int up_off, T *out, long long lo_off) {
+__global__ void __launch_bounds__(256) k_swiglu(const float *__restrict__ part, const int *__restrict__ planes,
+                                                long long sstride, int ldp, int nrows, int F, int up_off,
+                                                T *__restrict__ out, long long lo_off) {
     pdl_trigger();
     pdl_wait();
     const int F4 = F / 4;
     const long long n = static_cast<long long>(nrows) * F4;
-    for (long long t = blockIdx.x * 256ll + threadIdx.x; t < n; t += gridDim.x * 256ll) {
-        const int r = static_cast<int>(t / F4), f = 4 * static_cast<int>(t % F4);
-        const float *pr = part + static_cast<long long>(r) * ldp;
-        const int npg = planes ? planes[f >> 7] : 1, npu = planes ? planes[(up_off + f) >> 7] : 1;
-        float4 g, u;
-        sum_planes4x2(pr + f, npg, pr + up_off + f, npu, sstride, g, u);
-        store_act4(out, static_cast<long long>(r) * F + f,
-                   make_float4(g.x / (1.f + expf(-g.x)) * u.x, g.y / (1.f + expf(-g.y)) * u.y,
-                               g.z / (1.f + expf(-g.z)) * u.z, g.w / (1.f + expf(-g.w)) * u.w),
-                   lo_off);
+    const long long stride = gridDim.x * 256ll;
+    for (long long t0 = blockIdx.x * 256ll + threadIdx.x; t0 < n; t0 += kSwigluBatch * stride) {
+        float4 g[kSwigluBatch], u[kSwigluBatch];
+        int row[kSwigluBatch], col[kSwigluBatch];
+#pragma unroll
+        for (int b = 0; b < kSwigluBatch; ++b) {
+            const long long t = t0 + b * stride;
+            const long long tt = t < n ? t : t0;   // past the end: repeat the first item, not stored
+            row[b] = static_cast<int>(tt / F4);
+            col[b] = 4 * static_cast<int>(tt % F4);
+        }
+        // planes 0 and 1 of every item first (a tile rarely has more), then the rest
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 xg[kSwigluBatch][2], xu[kSwigluBatch][2];
+        int npg[kSwigluBatch], npu[kSwigluBatch];
+#pragma unroll
+        for (int b = 0; b < kSwigluBatch; ++b) {
+            const float *pr = part + static_cast<long long>(row[b]) * ldp;
+            const int f = col[b];
+            npg[b] = planes ? planes[f >> 7] : 1;
+            npu[b] = planes ? planes[(up_off + f) >> 7] : 1;
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                xg[b][k] = k < npg[b] ? *reinterpret_cast<const float4 *>(pr + f + k * sstride) : z;
+                xu[b][k] = k < npu[b] ? *reinterpret_cast<const float4 *>(pr + up_off + f + k * sstride) : z;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kSwigluBatch; ++b) {
+            g[b] = xg[b][0];
+            u[b] = xu[b][0];
+            if (npg[b] > 1) add4(g[b], xg[b][1]);
+            if (npu[b] > 1) add4(u[b], xu[b][1]);
+            if (npg[b] > 2 || npu[b] > 2) {
+                const float *pr = part + static_cast<long long>(row[b]) * ldp + 2 * sstride;
+                float4 rg, ru;
+                sum_planes4x2(pr + col[b], npg[b] - 2, pr + up_off + col[b], npu[b] - 2, sstride, rg, ru);
+                if (npg[b] > 2) add4(g[b], rg);
+                if (npu[b] > 2) add4(u[b], ru);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kSwigluBatch; ++b) {
+            if (t0 + b * stride >= n) break;
+            const float4 gg = g[b], uu = u[b];
+            store_act4(out, static_cast<long long>(row[b]) * F + col[b],
+                       make_float4(gg.x / (1.f + expf(-gg.x)) * uu.x, gg.y / (1.f + expf(-gg.y)) * uu.y,
+                                   gg.z / (1.f + expf(-gg.z)) * uu.z, gg.w / (1.f + expf(-gg.w)) * uu.w),
+                       lo_off);
+        }
     }
 }
 

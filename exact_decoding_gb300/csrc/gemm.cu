@@ -252,13 +252,20 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
 // (columns c = hi row c, c + 128 = lo row c), drained by its own epilogue.
 // Compared with the 1-SM kernel, a shared-memory stage per SM is half as
 // large (16 KB weights + 16 KB rows) and one MMA covers twice the weights.
+// With nrt = 2 (prefill chunks of 256 rows) a stage carries two row tiles:
+// each weight k-block feeds two MMAs, into the two TMEM accumulators
+// (columns t * 256 ..), so the accumulators are no longer double-buffered
+// across segments; the ring is 4 stages of 48 KB.
+template <int NRT>
 __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     constexpr uint32_t a_bytes = kTileM * kBlockK * 2;     // 128 weight rows
-    constexpr uint32_t b_bytes = kTileM * kBlockK * 2;     // 128 input rows (this CTA's half)
-    constexpr uint32_t stage_bytes = a_bytes + b_bytes;
+    constexpr uint32_t b_bytes = kTileM * kBlockK * 2;     // 128 input rows of one tile (this CTA's half)
+    constexpr int nrt = NRT;
+    constexpr int nbuf = nrt == 1 ? 2 : 1;                 // accumulators in flight
+    constexpr uint32_t stage_bytes = a_bytes + static_cast<uint32_t>(nrt) * b_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * stage_bytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + p.stages;
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
             for (int sg = 0; sg < p.nseg; ++sg) prefetch_tensormap(&p.a[sg]);
             prefetch_tensormap(&p.b);
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            const int brow = static_cast<int>(rank) * kTileM;   // hi rows (rank 0) or lo rows (rank 1)
+            const int brow = static_cast<int>(rank) * p.bh;     // hi rows (rank 0) or lo rows (rank 1)
             auto weight_row = [&](const SegInfo &g) { return 2 * g.row0 + static_cast<int>(rank) * kTileM; };
             int it = 0;
             for (int i = sbeg; i < send && it < p.stages; ++i) {
@@ -322,7 +329,10 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                     const uint32_t sa = smem_u32(smem + st * stage_bytes);
                     const uint32_t fl = mapa_shared(smem_u32(&full[st]), 0);
                     if (it < npre) {
-                        tma_load_2d_pair(sa + a_bytes, &p.b, kb * kBlockK, brow, fl, pol_x);
+#pragma unroll
+                        for (int t = 0; t < nrt; ++t)
+                            tma_load_2d_pair(sa + a_bytes + t * b_bytes, &p.b, kb * kBlockK, brow + t * kTileM, fl,
+                                             pol_x);
                         continue;
                     }
                     if (!mbar_wait_cluster(smem_u32(&empty[st]), ((it / p.stages) & 1) ^ 1, p.err, ERR_TIMEOUT_EMPTY)) {
@@ -331,7 +341,9 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                     }
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full[st]), 2 * stage_bytes);
                     tma_load_2d_pair(sa, &p.a[g.seg], kb * kBlockK, weight_row(g), fl, pol_w);
-                    tma_load_2d_pair(sa + a_bytes, &p.b, kb * kBlockK, brow, fl, pol_x);
+#pragma unroll
+                    for (int t = 0; t < nrt; ++t)
+                        tma_load_2d_pair(sa + a_bytes + t * b_bytes, &p.b, kb * kBlockK, brow + t * kTileM, fl, pol_x);
                 }
             }
         }
@@ -343,9 +355,9 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
             bool ok = true;
             for (int i = sbeg; i < send; ++i, ++ul) {
                 const SegInfo g = segment(p, i);
-                const int buf = ul & 1;
-                if (ok && ul >= 2)
-                    ok = mbar_wait_cluster(smem_u32(&accempty[buf]), ((ul >> 1) & 1) ^ 1, p.err, ERR_TIMEOUT_ACCUM);
+                const int buf = ul % nbuf, use = ul / nbuf;   // use-th time this accumulator is filled
+                if (ok && use >= 1)
+                    ok = mbar_wait_cluster(smem_u32(&accempty[buf]), (use - 1) & 1, p.err, ERR_TIMEOUT_ACCUM);
                 tc_fence_after();
                 const uint32_t d = tmem + static_cast<uint32_t>(buf * 2 * kTileM);
                 for (int kb = g.kb0; kb < g.kb1 && ok; ++kb, ++it) {
@@ -356,10 +368,15 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + st * stage_bytes);
-                    const uint64_t da = umma_desc_sw128(sa), db = umma_desc_sw128(sa + a_bytes);
+                    const uint64_t da = umma_desc_sw128(sa);
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / 16; ++kk)
-                        umma_pair_bf16(d, da + 2 * kk, db + 2 * kk, idesc, (kb != g.kb0 || kk != 0) ? 1u : 0u);
+                    for (int t = 0; t < nrt; ++t) {
+                        const uint64_t db = umma_desc_sw128(sa + a_bytes + t * b_bytes);
+                        const uint32_t dt = d + static_cast<uint32_t>(t * 2 * kTileM);
+#pragma unroll
+                        for (int kk = 0; kk < kBlockK / 16; ++kk)
+                            umma_pair_bf16(dt, da + 2 * kk, db + 2 * kk, idesc, (kb != g.kb0 || kk != 0) ? 1u : 0u);
+                    }
                     umma_pair_commit(smem_u32(&empty[st]), 0x3);
                 }
                 umma_pair_commit(smem_u32(&accfull[buf]), 0x3);
@@ -373,8 +390,8 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
         int ul = 0;
         for (int i = sbeg; i < send; ++i, ++ul) {
             const SegInfo g = segment(p, i);
-            const int buf = ul & 1;
-            bool ok = mbar_wait_cluster(smem_u32(&accfull[buf]), (ul >> 1) & 1, p.err, ERR_TIMEOUT_ACCUM);
+            const int buf = ul % nbuf;
+            bool ok = mbar_wait_cluster(smem_u32(&accfull[buf]), (ul / nbuf) & 1, p.err, ERR_TIMEOUT_ACCUM);
             ok = __all_sync(0xffffffffu, ok);
             __syncwarp();
             tc_fence_after();
@@ -383,10 +400,12 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
             const bool fv = f < p.seg_out[g.seg];
             float *out = p.out + static_cast<long long>(g.plane) * p.split_stride + p.seg_col0[g.seg] + f;
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * 2 * kTileM);
-            for (int c0 = 0; c0 < kTileM; c0 += 32) {
+            for (int c0 = 0; c0 < nrt * kTileM; c0 += 32) {
+                // rows c0 .. c0 + 31: tile t = c0 / 128 at columns t * 256 + (c0 % 128) (hi) and + 128 (lo)
+                const uint32_t col = static_cast<uint32_t>((c0 / kTileM) * 2 * kTileM + c0 % kTileM);
                 uint32_t r[32], s2[32];
-                tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0), r);
-                tmem_ld_32x32b_x32(lane_base + static_cast<uint32_t>(c0 + kTileM), s2);
+                tmem_ld_32x32b_x32(lane_base + col, r);
+                tmem_ld_32x32b_x32(lane_base + col + kTileM, s2);
                 tmem_ld_wait();
                 if (fv && c0 < p.nrows) {
 #pragma unroll
@@ -412,12 +431,12 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
     }
 }
 
-size_t tc_gemm2_smem_bytes(int stages) {
-    return static_cast<size_t>(stages) * (2 * kTileM * kBlockK * 2) + 1024 + 256;
+size_t tc_gemm2_smem_bytes(int stages, int nrt) {
+    return static_cast<size_t>(stages) * ((1 + nrt) * kTileM * kBlockK * 2) + 1024 + 256;
 }
 
-int tc_gemm2_stages() {
-    return static_cast<int>((200 * 1024) / (2 * kTileM * kBlockK * 2));   // 6
+int tc_gemm2_stages(int nrt) {
+    return static_cast<int>((200 * 1024) / ((1 + nrt) * kTileM * kBlockK * 2));   // 6 (one row tile), 4 (two)
 }
 
 // Raise a kernel's dynamic shared-memory limit to the device's opt-in
@@ -441,8 +460,10 @@ static cudaError_t smem_attr_per_device(const void *fn, std::atomic<unsigned lon
 }
 
 static cudaError_t gemm2_smem_attr() {
-    static std::atomic<unsigned long long> done{0};
-    return smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2), done);
+    static std::atomic<unsigned long long> done1{0}, done2{0};
+    cudaError_t e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<1>), done1);
+    if (e == cudaSuccess) e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<2>), done2);
+    return e;
 }
 
 int tc_gemm2_max_pairs() {
@@ -459,7 +480,7 @@ int tc_gemm2_max_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc2, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc2<1>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 
@@ -480,7 +501,7 @@ cudaError_t tc_gemm2_launch(const TcGemm &g, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc2, g.p);
+    return g.p.nrt == 2 ? cudaLaunchKernelEx(&cfg, k_gemm_tc2<2>, g.p) : cudaLaunchKernelEx(&cfg, k_gemm_tc2<1>, g.p);
 }
 
 size_t tc_gemm_smem_bytes(int bn, int stages) {
@@ -556,9 +577,10 @@ int choose_splits(int tiles, int n_kb, int slots) {
 
 void tc_gemm_finalize(TcGemm &g) {
     if (g.pair) {
-        g.p.stages = tc_gemm2_stages();
+        if (g.p.nrt < 1) g.p.nrt = 1;
+        g.p.stages = tc_gemm2_stages(g.p.nrt);
         g.grid = 2 * g.ctas;
-        g.smem = tc_gemm2_smem_bytes(g.p.stages);
+        g.smem = tc_gemm2_smem_bytes(g.p.stages, g.p.nrt);
         return;
     }
     g.grid = g.p.segs ? g.ctas : g.p.seg_tile0[g.p.nseg] * g.p.splits;

@@ -45,7 +45,9 @@ int fail(int code, const char *fmt, ...) {
                                            __FILE__, __LINE__);                                           \
     } while (0)
 
-constexpr int kPrefillRows = 128;
+// Prompt rows per prefill pass.  Each pass streams every weight once; the
+// 2-SM GEMM multiplies each weight stage with two 128-row tiles of them.
+constexpr int kPrefillRows = 256;
 
 enum Mode { STEP = 0, PREFILL = 1 };
 enum Kind { QKV = 0, OPROJ = 1, GATEUP = 2, DOWN = 3 };
@@ -63,6 +65,7 @@ struct la_handle {
     bool bf16 = true;
     int L = 0, d = 0, nh = 0, nkv = 0, hd = 0, F = 0, V = 0, qd = 0, kvd = 0, qkv_out = 0;
     int N = 0, W = 0, G = 0, M = 0, U = 0, cap = 0, max_seq = 0, R = 0;
+    int Rp[2] = {0, 0};   // rows per GEMM partial plane: a step's rows, a prefill pass's rows
     int bn_step = 0, bn_pf = 0, bn_u = 0;
     // bf16 models: GEMM inputs are bf16 hi/lo planes, hi rows [0, bh), lo rows [bh, 2 bh)
     int bh_step = 0, bh_pf = 0, bh_u = 0;
@@ -289,6 +292,10 @@ int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
     if (h->bf16) {
         TcGemm g = h->plan[mode][kind][l];
         g.p.nrows = nrows;
+        if (mode == PREFILL) {   // one or two 128-row tiles per weight stage
+            g.p.nrt = nrows > kTileM ? 2 : 1;
+            tc_gemm_finalize(g);
+        }
         CK(tc_gemm_launch(g, h->stream));
         h->prof_end(pe, 0, gemm_bytes(h, kind, nrows));
         return LA_OK;
@@ -388,7 +395,7 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
     for (int l = 0; l < h->L; ++l) {
         int rc;
         if ((rc = run_gemm(h, mode, QKV, l, nrows)) != LA_OK) return rc;
-        const long long ss_qkv = static_cast<long long>(h->R) * h->ldo[QKV];
+        const long long ss_qkv = static_cast<long long>(h->Rp[mode]) * h->ldo[QKV];
         // Algorithmic bytes of one attention launch: the prefix and step K/V
         // once at the weights' element size (the hi/lo planes double that).
         const double attn_bytes = (2.0 * P * h->kvd + 2.0 * nrows * h->kvd) * h->act;
@@ -440,21 +447,21 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         h->launches += 2 + (nch > 0 ? 1 : 0);   // qkv_rope, attention passes
         }
         if ((rc = run_gemm(h, mode, OPROJ, l, nrows)) != LA_OK) return rc;
-        const long long ss_d = static_cast<long long>(h->R) * h->ldo[OPROJ];
+        const long long ss_d = static_cast<long long>(h->Rp[mode]) * h->ldo[OPROJ];
         pe = mode == STEP ? h->prof_begin() : -1;
         CK(resid_norm_launch<T>(h->h, h->part, h->planes[mode][OPROJ], ss_d, h->ldo[OPROJ], h->d,
                                 static_cast<const T *>(h->ffn_norm[l]), eps, nullptr, nrows,
                                 static_cast<T *>(h->xn), bh * h->d, s));
         h->prof_end(pe, 2, 0.0);
         if ((rc = run_gemm(h, mode, GATEUP, l, nrows)) != LA_OK) return rc;
-        const long long ss_gu = static_cast<long long>(h->R) * h->ldo[GATEUP];
+        const long long ss_gu = static_cast<long long>(h->Rp[mode]) * h->ldo[GATEUP];
         pe = mode == STEP ? h->prof_begin() : -1;
         CK(swiglu_launch<T>(h->part, h->planes[mode][GATEUP], ss_gu, h->ldo[GATEUP], nrows, h->F, h->up_off,
                             static_cast<T *>(h->fa), bh * h->F, s));
         h->prof_end(pe, 2, 0.0);
         h->launches += 3;   // resid_norm after O, swiglu, resid_norm after down
         if ((rc = run_gemm(h, mode, DOWN, l, nrows)) != LA_OK) return rc;
-        const long long ss_dn = static_cast<long long>(h->R) * h->ldo[DOWN];
+        const long long ss_dn = static_cast<long long>(h->Rp[mode]) * h->ldo[DOWN];
         pe = mode == STEP ? h->prof_begin() : -1;
         if (l + 1 < h->L) {
             CK(resid_norm_launch<T>(h->h, h->part, h->planes[mode][DOWN], ss_dn, h->ldo[DOWN], h->d,
@@ -601,7 +608,7 @@ int build_plans(la_handle *h) {
             if ((rc = upload_schedule(h, tiles, nseg, 2, n_kb, pairs, proto, &h->planes[mode][kind], &maxp, group0)) !=
                 LA_OK)
                 return rc;
-            part_max = std::max(part_max, static_cast<size_t>(maxp) * h->R * h->ldo[kind]);
+            part_max = std::max(part_max, static_cast<size_t>(maxp) * h->Rp[mode] * h->ldo[kind]);
             h->plan[mode][kind].resize(h->L);
             for (int l = 0; l < h->L; ++l) {
                 TcGemm &g = h->plan[mode][kind][l];
@@ -633,7 +640,7 @@ int build_plans(la_handle *h) {
                 g.p.bn = bn;
                 g.p.bh = bhm;
                 g.p.ldo = h->ldo[kind];
-                g.p.split_stride = static_cast<long long>(h->R) * h->ldo[kind];
+                g.p.split_stride = static_cast<long long>(h->Rp[mode]) * h->ldo[kind];
                 g.p.out = h->part;
                 g.p.err = &h->st->err;
                 tc_gemm_finalize(g);
@@ -747,12 +754,14 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
     h->cap = O.pool_cap > 0 ? O.pool_cap : std::max(O.G, 1);
     h->max_seq = O.max_seq;
     h->R = round_up(std::max(M, kPrefillRows), 16);
+    h->Rp[STEP] = round_up(std::max(M, kTileM), 16);
+    h->Rp[PREFILL] = kPrefillRows;
     h->bn_step = round_up(M, 16);
     h->bn_pf = kPrefillRows;
     h->bn_u = round_up(h->U, 16);
     // bf16 GEMM inputs: hi rows [0, 128), lo rows [128, 256) of each buffer
     h->bh_step = kTileM;
-    h->bh_pf = kTileM;
+    h->bh_pf = kPrefillRows;
     h->bh_u = kTileM;
     h->act_rows = h->bf16 ? 2 * kPrefillRows : h->R;
     h->seq = h->bf16 ? round_up(h->max_seq, 64) : h->max_seq;
@@ -771,7 +780,7 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
     h->ldo[DOWN] = h->td * kTileM;
     h->ldo_lm = h->tv * kTileM;
     h->lm_stride = static_cast<long long>(std::max(h->U, 1)) * h->ldo_lm;
-    if (h->bf16 && M > kPrefillRows) {
+    if (h->bf16 && M > kTileM) {
         return fail(LA_ERR_UNSUPPORTED, "bf16 models need 1 + (W+G)(N-1) <= 128");
     }
     h->embed = w->embed;
