@@ -256,13 +256,20 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
 // each weight k-block feeds two MMAs, into the two TMEM accumulators
 // (columns t * 256 ..), so the accumulators are no longer double-buffered
 // across segments; the ring is 4 stages of 48 KB.
-template <int NRT>
+//
+// With SUB = 2 a stage holds two adjacent 64-column k-blocks of the same
+// weight rows (and rows), loaded back to back: the weight rows are read 256
+// contiguous bytes at a time instead of 128, and the producer waits once per
+// two k-blocks.  The schedule's k units are then 128 columns wide; a unit
+// past K reads zeros (TMA fill), which add nothing.
+template <int NRT, int SUB>
 __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-    constexpr uint32_t a_bytes = kTileM * kBlockK * 2;     // 128 weight rows
-    constexpr uint32_t b_bytes = kTileM * kBlockK * 2;     // 128 input rows of one tile (this CTA's half)
+    constexpr uint32_t box_bytes = kTileM * kBlockK * 2;   // 128 rows x 64 columns
+    constexpr uint32_t a_bytes = SUB * box_bytes;          // 128 weight rows, SUB k-blocks
+    constexpr uint32_t b_bytes = SUB * box_bytes;          // 128 input rows of one tile (this CTA's half)
     constexpr int nrt = NRT;
     constexpr int nbuf = nrt == 1 ? 2 : 1;                 // accumulators in flight
     constexpr uint32_t stage_bytes = a_bytes + static_cast<uint32_t>(nrt) * b_bytes;
@@ -314,8 +321,10 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                 for (int kb = g.kb0; kb < g.kb1 && it < p.stages; ++kb, ++it) {
                     const uint32_t fl = mapa_shared(smem_u32(&full[it]), 0);
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full[it]), 2 * stage_bytes);
-                    tma_load_2d_pair(smem_u32(smem + it * stage_bytes), &p.a[g.seg], kb * kBlockK, weight_row(g), fl,
-                                     pol_w);
+#pragma unroll
+                    for (int s = 0; s < SUB; ++s)
+                        tma_load_2d_pair(smem_u32(smem + it * stage_bytes) + s * box_bytes, &p.a[g.seg],
+                                         (kb * SUB + s) * kBlockK, weight_row(g), fl, pol_w);
                 }
             }
             const int npre = it;
@@ -331,8 +340,10 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                     if (it < npre) {
 #pragma unroll
                         for (int t = 0; t < nrt; ++t)
-                            tma_load_2d_pair(sa + a_bytes + t * b_bytes, &p.b, kb * kBlockK, brow + t * kTileM, fl,
-                                             pol_x);
+#pragma unroll
+                            for (int s = 0; s < SUB; ++s)
+                                tma_load_2d_pair(sa + a_bytes + t * b_bytes + s * box_bytes, &p.b, (kb * SUB + s) * kBlockK,
+                                                 brow + t * kTileM, fl, pol_x);
                         continue;
                     }
                     if (!mbar_wait_cluster(smem_u32(&empty[st]), ((it / p.stages) & 1) ^ 1, p.err, ERR_TIMEOUT_EMPTY)) {
@@ -340,10 +351,16 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full[st]), 2 * stage_bytes);
-                    tma_load_2d_pair(sa, &p.a[g.seg], kb * kBlockK, weight_row(g), fl, pol_w);
+#pragma unroll
+                    for (int s = 0; s < SUB; ++s)
+                        tma_load_2d_pair(sa + s * box_bytes, &p.a[g.seg], (kb * SUB + s) * kBlockK, weight_row(g), fl,
+                                         pol_w);
 #pragma unroll
                     for (int t = 0; t < nrt; ++t)
-                        tma_load_2d_pair(sa + a_bytes + t * b_bytes, &p.b, kb * kBlockK, brow + t * kTileM, fl, pol_x);
+#pragma unroll
+                        for (int s = 0; s < SUB; ++s)
+                            tma_load_2d_pair(sa + a_bytes + t * b_bytes + s * box_bytes, &p.b, (kb * SUB + s) * kBlockK,
+                                             brow + t * kTileM, fl, pol_x);
                 }
             }
         }
@@ -368,14 +385,18 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_u32(smem + st * stage_bytes);
-                    const uint64_t da = umma_desc_sw128(sa);
 #pragma unroll
                     for (int t = 0; t < nrt; ++t) {
-                        const uint64_t db = umma_desc_sw128(sa + a_bytes + t * b_bytes);
                         const uint32_t dt = d + static_cast<uint32_t>(t * 2 * kTileM);
 #pragma unroll
-                        for (int kk = 0; kk < kBlockK / 16; ++kk)
-                            umma_pair_bf16(dt, da + 2 * kk, db + 2 * kk, idesc, (kb != g.kb0 || kk != 0) ? 1u : 0u);
+                        for (int s = 0; s < SUB; ++s) {
+                            const uint64_t da = umma_desc_sw128(sa + s * box_bytes);
+                            const uint64_t db = umma_desc_sw128(sa + a_bytes + t * b_bytes + s * box_bytes);
+#pragma unroll
+                            for (int kk = 0; kk < kBlockK / 16; ++kk)
+                                umma_pair_bf16(dt, da + 2 * kk, db + 2 * kk, idesc,
+                                               (kb != g.kb0 || s != 0 || kk != 0) ? 1u : 0u);
+                        }
                     }
                     umma_pair_commit(smem_u32(&empty[st]), 0x3);
                 }
@@ -431,12 +452,13 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
     }
 }
 
-size_t tc_gemm2_smem_bytes(int stages, int nrt) {
-    return static_cast<size_t>(stages) * ((1 + nrt) * kTileM * kBlockK * 2) + 1024 + 256;
+size_t tc_gemm2_smem_bytes(int stages, int nrt, int sub) {
+    return static_cast<size_t>(stages) * ((1 + nrt) * sub * kTileM * kBlockK * 2) + 1024 + 256;
 }
 
-int tc_gemm2_stages(int nrt) {
-    return static_cast<int>((200 * 1024) / ((1 + nrt) * kTileM * kBlockK * 2));   // 6 (one row tile), 4 (two)
+int tc_gemm2_stages(int nrt, int sub) {
+    // 6 stages (one row tile), 4 (two row tiles), 3 (one row tile, two k-blocks per stage)
+    return static_cast<int>((200 * 1024) / ((1 + nrt) * sub * kTileM * kBlockK * 2));
 }
 
 // Raise a kernel's dynamic shared-memory limit to the device's opt-in
@@ -460,9 +482,10 @@ static cudaError_t smem_attr_per_device(const void *fn, std::atomic<unsigned lon
 }
 
 static cudaError_t gemm2_smem_attr() {
-    static std::atomic<unsigned long long> done1{0}, done2{0};
-    cudaError_t e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<1>), done1);
-    if (e == cudaSuccess) e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<2>), done2);
+    static std::atomic<unsigned long long> done1{0}, done2{0}, done3{0};
+    cudaError_t e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<1, 1>), done1);
+    if (e == cudaSuccess) e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<2, 1>), done2);
+    if (e == cudaSuccess) e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<1, 2>), done3);
     return e;
 }
 
@@ -480,7 +503,7 @@ int tc_gemm2_max_pairs() {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc2<1>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, k_gemm_tc2<1, 1>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 
@@ -501,7 +524,9 @@ cudaError_t tc_gemm2_launch(const TcGemm &g, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return g.p.nrt == 2 ? cudaLaunchKernelEx(&cfg, k_gemm_tc2<2>, g.p) : cudaLaunchKernelEx(&cfg, k_gemm_tc2<1>, g.p);
+    if (g.p.nrt == 2) return cudaLaunchKernelEx(&cfg, k_gemm_tc2<2, 1>, g.p);
+    if (g.p.sub == 2) return cudaLaunchKernelEx(&cfg, k_gemm_tc2<1, 2>, g.p);
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc2<1, 1>, g.p);
 }
 
 size_t tc_gemm_smem_bytes(int bn, int stages) {
@@ -578,9 +603,10 @@ int choose_splits(int tiles, int n_kb, int slots) {
 void tc_gemm_finalize(TcGemm &g) {
     if (g.pair) {
         if (g.p.nrt < 1) g.p.nrt = 1;
-        g.p.stages = tc_gemm2_stages(g.p.nrt);
+        if (g.p.sub < 1 || g.p.nrt == 2) g.p.sub = 1;
+        g.p.stages = tc_gemm2_stages(g.p.nrt, g.p.sub);
         g.grid = 2 * g.ctas;
-        g.smem = tc_gemm2_smem_bytes(g.p.stages, g.p.nrt);
+        g.smem = tc_gemm2_smem_bytes(g.p.stages, g.p.nrt, g.p.sub);
         return;
     }
     g.grid = g.p.segs ? g.ctas : g.p.seg_tile0[g.p.nseg] * g.p.splits;

@@ -48,6 +48,9 @@ int fail(int code, const char *fmt, ...) {
 // Prompt rows per prefill pass.  Each pass streams every weight once; the
 // 2-SM GEMM multiplies each weight stage with two 128-row tiles of them.
 constexpr int kPrefillRows = 256;
+// 64-column k-blocks per ring stage of a step's GEMMs (2: each weight row is
+// read 256 contiguous bytes at a time).  Prefill passes use one.
+constexpr int kStepSub = 2;
 
 enum Mode { STEP = 0, PREFILL = 1 };
 enum Kind { QKV = 0, OPROJ = 1, GATEUP = 2, DOWN = 3 };
@@ -600,7 +603,8 @@ int build_plans(la_handle *h) {
             }
             int tiles[3];
             for (int i = 0; i < nseg; ++i) tiles[i] = (outs[i] + kTileM - 1) / kTileM;
-            const int n_kb = (K + kBlockK - 1) / kBlockK;
+            const int sub = mode == STEP ? kStepSub : 1;
+            const int n_kb = (K + kBlockK * sub - 1) / (kBlockK * sub);
             TcGemm proto;
             std::memset(&proto.p, 0, sizeof(proto.p));
             proto.pair = true;
@@ -635,6 +639,7 @@ int build_plans(la_handle *h) {
                 g.p.b = bmap;
                 g.p.nseg = nseg;
                 g.p.n_kb = n_kb;
+                g.p.sub = sub;
                 g.p.splits = 1;
                 g.p.nrows = mode == STEP ? h->M : kPrefillRows;
                 g.p.bn = bn;
@@ -656,7 +661,7 @@ int build_plans(la_handle *h) {
         if (make_tmap_bf16(&g.p.a[0], h->lm_head, h->d, h->V, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM) ||
             make_tmap_bf16(&g.p.b, h->xu, h->d, bn, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM))
             return fail(LA_ERR_INVALID_ARG, "tensor map for lm_head failed");
-        const int n_kb = (h->d + kBlockK - 1) / kBlockK;
+        const int n_kb = (h->d + kBlockK * kStepSub - 1) / (kBlockK * kStepSub);
         int maxp = 1, rc, group0[2];
         if ((rc = upload_schedule(h, &h->tv, 1, 2, n_kb, pairs, g, &h->planes_lm, &maxp, group0)) != LA_OK) return rc;
         g.p.nseg = 1;
@@ -665,6 +670,7 @@ int build_plans(la_handle *h) {
         g.p.seg_out[0] = h->V;
         g.p.seg_col0[0] = 0;
         g.p.n_kb = n_kb;
+        g.p.sub = kStepSub;
         g.p.splits = 1;
         g.p.nrows = h->U;
         g.p.bn = bn;

@@ -32,6 +32,8 @@ struct TcGemmParams {
     int stages;                  // shared-memory pipeline depth
     int nrt;                     // 2-SM kernel: row tiles of 128 rows (1 or 2) multiplied with each weight
                                  //   stage; tile t of the hi (lo) rows starts at row t * 128 (bh + t * 128)
+    int sub;                     // 2-SM kernel: 64-column k-blocks per stage (1, or 2 with nrt == 1); the
+                                 //   schedule's k units (kb0, kb1, n_kb) are sub * 64 columns wide
     long long split_stride;      // floats between partial planes
     float *out;
     unsigned *err;
@@ -80,8 +82,8 @@ void stream_k_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, st
 void tc_gemm_finalize(TcGemm &g);
 cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s);
 // 2-SM kernel: shared memory, ring depth, and CTA pairs that fit at once.
-size_t tc_gemm2_smem_bytes(int stages, int nrt = 1);
-int tc_gemm2_stages(int nrt = 1);   // ring depth with nrt row tiles per stage
+size_t tc_gemm2_smem_bytes(int stages, int nrt = 1, int sub = 1);
+int tc_gemm2_stages(int nrt = 1, int sub = 1);   // ring depth with nrt row tiles, sub k-blocks per stage
 int tc_gemm2_max_pairs();
 cudaError_t tc_gemm2_launch(const TcGemm &g, cudaStream_t s);
 cudaError_t simt_gemm_launch(const SimtGemmParams &p, int total_f, cudaStream_t s);
