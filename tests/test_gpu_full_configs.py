@@ -8,6 +8,7 @@
     recomputes the KV by prefill) gives the same next step (logits within
     2e-2, tokens and pool identical) as the handle that kept stepping."""
 import dataclasses
+import os
 import time
 
 import numpy as np
@@ -103,6 +104,26 @@ def test_13b_full_depth_step_matches_oracle(lib):
     print(f"13B weights on device in {time.time() - t:.0f} s")
     tally = teacher_forced_step(lib, wl, w, synth.prompt(wl0)[:128], steps_before=1, max_tries=2, device_weights=dw)
     print(f"13B full depth: {tally}")
+    del dw
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.skipif(os.environ.get("LA_TEST_70B_FULL_DEPTH") != "1",
+                    reason="all 80 layers through the fp64 oracle take minutes of host time; "
+                           "set LA_TEST_70B_FULL_DEPTH=1 to run")
+def test_70b_full_depth_step_matches_oracle(lib):
+    """All 80 layers of the LLaMA-2-70B shape (GQA 64/8, N=5, W=5, G=5)
+    against the oracle on the first 64 tokens of the workload's prompt:
+    the bf16 error after 80 layers stays inside 2e-2."""
+    import torch
+    wl0 = synth.WORKLOADS["llama70b-bf16-greedy"]
+    wl = dataclasses.replace(wl0, prompt_len=64, new_tokens=16)
+    w = lazy_weights(wl.dims, wl.seed)
+    t = time.time()
+    dw = lib.DeviceWeights(w)
+    print(f"70B weights on device in {time.time() - t:.0f} s")
+    tally = teacher_forced_step(lib, wl, w, synth.prompt(wl0)[:64], steps_before=1, max_tries=2, device_weights=dw)
+    print(f"70B full depth: {tally}")
     del dw
     torch.cuda.empty_cache()
 
