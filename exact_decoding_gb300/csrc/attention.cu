@@ -260,11 +260,14 @@ cudaError_t attention_launch(const AttnArgs &a, cudaStream_t s) {
 // Per chunk:
 //   TMA   K (hi, lo) [128 keys x hd] and V^T (hi, lo) [hd x 128 keys]
 //   UMMA  S = Qh Kh^T + Qh Kl^T + Ql Kh^T          (TMEM columns 0..127)
+//   TMA   as soon as S is done, the next chunk's K into the same buffer
 //   warps 16 warps, each a 32-query x 32-key block of S (a warp reads only
 //         its own quarter of the TMEM lanes): mask, running max through
-//         shared memory, P = exp(S - m) split into (hi, lo) and stored as
-//         the next UMMA's A operand; O of earlier chunks rescaled in TMEM
-//   UMMA  O += Ph Vh + Ph Vl + Pl Vh                (TMEM columns 128..)
+//         shared memory, P = exp(S - m) split into (hi, lo) bf16 pairs and
+//         stored into TMEM (columns 256.. and 320..) as the next UMMA's A
+//         operand; O of earlier chunks rescaled in TMEM
+//   UMMA  O += Ph Vh + Ph Vl + Pl Vh                (A from TMEM; O in TMEM columns 128..)
+//   TMA   the next chunk's V
 // The products keep about 16 mantissa bits (the lo * lo term is dropped),
 // the softmax is fp32.  At the end each CTA leaves (O, m, l) per query
 // vector in its shared memory, and after a cluster barrier CTA j merges
@@ -275,13 +278,27 @@ constexpr int kUQ = 128;                     // query vectors per tile (UMMA M)
 constexpr int kUThreads = 512;               // 16 warps: 4 lane quarters x 4 column quarters
 constexpr uint32_t kUBox = 128u * 128u;      // bytes of a [128 rows x 64 bf16] swizzled box
 constexpr float kLog2e = 1.4426950408889634f;
+// TMEM columns: S [0, 128), O [128, 128 + hd), P hi [256, 320), P lo [320, 384)
+// (a bf16 pair of keys per 32-bit column).
+constexpr uint32_t kTmemO = 128, kTmemPh = 256, kTmemPl = 320, kTmemCols = 512;
+
+// O (+)= A * B^T with A (M x 16, bf16) read from tensor memory at a_tmem and
+// B from shared memory (descriptor), one UMMA of shape M x N x 16.
+static __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 
 template <int HD>
 struct AttnLayout {
     static constexpr uint32_t q_bytes = 2u * (HD / 64) * kUBox;          // (hi, lo) x d blocks of 64
     static constexpr uint32_t k_bytes = 2u * (HD / 64) * kUBox;
-    static constexpr uint32_t p_bytes = 2u * (kUKeys / 64) * kUBox;      // (hi, lo) x key blocks of 64
-    static constexpr uint32_t kp_bytes = k_bytes > p_bytes ? k_bytes : p_bytes;
+    static constexpr uint32_t kp_bytes = k_bytes;                        // K only: P lives in TMEM
     static constexpr uint32_t vbox = static_cast<uint32_t>(HD) * 128u;   // [hd rows x 64 keys]
     static constexpr uint32_t v_bytes = 2u * (kUKeys / 64) * vbox;
     static constexpr int o_ld = HD + 4;                                  // floats per merge row
@@ -346,7 +363,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
         prefetch_tensormap(&p.tv);
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -355,7 +372,9 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     const uint32_t tmem = *tmem_slot;
     const uint32_t lane_off = static_cast<uint32_t>(32 * qw) << 16;
     const uint32_t t_s = tmem + lane_off + static_cast<uint32_t>(32 * cw);              // 32 S columns
-    const uint32_t t_o = tmem + lane_off + static_cast<uint32_t>(kUKeys + kCW * cw);    // kCW O columns
+    const uint32_t t_o = tmem + lane_off + kTmemO + static_cast<uint32_t>(kCW * cw);    // kCW O columns
+    const uint32_t t_ph = tmem + lane_off + kTmemPh + static_cast<uint32_t>(16 * cw);   // this warp's 32 keys of P
+    const uint32_t t_pl = tmem + lane_off + kTmemPl + static_cast<uint32_t>(16 * cw);
 
     const int QV = p.nrows * p.gq;
     const int qv = qt * kUQ + row;
@@ -366,8 +385,10 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     const int vrows_plane = p.nkv * HD;
     const int ky0 = (p.layer * 2 * p.nkv + g) * p.seq;
     const int vy0 = (p.layer * 2 * p.nkv + g) * HD;
-    // K of chunk c completes on bar_ld, V on bar_v (S can start while V lands).
-    auto issue_kv = [&](int c, uint64_t pol) {
+    // K of chunk c completes on bar_ld (the caller accounts its bytes), V on
+    // bar_v; S can start while V lands.  Issued by thread 0, which counts them.
+    int k_issued = 0, v_issued = 0;
+    auto issue_k = [&](int c, uint64_t pol) {
         const int key0 = c * kUKeys;
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
@@ -375,6 +396,10 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
             for (int db = 0; db < HD / 64; ++db)
                 tma_load_2d(s_kp + (pl * (HD / 64) + db) * kUBox, &p.tk, db * 64,
                             static_cast<int>(ky0 + pl * krows_plane + key0), bar_ld, pol);
+        ++k_issued;
+    };
+    auto issue_v = [&](int c, uint64_t pol) {
+        const int key0 = c * kUKeys;
         mbar_arrive_expect_tx(bar_v, Lay::v_bytes);
 #pragma unroll
         for (int pl = 0; pl < 2; ++pl)
@@ -382,6 +407,11 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
             for (int kb = 0; kb < kUKeys / 64; ++kb)
                 tma_load_2d(s_v + (pl * (kUKeys / 64) + kb) * Lay::vbox, &p.tv, key0 + kb * 64, vy0 + pl * vrows_plane,
                             bar_v, pol);
+        ++v_issued;
+    };
+    auto issue_kv = [&](int c, uint64_t pol) {
+        issue_k(c, pol);
+        issue_v(c, pol);
     };
     // Cached-prefix chunk first in line: its K/V were written before this
     // launch began, so they load while the prologue runs.
@@ -565,6 +595,10 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
             }
             umma_commit(bar_s);
             w0 = mbar_wait(bar_s, ph, p.err, ERR_TIMEOUT_ATTN);
+            if (w0 && c + 1 < c_end) {   // S has read K: the next chunk's K loads during softmax and P.V
+                mbar_arrive_expect_tx(bar_ld, Lay::k_bytes);
+                issue_k(c + 1, policy_evict_normal());
+            }
         }
         ok = __syncthreads_and(w0);
         if (!ok) break;
@@ -594,26 +628,21 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
             ls += pv[j];
         }
         l_part = l_part * alpha + ls;
-        // Keys 32 cw .. 32 cw + 31 of this query vector's P row: four 16-byte
-        // chunks of the 128-byte row in key block cw / 2, 128-byte swizzle.
+        // Keys 32 cw .. 32 cw + 31 of this query vector's P row, as (hi, lo)
+        // bf16 pairs, into TMEM: column 16 cw + j holds keys 32 cw + 2j (low
+        // half) and 32 cw + 2j + 1.
         {
-            const uint32_t rowh = s_kp + (cw / 2) * kUBox + row * 128u;
-            const uint32_t rowl = rowh + 2u * kUBox;
+            uint32_t hh[16], ll[16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t hh[4], ll[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = pv[q4 * 8 + 2 * e], b = pv[q4 * 8 + 2 * e + 1];
-                    const __nv_bfloat162 hb = __floats2bfloat162_rn(a, b);
-                    const float2 hf = __bfloat1622float2(hb);
-                    hh[e] = *reinterpret_cast<const uint32_t *>(&hb);
-                    ll[e] = pack_bf16x2(a - hf.x, b - hf.y);
-                }
-                const uint32_t chunk = static_cast<uint32_t>((cw % 2) * 4 + q4) ^ static_cast<uint32_t>(row & 7);
-                st_shared_u32x4(rowh + chunk * 16u, hh[0], hh[1], hh[2], hh[3]);
-                st_shared_u32x4(rowl + chunk * 16u, ll[0], ll[1], ll[2], ll[3]);
+            for (int e = 0; e < 16; ++e) {
+                const float a = pv[2 * e], b = pv[2 * e + 1];
+                const __nv_bfloat162 hb = __floats2bfloat162_rn(a, b);
+                const float2 hf = __bfloat1622float2(hb);
+                hh[e] = *reinterpret_cast<const uint32_t *>(&hb);
+                ll[e] = pack_bf16x2(a - hf.x, b - hf.y);
             }
+            tmem_st_32x32b_x16(t_ph, hh);
+            tmem_st_32x32b_x16(t_pl, ll);
         }
         // O of the earlier chunks (in TMEM) to the new running max.
         if (it > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -635,29 +664,26 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
             tmem_st_wait();
         }
         m_run = m_new;
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         __syncthreads();
         if (tid == 0 && mbar_wait(bar_v, ph, p.err, ERR_TIMEOUT_ATTN)) {
             tc_fence_after();
 #pragma unroll
             for (int kb = 0; kb < kUKeys / 64; ++kb) {
-                const uint64_t ph_ = umma_desc_sw128(s_kp + kb * kUBox), pl_ = umma_desc_sw128(s_kp + (2 + kb) * kUBox);
                 const uint64_t vh = umma_desc_sw128(s_v + kb * Lay::vbox);
                 const uint64_t vl = umma_desc_sw128(s_v + (kUKeys / 64 + kb) * Lay::vbox);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    umma_bf16(tmem + kUKeys, ph_ + 2 * kk, vh + 2 * kk, idesc_o, (it | kb | kk) ? 1u : 0u);
-                    umma_bf16(tmem + kUKeys, ph_ + 2 * kk, vl + 2 * kk, idesc_o, 1u);
-                    umma_bf16(tmem + kUKeys, pl_ + 2 * kk, vh + 2 * kk, idesc_o, 1u);
+                    const uint32_t pc = static_cast<uint32_t>(kb * 32 + kk * 8);   // 16 keys = 8 columns
+                    umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemPh + pc, vh + 2 * kk, idesc_o, (it | kb | kk) ? 1u : 0u);
+                    umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemPh + pc, vl + 2 * kk, idesc_o, 1u);
+                    umma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemPl + pc, vh + 2 * kk, idesc_o, 1u);
                 }
             }
             umma_commit(bar_pv);
             w0 = mbar_wait(bar_pv, ph, p.err, ERR_TIMEOUT_ATTN);
-            if (w0 && c + 1 < c_end) {   // K/P and V are free again
-                mbar_arrive_expect_tx(bar_ld, Lay::k_bytes);
-                issue_kv(c + 1, policy_evict_normal());
-            }
+            if (w0 && c + 1 < c_end) issue_v(c + 1, policy_evict_normal());   // V is free again
         } else if (tid == 0) {
             w0 = false;   // V never landed
         }
@@ -668,9 +694,9 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     if (!ok) {   // a load or an MMA never completed: wait (bounded) for TMA still in flight
         m_run = -INFINITY;
         l_part = 0.f;
-        if (tid == 0 && it < c_end - c_beg) {
-            mbar_wait(bar_ld, static_cast<uint32_t>(it & 1), p.err, ERR_TIMEOUT_ATTN);
-            mbar_wait(bar_v, static_cast<uint32_t>(it & 1), p.err, ERR_TIMEOUT_ATTN);
+        if (tid == 0) {
+            for (int j = it; j < k_issued; ++j) mbar_wait(bar_ld, static_cast<uint32_t>(j & 1), p.err, ERR_TIMEOUT_ATTN);
+            for (int j = it; j < v_issued; ++j) mbar_wait(bar_v, static_cast<uint32_t>(j & 1), p.err, ERR_TIMEOUT_ATTN);
         }
     }
 
@@ -767,7 +793,7 @@ __global__ void __launch_bounds__(kUThreads, 1) k_attn_umma(const __grid_constan
     cluster_sync_all();   // peers are done reading this CTA's shared memory
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
