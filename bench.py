@@ -346,7 +346,7 @@ def run_ours(args, wl, rank, world, local_rank):
         log(f"autoregressive baseline: {ar_ms:.3f} ms/token")
 
     # ---- prefill, reported on its own: la_prefill of the host prompt (prompt
-    # copy in, KV of every prompt token in 128-row chunks, first token back)
+    # copy in, KV of every prompt token in 256-row passes, first token back)
     prefill_ms = None
     if not args.ncu:
         fresh()
@@ -435,8 +435,8 @@ def run_ours(args, wl, rank, world, local_rank):
                     "speedup on trained models"},
         "prefill": None if prefill_ms is None else {
             "tokens": len(prompt), "ms": prefill_ms, "tokens_per_s": len(prompt) / (prefill_ms * 1e-3),
-            "note": "la_prefill from a host prompt (copy in, 128-row chunks through the step kernels, each chunk "
-                    "streaming every weight once, first token read back); not part of value or ms_per_step"},
+            "note": "la_prefill from a host prompt (copy in, 256-row passes through the GEMM and attention kernels, each "
+                    "pass streaming every weight once, first token read back); not part of value or ms_per_step"},
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and not args.ncu and world == 1:
