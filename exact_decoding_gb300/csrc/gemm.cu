@@ -262,7 +262,82 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc(const __grid_constant__ TcGe
 // contiguous bytes at a time instead of 128, and the producer waits once per
 // two k-blocks.  The schedule's k units are then 128 columns wide; a unit
 // past K reads zeros (TMA fill), which add nothing.
-template <int NRT, int SUB>
+// Named barrier over the `n` threads of the calling warps (id != 0); the
+// .red form returns the AND of every thread's predicate.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// Fused SwiGLU of rows [r0, r1) of one split 128-column tile t2 of the
+// gate/up GEMM, run by the epilogue's 128 threads (e = 0..127) of one CTA
+// that contributed a piece of the tile, once every piece has arrived: gate =
+// sum of the tile's planes at columns 128 t2 + j, up = at 128 t2 + 64 + j
+// (j < 64), in plane order; feature f = 64 t2 + j.  Two items (a row's four
+// features) per thread per pass, four planes of both loaded together.  Loads
+// bypass L1: other SMs wrote the planes during this launch.
+__device__ __noinline__ void swiglu_fixup(const TcGemmParams &p, int t2, int r0, int r1, int e) {
+    const int np = p.fuse_np[t2];
+    const long long ss = p.split_stride;
+    const float *base = p.out + static_cast<long long>(r0) * p.ldo + t2 * kTileM;
+    const int fbase = t2 * 64, nit = (r1 - r0) * 16;
+    for (int i0 = e; i0 < nit; i0 += 2 * 128) {
+        const float *pr[2];
+        float4 g[2], u[2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int i = i0 + b * 128 < nit ? i0 + b * 128 : i0;
+            pr[b] = base + static_cast<long long>(i >> 4) * p.ldo + 4 * (i & 15);
+            g[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+            u[b] = g[b];
+        }
+        for (int k0 = 0; k0 < np; k0 += 4) {   // four planes of both items in flight, added in plane order
+            float4 xg[2][4], xu[2][4];
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (k0 + k < np) {
+                        xg[b][k] = __ldcg(reinterpret_cast<const float4 *>(pr[b] + (k0 + k) * ss));
+                        xu[b][k] = __ldcg(reinterpret_cast<const float4 *>(pr[b] + 64 + (k0 + k) * ss));
+                    }
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (k0 + k < np) {
+                        add4(g[b], xg[b][k]);
+                        add4(u[b], xu[b][k]);
+                    }
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int i = i0 + b * 128;
+            const int f = fbase + 4 * (i & 15);
+            const float4 gg = g[b], uu = u[b];
+            if (i < nit && f < p.fuse_F)
+                store_act4(p.fuse_out, static_cast<long long>(r0 + (i >> 4)) * p.fuse_F + f,
+                           make_float4(__fdividef(gg.x, 1.f + __expf(-gg.x)) * uu.x,
+                                       __fdividef(gg.y, 1.f + __expf(-gg.y)) * uu.y,
+                                       __fdividef(gg.z, 1.f + __expf(-gg.z)) * uu.z,
+                                       __fdividef(gg.w, 1.f + __expf(-gg.w)) * uu.w),
+                           p.fuse_lo_off);
+        }
+    }
+}
+
+template <int NRT, int SUB, bool FUSE = false>
 __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcGemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -315,16 +390,28 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             const int brow = static_cast<int>(rank) * p.bh;     // hi rows (rank 0) or lo rows (rank 1)
             auto weight_row = [&](const SegInfo &g) { return 2 * g.row0 + static_cast<int>(rank) * kTileM; };
+            // The weight half of one stage: SUB boxes of 128 rows, or with
+            // FUSE a 64-row gate box and the matching 64-row up box each.
+            auto load_w = [&](uint32_t sa, const SegInfo &g, int kb, uint32_t fl) {
+#pragma unroll
+                for (int s = 0; s < SUB; ++s) {
+                    const int col = (kb * SUB + s) * kBlockK;
+                    if constexpr (FUSE) {
+                        const int f0 = g.row0 + 64 * static_cast<int>(rank);
+                        tma_load_2d_pair(sa + s * box_bytes, &p.a[0], col, f0, fl, pol_w);
+                        tma_load_2d_pair(sa + s * box_bytes + box_bytes / 2, &p.a[1], col, f0, fl, pol_w);
+                    } else {
+                        tma_load_2d_pair(sa + s * box_bytes, &p.a[g.seg], col, weight_row(g), fl, pol_w);
+                    }
+                }
+            };
             int it = 0;
             for (int i = sbeg; i < send && it < p.stages; ++i) {
                 const SegInfo g = segment(p, i);
                 for (int kb = g.kb0; kb < g.kb1 && it < p.stages; ++kb, ++it) {
                     const uint32_t fl = mapa_shared(smem_u32(&full[it]), 0);
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full[it]), 2 * stage_bytes);
-#pragma unroll
-                    for (int s = 0; s < SUB; ++s)
-                        tma_load_2d_pair(smem_u32(smem + it * stage_bytes) + s * box_bytes, &p.a[g.seg],
-                                         (kb * SUB + s) * kBlockK, weight_row(g), fl, pol_w);
+                    load_w(smem_u32(smem + it * stage_bytes), g, kb, fl);
                 }
             }
             const int npre = it;
@@ -351,10 +438,7 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                         break;
                     }
                     if (leader) mbar_arrive_expect_tx(smem_u32(&full[st]), 2 * stage_bytes);
-#pragma unroll
-                    for (int s = 0; s < SUB; ++s)
-                        tma_load_2d_pair(sa + s * box_bytes, &p.a[g.seg], (kb * SUB + s) * kBlockK, weight_row(g), fl,
-                                         pol_w);
+                    load_w(sa, g, kb, fl);
 #pragma unroll
                     for (int t = 0; t < nrt; ++t)
 #pragma unroll
@@ -408,15 +492,100 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
         // and c + 128 are the hi and lo input row c.
         const int q = warp & 3;
         const uint32_t acc_leader[2] = {mapa_shared(smem_u32(&accempty[0]), 0), mapa_shared(smem_u32(&accempty[1]), 0)};
+        // FUSE: split tiles this CTA has published a piece of, waiting for
+        // the rest: (tile, arrival count that completes it, share = plane).
+        // Every piece is published before any wait, so no CTA waits on a
+        // CTA that is itself waiting.
+        __shared__ int4 s_pend[8];
+        __shared__ int s_ok;
+        int npend = 0;
+        auto flush = [&]() {
+            named_bar_sync(1, 128);   // s_pend written by thread 64
+            for (int k = 0; k < npend; ++k) {
+                const int4 pd = s_pend[k];
+                if (threadIdx.x == 64) {
+                    bool arrived = ld_acquire_gpu(p.fuse_cnt + pd.x) - pd.y >= 0;
+                    const uint64_t t0 = globaltimer();
+                    while (!arrived) {
+                        __nanosleep(64);
+                        arrived = ld_acquire_gpu(p.fuse_cnt + pd.x) - pd.y >= 0;
+                        if (!arrived && globaltimer() - t0 > kWaitNs) {
+                            atomicOr(p.err, ERR_TIMEOUT_TILE);
+                            break;
+                        }
+                    }
+                    s_ok = arrived;
+                }
+                named_bar_sync(1, 128);
+                if (s_ok) {
+                    const int np = p.fuse_np[pd.x];
+                    swiglu_fixup(p, pd.x, pd.z * p.nrows / np, (pd.z + 1) * p.nrows / np,
+                                 static_cast<int>(threadIdx.x) - 64);
+                }
+                named_bar_sync(1, 128);   // s_ok is rewritten for the next entry
+            }
+            npend = 0;
+        };
         int ul = 0;
         for (int i = sbeg; i < send; ++i, ++ul) {
             const SegInfo g = segment(p, i);
             const int buf = ul % nbuf;
+            if constexpr (FUSE) {
+                // before waiting for a whole tile's accumulator, finish the
+                // split tiles (their other pieces are done early in every run)
+                if (npend > 0 && (npend == 8 || p.fuse_np[2 * g.row0 / kTileM + static_cast<int>(rank)] == 1)) flush();
+            }
             bool ok = mbar_wait_cluster(smem_u32(&accfull[buf]), (ul / nbuf) & 1, p.err, ERR_TIMEOUT_ACCUM);
             ok = __all_sync(0xffffffffu, ok);
+            // With FUSE the four epilogue warps meet at named barriers below,
+            // so they take the same branch here.
+            if constexpr (FUSE) ok = named_bar_and(1, 128, ok);
             __syncwarp();
             tc_fence_after();
             if (!ok) break;
+            if constexpr (FUSE) {
+                // A tile no other CTA touched (one plane): SwiGLU straight
+                // from TMEM.  Lanes 0..63 hold gate rows, 64..127 the up rows
+                // of the same features; the up warps pass their sums through
+                // shared memory, 32 input rows at a time.
+                const int t2 = 2 * g.row0 / kTileM + static_cast<int>(rank);
+                if (p.fuse_np[t2] == 1) {
+                    // [128 lanes][33]: this chunk's gate (lanes 0..63) and up
+                    // (64..127) sums; then thread e takes features 2 (e % 32),
+                    // + 1 of rows e / 32 + 4 k, so a warp stores 64 bf16 of one row.
+                    __shared__ float xch[128 * 33];
+                    const uint32_t lb = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * 2 * kTileM);
+                    const int e = static_cast<int>(threadIdx.x) - 64, fp = 2 * (e & 31), f = 64 * t2 + fp;
+                    for (int c0 = 0; c0 < kTileM && c0 < p.nrows; c0 += 32) {
+                        uint32_t r[32], s2[32];
+                        tmem_ld_32x32b_x32(lb + static_cast<uint32_t>(c0), r);
+                        tmem_ld_32x32b_x32(lb + static_cast<uint32_t>(c0 + kTileM), s2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            xch[(32 * q + lane) * 33 + j] = __uint_as_float(r[j]) + __uint_as_float(s2[j]);
+                        named_bar_sync(1, 128);
+                        if (f < p.fuse_F) {
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                const int j = (e >> 5) + 4 * k, row = c0 + j;
+                                if (row < p.nrows) {
+                                    const float g0 = xch[fp * 33 + j], g1 = xch[(fp + 1) * 33 + j];
+                                    const float u0 = xch[(64 + fp) * 33 + j], u1 = xch[(65 + fp) * 33 + j];
+                                    store_act2(p.fuse_out, static_cast<long long>(row) * p.fuse_F + f,
+                                               __fdividef(g0, 1.f + __expf(-g0)) * u0,
+                                               __fdividef(g1, 1.f + __expf(-g1)) * u1, p.fuse_lo_off);
+                                }
+                            }
+                        }
+                        named_bar_sync(1, 128);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acc_leader[buf]);
+                    continue;
+                }
+            }
             const int f = 2 * g.row0 + static_cast<int>(rank) * kTileM + 32 * q + lane;
             const bool fv = f < p.seg_out[g.seg];
             float *out = p.out + static_cast<long long>(g.plane) * p.split_stride + p.seg_col0[g.seg] + f;
@@ -440,6 +609,23 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_leader[buf]);
+            if constexpr (FUSE) {
+                // Publish this partial and count the arrival.  The count only
+                // grows (by the tile's planes per launch): the pieces of this
+                // launch are complete when it reaches the next multiple of them.
+                const int t2 = 2 * g.row0 / kTileM + static_cast<int>(rank);
+                __threadfence();
+                named_bar_sync(1, 128);
+                if (threadIdx.x == 64) {
+                    const int np = p.fuse_np[t2];
+                    const int old = atomicAdd(p.fuse_cnt + t2, 1);
+                    s_pend[npend] = make_int4(t2, (old / np + 1) * np, g.plane, 0);
+                }
+                ++npend;
+            }
+        }
+        if constexpr (FUSE) {
+            if (npend > 0) flush();
         }
     }
     tc_fence_before();
@@ -482,10 +668,11 @@ static cudaError_t smem_attr_per_device(const void *fn, std::atomic<unsigned lon
 }
 
 static cudaError_t gemm2_smem_attr() {
-    static std::atomic<unsigned long long> done1{0}, done2{0}, done3{0};
+    static std::atomic<unsigned long long> done1{0}, done2{0}, done3{0}, done4{0};
     cudaError_t e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<1, 1>), done1);
     if (e == cudaSuccess) e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<2, 1>), done2);
     if (e == cudaSuccess) e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<1, 2>), done3);
+    if (e == cudaSuccess) e = smem_attr_per_device(reinterpret_cast<const void *>(k_gemm_tc2<1, 2, true>), done4);
     return e;
 }
 
@@ -524,6 +711,10 @@ cudaError_t tc_gemm2_launch(const TcGemm &g, cudaStream_t s) {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    if (g.p.fuse_out) {   // fused SwiGLU: step mode only (one row tile, two k-blocks per stage)
+        if (g.p.nrt != 1 || g.p.sub != 2) return cudaErrorInvalidValue;
+        return cudaLaunchKernelEx(&cfg, k_gemm_tc2<1, 2, true>, g.p);
+    }
     if (g.p.nrt == 2) return cudaLaunchKernelEx(&cfg, k_gemm_tc2<2, 1>, g.p);
     if (g.p.sub == 2) return cudaLaunchKernelEx(&cfg, k_gemm_tc2<1, 2>, g.p);
     return cudaLaunchKernelEx(&cfg, k_gemm_tc2<1, 1>, g.p);
@@ -557,6 +748,48 @@ void stream_k_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, st
             segs.push_back(k1);
             segs.push_back(tile_planes[t]++);
             s += k1 - k0;
+        }
+    }
+    cta_first[ctas] = static_cast<int>(segs.size() / 4);
+}
+
+// Whole tiles first, stream-K for the rest: each CTA takes an even share of
+// the k-blocks of the last `tiles % ctas` tiles (split as above, planes in
+// CTA order), then `tiles / ctas` whole tiles of its own (one plane each).
+// Split tiles are done early in every CTA's run, so the CTA that completes
+// one can finish it while its whole tiles stream.
+void hybrid_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, std::vector<int> &cta_first,
+                     std::vector<int> &tile_planes) {
+    const int whole = ctas > 0 ? tiles / ctas : 0;
+    if (whole == 0) {
+        stream_k_schedule(tiles, n_kb, ctas, segs, cta_first, tile_planes);
+        return;
+    }
+    const int t_split = whole * ctas;   // tiles [t_split, tiles) are split
+    const long long W = static_cast<long long>(tiles - t_split) * n_kb;
+    segs.clear();
+    cta_first.assign(ctas + 1, 0);
+    tile_planes.assign(tiles, 0);
+    for (int c = 0; c < ctas; ++c) {
+        cta_first[c] = static_cast<int>(segs.size() / 4);
+        long long s = W * c / ctas;
+        const long long e = W * (c + 1) / ctas;
+        while (s < e) {
+            const int t = t_split + static_cast<int>(s / n_kb);
+            const int k0 = static_cast<int>(s % n_kb);
+            const int k1 = static_cast<int>(std::min<long long>(n_kb, k0 + (e - s)));
+            segs.push_back(t);
+            segs.push_back(k0);
+            segs.push_back(k1);
+            segs.push_back(tile_planes[t]++);
+            s += k1 - k0;
+        }
+        for (int w = 0; w < whole; ++w) {
+            const int t = c * whole + w;
+            segs.push_back(t);
+            segs.push_back(0);
+            segs.push_back(n_kb);
+            segs.push_back(tile_planes[t]++);
         }
     }
     cta_first[ctas] = static_cast<int>(segs.size() / 4);

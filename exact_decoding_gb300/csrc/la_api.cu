@@ -116,6 +116,11 @@ struct la_handle {
     // Per-tile partial-plane counts of each stream-K schedule ([mode][kind]);
     // null on the fp32 path (one plane).
     int *planes[2][4] = {{nullptr, nullptr, nullptr, nullptr}, {nullptr, nullptr, nullptr, nullptr}};
+    // Step gate/up GEMM with SwiGLU in its epilogue: arrival count per
+    // 128-column tile (zero between launches).
+    bool fuse_swiglu = false;
+    int *fuse_cnt = nullptr;
+    int fuse_tiles = 0;
     int *planes_lm = nullptr;
     float *lm_part = nullptr;
     long long lm_stride = 0;
@@ -458,11 +463,14 @@ int forward(la_handle *h, Mode mode, const int *tok, int nrows, int P, bool want
         h->prof_end(pe, 2, 0.0);
         if ((rc = run_gemm(h, mode, GATEUP, l, nrows)) != LA_OK) return rc;
         const long long ss_gu = static_cast<long long>(h->Rp[mode]) * h->ldo[GATEUP];
-        pe = mode == STEP ? h->prof_begin() : -1;
-        CK(swiglu_launch<T>(h->part, h->planes[mode][GATEUP], ss_gu, h->ldo[GATEUP], nrows, h->F, h->up_off,
-                            static_cast<T *>(h->fa), bh * h->F, s));
-        h->prof_end(pe, 2, 0.0);
-        h->launches += 3;   // resid_norm after O, swiglu, resid_norm after down
+        if (!(mode == STEP && h->fuse_swiglu)) {   // else the gate/up GEMM wrote fa
+            pe = mode == STEP ? h->prof_begin() : -1;
+            CK(swiglu_launch<T>(h->part, h->planes[mode][GATEUP], ss_gu, h->ldo[GATEUP], nrows, h->F, h->up_off,
+                                static_cast<T *>(h->fa), bh * h->F, s));
+            h->prof_end(pe, 2, 0.0);
+            h->launches += 1;   // swiglu
+        }
+        h->launches += 2;   // resid_norm after O, resid_norm after down
         if ((rc = run_gemm(h, mode, DOWN, l, nrows)) != LA_OK) return rc;
         const long long ss_dn = static_cast<long long>(h->Rp[mode]) * h->ldo[DOWN];
         pe = mode == STEP ? h->prof_begin() : -1;
@@ -499,6 +507,8 @@ int check_device_error(la_handle *h) {
     if (h->st_host->err) {
         const unsigned e = h->st_host->err;
         h->prefilled = false;
+        // A gate/up launch whose waits gave up may have left arrival counts.
+        if (h->fuse_cnt) cudaMemsetAsync(h->fuse_cnt, 0, sizeof(int) * h->fuse_tiles, h->stream);
         return fail(LA_ERR_DEVICE_TIMEOUT, "device error bits 0x%x (bounded wait gave up or pool full)", e);
     }
     return LA_OK;
@@ -535,7 +545,7 @@ int reset_pool(la_handle *h) {
 // tp = 2); returns per-128-column-tile plane counts for the consumers, the
 // max plane count and each matrix's first group.
 int upload_schedule(la_handle *h, const int *tiles, int nseg, int tp, int n_kb, int ctas, TcGemm &g,
-                    int **planes_dev, int *max_planes, int *group0) {
+                    int **planes_dev, int *max_planes, int *group0, bool whole_first = false) {
     int ngroups = 0;
     for (int i = 0; i < nseg; ++i) {
         group0[i] = ngroups;
@@ -543,7 +553,8 @@ int upload_schedule(la_handle *h, const int *tiles, int nseg, int tp, int n_kb, 
     }
     group0[nseg] = ngroups;
     std::vector<int> segs, first, gplanes;
-    stream_k_schedule(ngroups, n_kb, ctas, segs, first, gplanes);
+    if (whole_first) hybrid_schedule(ngroups, n_kb, ctas, segs, first, gplanes);
+    else stream_k_schedule(ngroups, n_kb, ctas, segs, first, gplanes);
     std::vector<int> planes;   // per 128-column tile, in column order
     for (int i = 0; i < nseg; ++i)
         for (int t = 0; t < tiles[i]; ++t) planes.push_back(gplanes[group0[i] + t / tp]);
@@ -566,6 +577,14 @@ int upload_schedule(la_handle *h, const int *tiles, int nseg, int tp, int n_kb, 
 int build_plans(la_handle *h) {
     int dev = 0;
     CK(cudaGetDevice(&dev));
+    // SwiGLU in the step's gate/up GEMM epilogue (rows of 4-feature groups).
+    h->fuse_swiglu = h->F % 4 == 0;
+    if (h->fuse_swiglu) {
+        h->fuse_tiles = 2 * h->tg;
+        int rc = h->alloc(&h->fuse_cnt, static_cast<size_t>(h->fuse_tiles));
+        if (rc != LA_OK) return rc;
+        CK(cudaMemset(h->fuse_cnt, 0, sizeof(int) * h->fuse_tiles));
+    }
     int nsm = 0;
     CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
     const int bhs[2] = {h->bh_step, h->bh_pf};
@@ -580,6 +599,7 @@ int build_plans(la_handle *h) {
         const int bn = 2 * bhm;             // hi rows + lo rows
         for (int kind = 0; kind < 4; ++kind) {
             const int K = Ks[kind];
+            const bool fuse = h->fuse_swiglu && mode == STEP && kind == GATEUP;
             CUtensorMap bmap;
             if (make_tmap_bf16(&bmap, xs[kind], K, bn, static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
                 return fail(LA_ERR_CUDA, "tensor map for activations failed");
@@ -591,6 +611,12 @@ int build_plans(la_handle *h) {
                 col0[0] = 0;
                 col0[1] = h->k_off;
                 col0[2] = h->v_off;
+            } else if (kind == GATEUP && fuse) {
+                // one segment of 2 tg 128-row tiles: tile 2 t + r = gate and
+                // up rows 128 t + 64 r .. + 63 (two 64-row boxes)
+                nseg = 1;
+                outs[0] = 2 * h->tg * kTileM;
+                col0[0] = 0;
             } else if (kind == GATEUP) {
                 nseg = 2;
                 outs[0] = outs[1] = h->F;
@@ -609,8 +635,8 @@ int build_plans(la_handle *h) {
             std::memset(&proto.p, 0, sizeof(proto.p));
             proto.pair = true;
             int maxp = 1, rc, group0[4];
-            if ((rc = upload_schedule(h, tiles, nseg, 2, n_kb, pairs, proto, &h->planes[mode][kind], &maxp, group0)) !=
-                LA_OK)
+            if ((rc = upload_schedule(h, tiles, nseg, 2, n_kb, pairs, proto, &h->planes[mode][kind], &maxp, group0,
+                                      fuse)) != LA_OK)
                 return rc;
             part_max = std::max(part_max, static_cast<size_t>(maxp) * h->Rp[mode] * h->ldo[kind]);
             h->plan[mode][kind].resize(h->L);
@@ -628,8 +654,12 @@ int build_plans(la_handle *h) {
                 } else {
                     ws[0] = kind == OPROJ ? h->wo[l] : h->wd[l];
                 }
+                if (fuse && (make_tmap_bf16(&g.p.a[0], h->wg[l], K, h->F, static_cast<uint64_t>(K) * 2, kBlockK, 64) ||
+                             make_tmap_bf16(&g.p.a[1], h->wu[l], K, h->F, static_cast<uint64_t>(K) * 2, kBlockK, 64)))
+                    return fail(LA_ERR_INVALID_ARG, "tensor map for a weight failed (16-byte alignment?)");
                 for (int i = 0; i < nseg; ++i) {
-                    if (make_tmap_bf16(&g.p.a[i], ws[i], K, outs[i], static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
+                    if (!fuse &&
+                        make_tmap_bf16(&g.p.a[i], ws[i], K, outs[i], static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
                         return fail(LA_ERR_INVALID_ARG, "tensor map for a weight failed (16-byte alignment?)");
                     g.p.seg_tile0[i] = group0[i];
                     g.p.seg_out[i] = outs[i];
@@ -648,6 +678,13 @@ int build_plans(la_handle *h) {
                 g.p.split_stride = static_cast<long long>(h->Rp[mode]) * h->ldo[kind];
                 g.p.out = h->part;
                 g.p.err = &h->st->err;
+                if (fuse) {
+                    g.p.fuse_cnt = h->fuse_cnt;
+                    g.p.fuse_np = h->planes[mode][kind];
+                    g.p.fuse_out = static_cast<__nv_bfloat16 *>(h->fa);
+                    g.p.fuse_lo_off = static_cast<long long>(bhm) * h->F;
+                    g.p.fuse_F = h->F;
+                }
                 tc_gemm_finalize(g);
             }
         }

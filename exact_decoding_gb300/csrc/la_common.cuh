@@ -21,6 +21,7 @@ enum : unsigned {
     ERR_POOL = 8u,             // pool probe found no slot (table full)
     ERR_TIMEOUT_ATTN = 16u,    // attention waited too long for a TMA load or an MMA
     ERR_TIMEOUT_SELFTEST = 32u,  // the bounded-wait self-test kernel gave up (as it is meant to)
+    ERR_TIMEOUT_TILE = 64u,    // gate/up epilogue waited too long for a split tile's other pieces
 };
 
 constexpr int kMaxSeg = 3;           // weight matrices sharing one GEMM launch
@@ -337,6 +338,13 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
                  : "memory");
     return v;
 }
+// Load with acquire semantics at GPU scope (a flag or count another CTA
+// publishes with a release or a fence).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 __device__ __forceinline__ void st_shared_u32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -349,6 +357,14 @@ __device__ __forceinline__ void add4(float4 &a, const float4 &b) {
     a.w += b.w;
 }
 // Four consecutive activations (i % 4 == 0) in store_act form.
+// Two adjacent values as a (hi, lo) bf16 pair each: one 4-byte store per plane (i even).
+__device__ __forceinline__ void store_act2(__nv_bfloat16 *p, long long i, float a, float b, long long lo_off) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 f = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - f.x, b - f.y);
+    *reinterpret_cast<__nv_bfloat162 *>(p + i) = h;
+    *reinterpret_cast<__nv_bfloat162 *>(p + i + lo_off) = l;
+}
 __device__ __forceinline__ void store_act4(float *p, long long i, float4 v, long long) {
     *reinterpret_cast<float4 *>(p + i) = v;
 }

@@ -39,6 +39,20 @@ struct TcGemmParams {
     unsigned *err;
     const int4 *segs;            // stream-K segments (tile, kb0, kb1, plane) or nullptr (one split per CTA)
     const int *cta_first;        // [ctas + 1]: CTA c runs segs[cta_first[c] .. cta_first[c+1])
+    // Gate/up GEMM with SwiGLU (2-SM kernel, fuse_out set).  a[0] = gate and
+    // a[1] = up weights, boxes of 64 rows: CTA rank r of pair tile t holds
+    // gate rows f0 .. f0 + 63 in its TMEM lanes 0..63 and the up rows of the
+    // same features in lanes 64..127, f0 = 128 t + 64 r.  Its partials go to
+    // output column 128 (2 t + r) + lane like any segment's.  The CTA that
+    // brings a 128-column tile's arrival count to fuse_np[tile] (the tile's
+    // planes) adds the planes in plane order, writes silu(gate) * up as
+    // (hi, lo) bf16 rows fuse_out[row][f] (+ fuse_lo_off) for f < fuse_F,
+    // and resets the count to 0 for the next launch.
+    int *fuse_cnt;
+    const int *fuse_np;
+    __nv_bfloat16 *fuse_out;
+    long long fuse_lo_off;
+    int fuse_F;
 };
 
 struct TcGemm {
@@ -76,6 +90,8 @@ int tc_gemm_ctas_per_sm(int bn, int stages);
 int choose_splits(int tiles, int n_kb, int slots);
 // Stream-K schedule over `ctas` CTAs: segs holds 4 ints per segment.
 void stream_k_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, std::vector<int> &cta_first,
+                       std::vector<int> &tile_planes);
+void hybrid_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, std::vector<int> &cta_first,
                        std::vector<int> &tile_planes);
 
 // Fill grid/smem of a plan whose params are set.
