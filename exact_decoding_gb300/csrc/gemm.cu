@@ -344,10 +344,14 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     constexpr uint32_t box_bytes = kTileM * kBlockK * 2;   // 128 rows x 64 columns
     constexpr uint32_t a_bytes = SUB * box_bytes;          // 128 weight rows, SUB k-blocks
-    constexpr uint32_t b_bytes = SUB * box_bytes;          // 128 input rows of one tile (this CTA's half)
+    // Input rows per CTA and row tile: bh (hi rows in rank 0, lo rows in rank
+    // 1) for a step's single row tile, else 128; the UMMA N is twice that.
+    const int nhalf = gemm2_nhalf(NRT, p.bh);
+    const uint32_t bbox_bytes = static_cast<uint32_t>(nhalf) * kBlockK * 2;
+    const uint32_t b_bytes = SUB * bbox_bytes;             // this CTA's input rows of one row tile
     constexpr int nrt = NRT;
     constexpr int nbuf = nrt == 1 ? 2 : 1;                 // accumulators in flight
-    constexpr uint32_t stage_bytes = a_bytes + static_cast<uint32_t>(nrt) * b_bytes;
+    const uint32_t stage_bytes = a_bytes + static_cast<uint32_t>(nrt) * b_bytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * stage_bytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + p.stages;
@@ -429,8 +433,8 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                         for (int t = 0; t < nrt; ++t)
 #pragma unroll
                             for (int s = 0; s < SUB; ++s)
-                                tma_load_2d_pair(sa + a_bytes + t * b_bytes + s * box_bytes, &p.b, (kb * SUB + s) * kBlockK,
-                                                 brow + t * kTileM, fl, pol_x);
+                                tma_load_2d_pair(sa + a_bytes + t * b_bytes + s * bbox_bytes, &p.b,
+                                                 (kb * SUB + s) * kBlockK, brow + t * kTileM, fl, pol_x);
                         continue;
                     }
                     if (!mbar_wait_cluster(smem_u32(&empty[st]), ((it / p.stages) & 1) ^ 1, p.err, ERR_TIMEOUT_EMPTY)) {
@@ -443,15 +447,15 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                     for (int t = 0; t < nrt; ++t)
 #pragma unroll
                         for (int s = 0; s < SUB; ++s)
-                            tma_load_2d_pair(sa + a_bytes + t * b_bytes + s * box_bytes, &p.b, (kb * SUB + s) * kBlockK,
-                                             brow + t * kTileM, fl, pol_x);
+                            tma_load_2d_pair(sa + a_bytes + t * b_bytes + s * bbox_bytes, &p.b,
+                                             (kb * SUB + s) * kBlockK, brow + t * kTileM, fl, pol_x);
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // Pair UMMA issuer: M = 256, N = 256, 4 k-steps of 16 per k-block.
-            const uint32_t idesc = umma_idesc_bf16(2 * kTileM, 2 * kTileM);
+            const uint32_t idesc = umma_idesc_bf16(2 * kTileM, 2 * nhalf);
             int it = 0, ul = 0;
             bool ok = true;
             for (int i = sbeg; i < send; ++i, ++ul) {
@@ -475,7 +479,7 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
 #pragma unroll
                         for (int s = 0; s < SUB; ++s) {
                             const uint64_t da = umma_desc_sw128(sa + s * box_bytes);
-                            const uint64_t db = umma_desc_sw128(sa + a_bytes + t * b_bytes + s * box_bytes);
+                            const uint64_t db = umma_desc_sw128(sa + a_bytes + t * b_bytes + s * bbox_bytes);
 #pragma unroll
                             for (int kk = 0; kk < kBlockK / 16; ++kk)
                                 umma_pair_bf16(dt, da + 2 * kk, db + 2 * kk, idesc,
@@ -559,7 +563,7 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
                     for (int c0 = 0; c0 < kTileM && c0 < p.nrows; c0 += 32) {
                         uint32_t r[32], s2[32];
                         tmem_ld_32x32b_x32(lb + static_cast<uint32_t>(c0), r);
-                        tmem_ld_32x32b_x32(lb + static_cast<uint32_t>(c0 + kTileM), s2);
+                        tmem_ld_32x32b_x32(lb + static_cast<uint32_t>(c0 + nhalf), s2);
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -590,12 +594,12 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
             const bool fv = f < p.seg_out[g.seg];
             float *out = p.out + static_cast<long long>(g.plane) * p.split_stride + p.seg_col0[g.seg] + f;
             const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * 2 * kTileM);
-            for (int c0 = 0; c0 < nrt * kTileM; c0 += 32) {
+            for (int c0 = 0; c0 < nrt * kTileM && c0 < p.nrows; c0 += 32) {
                 // rows c0 .. c0 + 31: tile t = c0 / 128 at columns t * 256 + (c0 % 128) (hi) and + 128 (lo)
                 const uint32_t col = static_cast<uint32_t>((c0 / kTileM) * 2 * kTileM + c0 % kTileM);
                 uint32_t r[32], s2[32];
                 tmem_ld_32x32b_x32(lane_base + col, r);
-                tmem_ld_32x32b_x32(lane_base + col + kTileM, s2);
+                tmem_ld_32x32b_x32(lane_base + col + static_cast<uint32_t>(nhalf), s2);
                 tmem_ld_wait();
                 if (fv && c0 < p.nrows) {
 #pragma unroll
@@ -638,13 +642,21 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
     }
 }
 
-size_t tc_gemm2_smem_bytes(int stages, int nrt, int sub) {
-    return static_cast<size_t>(stages) * ((1 + nrt) * sub * kTileM * kBlockK * 2) + 1024 + 256;
+// Stage: SUB k-blocks of 128 weight rows and of nrt row tiles of `nhalf`
+// input rows (nhalf = bh with one row tile, 128 with two).
+static size_t gemm2_stage_bytes(int nrt, int sub, int nhalf) {
+    return static_cast<size_t>(sub) * (kTileM + nrt * nhalf) * kBlockK * 2;
 }
 
-int tc_gemm2_stages(int nrt, int sub) {
-    // 6 stages (one row tile), 4 (two row tiles), 3 (one row tile, two k-blocks per stage)
-    return static_cast<int>((200 * 1024) / ((1 + nrt) * sub * kTileM * kBlockK * 2));
+size_t tc_gemm2_smem_bytes(int stages, int nrt, int sub, int nhalf) {
+    return static_cast<size_t>(stages) * gemm2_stage_bytes(nrt, sub, nhalf) + 1024 + 256;
+}
+
+int tc_gemm2_stages(int nrt, int sub, int nhalf) {
+    // as many stages as fit in 200 KB, at most 8 (128-row halves: 6 for one row
+    // tile, 4 for two, 3 for one row tile with two k-blocks per stage)
+    const int n = static_cast<int>((200 * 1024) / gemm2_stage_bytes(nrt, sub, nhalf));
+    return n > 8 ? 8 : n;
 }
 
 // Raise a kernel's dynamic shared-memory limit to the device's opt-in
@@ -837,9 +849,10 @@ void tc_gemm_finalize(TcGemm &g) {
     if (g.pair) {
         if (g.p.nrt < 1) g.p.nrt = 1;
         if (g.p.sub < 1 || g.p.nrt == 2) g.p.sub = 1;
-        g.p.stages = tc_gemm2_stages(g.p.nrt, g.p.sub);
+        const int nhalf = gemm2_nhalf(g.p.nrt, g.p.bh);
+        g.p.stages = tc_gemm2_stages(g.p.nrt, g.p.sub, nhalf);
         g.grid = 2 * g.ctas;
-        g.smem = tc_gemm2_smem_bytes(g.p.stages, g.p.nrt, g.p.sub);
+        g.smem = tc_gemm2_smem_bytes(g.p.stages, g.p.nrt, g.p.sub, nhalf);
         return;
     }
     g.grid = g.p.segs ? g.ctas : g.p.seg_tile0[g.p.nseg] * g.p.splits;

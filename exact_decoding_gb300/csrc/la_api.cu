@@ -601,7 +601,9 @@ int build_plans(la_handle *h) {
             const int K = Ks[kind];
             const bool fuse = h->fuse_swiglu && mode == STEP && kind == GATEUP;
             CUtensorMap bmap;
-            if (make_tmap_bf16(&bmap, xs[kind], K, bn, static_cast<uint64_t>(K) * 2, kBlockK, kTileM))
+            // box: a CTA's input rows of one row tile (bh in a step, 128 per tile in a prefill pass)
+            if (make_tmap_bf16(&bmap, xs[kind], K, bn, static_cast<uint64_t>(K) * 2, kBlockK,
+                               mode == STEP ? bhm : kTileM))
                 return fail(LA_ERR_CUDA, "tensor map for activations failed");
             int outs[3], col0[3], nseg;
             if (kind == QKV) {
@@ -696,7 +698,7 @@ int build_plans(la_handle *h) {
         const int bn = 2 * h->bh_u;
         g.pair = true;
         if (make_tmap_bf16(&g.p.a[0], h->lm_head, h->d, h->V, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM) ||
-            make_tmap_bf16(&g.p.b, h->xu, h->d, bn, static_cast<uint64_t>(h->d) * 2, kBlockK, kTileM))
+            make_tmap_bf16(&g.p.b, h->xu, h->d, bn, static_cast<uint64_t>(h->d) * 2, kBlockK, h->bh_u))
             return fail(LA_ERR_INVALID_ARG, "tensor map for lm_head failed");
         const int n_kb = (h->d + kBlockK * kStepSub - 1) / (kBlockK * kStepSub);
         int maxp = 1, rc, group0[2];
@@ -802,10 +804,11 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
     h->bn_step = round_up(M, 16);
     h->bn_pf = kPrefillRows;
     h->bn_u = round_up(h->U, 16);
-    // bf16 GEMM inputs: hi rows [0, 128), lo rows [128, 256) of each buffer
-    h->bh_step = kTileM;
+    // bf16 GEMM inputs: hi rows [0, bh), lo rows [bh, 2 bh) of each buffer; a
+    // step's GEMMs multiply 2 bh rows (UMMA N), so bh follows the row count
+    h->bh_step = round_up(M, 16);
     h->bh_pf = kPrefillRows;
-    h->bh_u = kTileM;
+    h->bh_u = round_up(std::max(h->U, 1), 16);
     h->act_rows = h->bf16 ? 2 * kPrefillRows : h->R;
     h->seq = h->bf16 ? round_up(h->max_seq, 64) : h->max_seq;
     h->qv_pad = kPrefillRows * (h->nh / h->nkv);

@@ -98,8 +98,12 @@ void hybrid_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, std:
 void tc_gemm_finalize(TcGemm &g);
 cudaError_t tc_gemm_launch(const TcGemm &g, cudaStream_t s);
 // 2-SM kernel: shared memory, ring depth, and CTA pairs that fit at once.
-size_t tc_gemm2_smem_bytes(int stages, int nrt = 1, int sub = 1);
-int tc_gemm2_stages(int nrt = 1, int sub = 1);   // ring depth with nrt row tiles, sub k-blocks per stage
+// Input rows per CTA and row tile of the 2-SM kernel: bh when one row tile
+// holds all rows (bh <= 128: a step, the lm_head), else 128-row tiles.
+__host__ __device__ inline int gemm2_nhalf(int nrt, int bh) { return nrt == 1 && bh <= kTileM ? bh : kTileM; }
+// nhalf: as gemm2_nhalf
+size_t tc_gemm2_smem_bytes(int stages, int nrt = 1, int sub = 1, int nhalf = kTileM);
+int tc_gemm2_stages(int nrt = 1, int sub = 1, int nhalf = kTileM);   // ring depth (at most 8)
 int tc_gemm2_max_pairs();
 cudaError_t tc_gemm2_launch(const TcGemm &g, cudaStream_t s);
 cudaError_t simt_gemm_launch(const SimtGemmParams &p, int total_f, cudaStream_t s);
