@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
     constexpr uint32_t a_bytes = SUB * box_bytes;          // 128 weight rows, SUB k-blocks
     // Input rows per CTA and row tile: bh (hi rows in rank 0, lo rows in rank
     // 1) for a step's single row tile, else 128; the UMMA N is twice that.
-    const int nhalf = gemm2_nhalf(NRT, p.bh);
+    const int nhalf = NRT == 1 && p.bnh > 0 ? p.bnh : gemm2_nhalf(NRT, p.bh);
     const uint32_t bbox_bytes = static_cast<uint32_t>(nhalf) * kBlockK * 2;
     const uint32_t b_bytes = SUB * bbox_bytes;             // this CTA's input rows of one row tile
     constexpr int nrt = NRT;
@@ -849,7 +849,7 @@ void tc_gemm_finalize(TcGemm &g) {
     if (g.pair) {
         if (g.p.nrt < 1) g.p.nrt = 1;
         if (g.p.sub < 1 || g.p.nrt == 2) g.p.sub = 1;
-        const int nhalf = gemm2_nhalf(g.p.nrt, g.p.bh);
+        const int nhalf = g.p.nrt == 1 && g.p.bnh > 0 ? g.p.bnh : gemm2_nhalf(g.p.nrt, g.p.bh);
         g.p.stages = tc_gemm2_stages(g.p.nrt, g.p.sub, nhalf);
         g.grid = 2 * g.ctas;
         g.smem = tc_gemm2_smem_bytes(g.p.stages, g.p.nrt, g.p.sub, nhalf);

@@ -47,6 +47,7 @@ int fail(int code, const char *fmt, ...) {
 
 // Prompt rows per prefill pass.  Each pass streams every weight once; the
 // 2-SM GEMM multiplies each weight stage with two 128-row tiles of them.
+constexpr int kArRows = 16;      // rows of a one-row forward's GEMM input boxes
 constexpr int kPrefillRows = 256;
 // 64-column k-blocks per ring stage of a step's GEMMs (2: each weight row is
 // read 256 contiguous bytes at a time).  Prefill passes use one.
@@ -107,6 +108,9 @@ struct la_handle {
 
     // GEMM plans (bf16): [mode][kind][layer]
     std::vector<TcGemm> plan[2][4];
+    // One-row forwards (la_ar_step): the prefill plans with 16-row input
+    // boxes (UMMA N = 32); same schedules, so the same partial planes.
+    std::vector<TcGemm> plan_ar[4];
     TcGemm plan_lm;
     // Column layout of the GEMM partials: every matrix starts on a 128-column
     // tile boundary, so column c belongs to tile c >> 7.
@@ -298,9 +302,10 @@ int run_gemm(la_handle *h, Mode mode, Kind kind, int l, int nrows) {
     h->launches += 1;
     const int pe = mode == STEP ? h->prof_begin() : -1;
     if (h->bf16) {
-        TcGemm g = h->plan[mode][kind][l];
+        const bool one_row = mode == PREFILL && nrows <= kArRows;
+        TcGemm g = one_row ? h->plan_ar[kind][l] : h->plan[mode][kind][l];
         g.p.nrows = nrows;
-        if (mode == PREFILL) {   // one or two 128-row tiles per weight stage
+        if (mode == PREFILL && !one_row) {   // one or two 128-row tiles per weight stage
             g.p.nrt = nrows > kTileM ? 2 : 1;
             tc_gemm_finalize(g);
         }
@@ -691,6 +696,19 @@ int build_plans(la_handle *h) {
             }
         }
     }
+    for (int kind = 0; kind < 4; ++kind) {
+        const int K = Ks[kind];
+        CUtensorMap bmap;
+        if (make_tmap_bf16(&bmap, xs[kind], K, 2 * h->bh_pf, static_cast<uint64_t>(K) * 2, kBlockK, kArRows))
+            return fail(LA_ERR_CUDA, "tensor map for activations failed");
+        h->plan_ar[kind] = h->plan[PREFILL][kind];
+        for (TcGemm &g : h->plan_ar[kind]) {
+            g.p.b = bmap;
+            g.p.nrt = 1;
+            g.p.bnh = kArRows;
+            tc_gemm_finalize(g);
+        }
+    }
     // lm_head over the used rows
     {
         TcGemm &g = h->plan_lm;
@@ -1000,6 +1018,8 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
         for (int m = 0; m < 2; ++m)
             for (int k = 0; k < 4; ++k)
                 for (auto &g : h->plan[m][k]) g.p.out = h->part;
+        for (int k = 0; k < 4; ++k)
+            for (auto &g : h->plan_ar[k]) g.p.out = h->part;
         h->plan_lm.p.out = h->lm_part;
     }
     if (rc == LA_OK) rc = reset_pool(h);

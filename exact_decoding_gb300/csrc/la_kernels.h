@@ -34,6 +34,8 @@ struct TcGemmParams {
                                  //   stage; tile t of the hi (lo) rows starts at row t * 128 (bh + t * 128)
     int sub;                     // 2-SM kernel: 64-column k-blocks per stage (1, or 2 with nrt == 1); the
                                  //   schedule's k units (kb0, kb1, n_kb) are sub * 64 columns wide
+    int bnh;                     // 2-SM kernel with nrt == 1: input rows per CTA (hi rows from row 0, lo rows
+                                 //   from row bh; UMMA N = 2 bnh, a multiple of 16 rows); 0: gemm2_nhalf(nrt, bh)
     long long split_stride;      // floats between partial planes
     float *out;
     unsigned *err;
