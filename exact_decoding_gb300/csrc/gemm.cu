@@ -344,8 +344,9 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     constexpr uint32_t box_bytes = kTileM * kBlockK * 2;   // 128 rows x 64 columns
     constexpr uint32_t a_bytes = SUB * box_bytes;          // 128 weight rows, SUB k-blocks
-    // Input rows per CTA and row tile: bh (hi rows in rank 0, lo rows in rank
-    // 1) for a step's single row tile, else 128; the UMMA N is twice that.
+    // Input rows per CTA and row tile (hi rows in rank 0, lo rows in rank 1):
+    // bnh when set (a one-row forward), else bh for a single row tile of at
+    // most 128 rows (a step, the lm_head), else 128; the UMMA N is twice that.
     const int nhalf = NRT == 1 && p.bnh > 0 ? p.bnh : gemm2_nhalf(NRT, p.bh);
     const uint32_t bbox_bytes = static_cast<uint32_t>(nhalf) * kBlockK * 2;
     const uint32_t b_bytes = SUB * bbox_bytes;             // this CTA's input rows of one row tile
@@ -643,7 +644,7 @@ __global__ void __launch_bounds__(192, 1) k_gemm_tc2(const __grid_constant__ TcG
 }
 
 // Stage: SUB k-blocks of 128 weight rows and of nrt row tiles of `nhalf`
-// input rows (nhalf = bh with one row tile, 128 with two).
+// input rows (nhalf as in the kernel: bnh, bh or 128).
 static size_t gemm2_stage_bytes(int nrt, int sub, int nhalf) {
     return static_cast<size_t>(sub) * (kTileM + nrt * nhalf) * kBlockK * 2;
 }
@@ -768,8 +769,8 @@ void stream_k_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, st
 // Whole tiles first, stream-K for the rest: each CTA takes an even share of
 // the k-blocks of the last `tiles % ctas` tiles (split as above, planes in
 // CTA order), then `tiles / ctas` whole tiles of its own (one plane each).
-// Split tiles are done early in every CTA's run, so the CTA that completes
-// one can finish it while its whole tiles stream.
+// Split tiles are done early in every CTA's run, so the CTAs that share one
+// can finish it (the fused SwiGLU) while their whole tiles stream.
 void hybrid_schedule(int tiles, int n_kb, int ctas, std::vector<int> &segs, std::vector<int> &cta_first,
                      std::vector<int> &tile_planes) {
     const int whole = ctas > 0 ? tiles / ctas : 0;

@@ -44,12 +44,14 @@ struct TcGemmParams {
     // Gate/up GEMM with SwiGLU (2-SM kernel, fuse_out set).  a[0] = gate and
     // a[1] = up weights, boxes of 64 rows: CTA rank r of pair tile t holds
     // gate rows f0 .. f0 + 63 in its TMEM lanes 0..63 and the up rows of the
-    // same features in lanes 64..127, f0 = 128 t + 64 r.  Its partials go to
-    // output column 128 (2 t + r) + lane like any segment's.  The CTA that
-    // brings a 128-column tile's arrival count to fuse_np[tile] (the tile's
-    // planes) adds the planes in plane order, writes silu(gate) * up as
-    // (hi, lo) bf16 rows fuse_out[row][f] (+ fuse_lo_off) for f < fuse_F,
-    // and resets the count to 0 for the next launch.
+    // same features in lanes 64..127, f0 = 128 t + 64 r.  A tile one segment
+    // covers (fuse_np[tile] == 1) goes from TMEM straight to silu(gate) * up,
+    // written as (hi, lo) bf16 rows fuse_out[row][f] (+ fuse_lo_off) for f <
+    // fuse_F.  A split tile's pieces go to output column 128 (2 t + r) + lane
+    // of their partial planes and add 1 to fuse_cnt[tile]; once the count
+    // reaches the next multiple of fuse_np[tile] (it is never reset), every
+    // contributing CTA adds the planes, in plane order, for its share of the
+    // rows (share = its plane) and writes them the same way.
     int *fuse_cnt;
     const int *fuse_np;
     __nv_bfloat16 *fuse_out;
