@@ -210,6 +210,8 @@ struct la_handle {
         s.U = U;
         s.T = opts.temperature;
         s.seed = opts.seed;
+        s.step_zero = fuse_cnt;
+        s.n_step_zero = fuse_cnt ? fuse_tiles : 0;
         return s;
     }
 
@@ -512,7 +514,8 @@ int check_device_error(la_handle *h) {
     if (h->st_host->err) {
         const unsigned e = h->st_host->err;
         h->prefilled = false;
-        // A gate/up launch whose waits gave up may have left arrival counts.
+        // A gate/up launch whose waits gave up may have left arrival counts
+        // (the next step's row build also clears them).
         if (h->fuse_cnt) cudaMemsetAsync(h->fuse_cnt, 0, sizeof(int) * h->fuse_tiles, h->stream);
         return fail(LA_ERR_DEVICE_TIMEOUT, "device error bits 0x%x (bounded wait gave up or pool full)", e);
     }

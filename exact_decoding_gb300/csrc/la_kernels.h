@@ -253,6 +253,8 @@ struct SpecDev {
     int N, W, G, M, U;
     float T;
     unsigned long long seed;
+    int *step_zero;       // [n_step_zero] counts the step's kernels start from 0 (gate/up arrivals), or nullptr
+    int n_step_zero;
 };
 
 cudaError_t build_rows_launch(const SpecDev &d, cudaStream_t s);

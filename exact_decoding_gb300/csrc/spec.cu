@@ -254,6 +254,10 @@ __device__ void pool_insert_warp(const SpecDev &d, int key, const int *suf, int 
 __global__ void __launch_bounds__(256) k_build_rows(SpecDev d) {
     pdl_trigger();
     pdl_wait();
+    // Every kernel of the previous step has completed: its gate/up GEMMs'
+    // arrival counts start this step from 0 (a step adds at most layers x
+    // planes to each, far from overflow).
+    for (int i = threadIdx.x; i < d.n_step_zero; i += blockDim.x) d.step_zero[i] = 0;
     __shared__ int s_g;
     __shared__ int s_c[32 * 8];
     const int L = d.N - 1;
