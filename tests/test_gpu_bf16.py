@@ -62,6 +62,15 @@ def test_bf16_long_prompt_spans_chunks(lib):
     run_teacher_forced(lib, w, p, N=5, W=7, G=7, steps=6)
 
 
+def test_bf16_short_prompt(lib):
+    """A 12-token prompt: the prefill pass has at most 16 rows, so its GEMMs
+    take the one-row forwards' 16-row input boxes."""
+    dims = SMALL["gqa-hd128"]
+    w = decisive_weights(dims, seed=15)
+    p = synth.uniform_tokens(12, dims.vocab, seed=16)
+    run_teacher_forced(lib, w, p, N=4, W=5, G=3, steps=6)
+
+
 def test_bf16_repetitive_prompt_accepts(lib):
     """A repeated prompt with prompt-as-reference: candidates hit, and at
     least one step that accepted more than one token is compared exactly."""
