@@ -1468,6 +1468,22 @@ static int la_selftest_timeout_body(la_handle *h, int64_t limit_ns, void *stream
     return LA_OK;
 }
 
+static int la_gemm_schedule_body(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,
+                                 int32_t max_segs, int32_t *cta_first, int32_t *ctas_used, int32_t *planes) {
+    if (tiles < 1 || n_kb < 1 || ctas < 1 || max_segs < 0 || !segs || !cta_first || !ctas_used || !planes)
+        return fail(LA_ERR_INVALID_ARG, "la_gemm_schedule: sizes must be >= 1 and pointers non-null");
+    std::vector<int> sg, first, tp;
+    if (whole_first) hybrid_schedule(tiles, n_kb, ctas, sg, first, tp);
+    else stream_k_schedule(tiles, n_kb, ctas, sg, first, tp);
+    const int nseg = static_cast<int>(sg.size() / 4);
+    if (nseg > max_segs) return fail(LA_ERR_CAPACITY, "la_gemm_schedule: %d segments, room for %d", nseg, max_segs);
+    std::copy(sg.begin(), sg.end(), segs);
+    std::copy(first.begin(), first.end(), cta_first);
+    std::copy(tp.begin(), tp.end(), planes);
+    *ctas_used = static_cast<int32_t>(first.size()) - 1;
+    return nseg;
+}
+
 // Exported entry points: each runs its body under abi_guard, so no C++
 // exception crosses the C ABI.
 int la_create(const la_model_dims *dims, const la_weights *w, const la_opts *opts, la_handle **out) {
@@ -1515,6 +1531,13 @@ int la_gemm_status(void *stream) {
 
 int la_selftest_timeout(la_handle *h, int64_t limit_ns, void *stream) {
     return abi_guard("la_selftest_timeout", [&] { return la_selftest_timeout_body(h, limit_ns, stream); });
+}
+
+int la_gemm_schedule(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,
+                     int32_t max_segs, int32_t *cta_first, int32_t *ctas_used, int32_t *planes) {
+    return abi_guard("la_gemm_schedule", [&] {
+        return la_gemm_schedule_body(tiles, n_kb, ctas, whole_first, segs, max_segs, cta_first, ctas_used, planes);
+    });
 }
 
 }  // extern "C"

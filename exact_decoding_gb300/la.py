@@ -61,6 +61,7 @@ class la_stats_t(ctypes.Structure):
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
+LA_ERR_CAPACITY = -3   # include/la.h
 
 
 class la_state_t(ctypes.Structure):
@@ -94,6 +95,8 @@ def load_library():
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
     lib.la_gemm_status.argtypes = [ctypes.c_void_p]
     lib.la_selftest_timeout.argtypes = [H, ctypes.c_int64, ctypes.c_void_p]
+    lib.la_gemm_schedule.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I32P,
+                                     ctypes.c_int32, _I32P, _I32P, _I32P]
     lib.la_destroy.argtypes = [H]
     lib.la_destroy.restype = None
     lib.la_strerror.argtypes = [ctypes.c_int]
@@ -102,7 +105,7 @@ def load_library():
     lib.la_last_error.restype = ctypes.c_char_p
     for name in ("la_create", "la_prefill", "la_step", "la_ar_step", "la_generate", "la_stats", "la_export_state",
                  "la_import_state", "la_debug_logits", "la_gemm_bf16", "la_gemm_bf16_noalloc", "la_gemm_status",
-                 "la_selftest_timeout"):
+                 "la_selftest_timeout", "la_gemm_schedule"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -229,6 +232,28 @@ def la_selftest_timeout(h, limit_ns: int, stream: Optional[int] = None) -> None:
     limit_ns and sets a timeout bit in h's error word, or with h None in the
     standalone GEMMs' words)."""
     _check(load_library().la_selftest_timeout(h, limit_ns, stream), "la_selftest_timeout")
+
+
+def la_gemm_schedule(tiles: int, n_kb: int, ctas: int, whole_first: bool):
+    """The projection GEMMs' work split, from the library's host code: returns
+    (segments [n][4] of (tile, kb0, kb1, plane), cta_first [ctas_used + 1],
+    planes per tile [tiles]) as int32 numpy arrays.  No GPU is touched."""
+    import numpy as np
+    lib = load_library()
+    cap = tiles + ctas + 16                      # a run adds at most one segment per tile boundary
+    while True:
+        segs = np.zeros((cap, 4), dtype=np.int32)
+        first = np.zeros(ctas + 1, dtype=np.int32)
+        used = np.zeros(1, dtype=np.int32)
+        planes = np.zeros(tiles, dtype=np.int32)
+        ptr = lambda a: a.ctypes.data_as(_I32P)
+        n = lib.la_gemm_schedule(tiles, n_kb, ctas, int(bool(whole_first)), ptr(segs), cap, ptr(first), ptr(used),
+                                 ptr(planes))
+        if n == LA_ERR_CAPACITY:
+            cap *= 2
+            continue
+        _check(n if n < 0 else 0, "la_gemm_schedule")
+        return segs[:n].copy(), first[:used[0] + 1].copy(), planes
 
 
 def la_destroy(h) -> None:

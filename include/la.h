@@ -311,6 +311,22 @@ int la_gemm_status(void *stream);
  * Asynchronous.  Errors: INVALID_ARG (limit), CUDA. */
 int la_selftest_timeout(la_handle *h, int64_t limit_ns, void *stream);
 
+/* Test support (no passage): the work split of the projection GEMMs,
+ * computed on the host; no GPU is touched.  `tiles` output tiles of n_kb
+ * k-units each over `ctas` persistent CTAs (CTA pairs on the GPU).
+ * whole_first = 0: stream-K (the flattened tile x k-unit work cut into equal
+ * contiguous runs); 1: the step gate/up GEMM's split (each CTA first takes
+ * an even share of the k-units of the last tiles % ctas tiles, then
+ * tiles / ctas whole tiles).  Writes up to max_segs segments as int32
+ * (tile, kb0, kb1, plane) quadruples to segs, cta_first[0 .. *ctas_used]
+ * (CTA c runs segments cta_first[c] .. cta_first[c + 1] - 1; cta_first must
+ * hold ctas + 1 entries) and planes[0 .. tiles) (partial planes per tile;
+ * plane p of a tile is its p-th segment in CTA order).  Returns the number
+ * of segments.  Errors: INVALID_ARG (a size < 1 or a null pointer),
+ * CAPACITY (more than max_segs segments; nothing written to segs). */
+int la_gemm_schedule(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,
+                     int32_t max_segs, int32_t *cta_first, int32_t *ctas_used, int32_t *planes);
+
 void la_destroy(la_handle *h);
 const char *la_strerror(int code);
 const char *la_last_error(void);
