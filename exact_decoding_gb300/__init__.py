@@ -7,9 +7,9 @@ runs in libla.so.  Import fails loudly if the library has not been built
 """
 from .la import (LaError, Decoder, DeviceWeights, la_create, la_prefill, la_step, la_ar_step, la_generate, la_stats,
                  la_export_state, la_import_state, la_debug_logits, la_gemm_bf16, la_gemm_bf16_noalloc, la_gemm_status,
-                 la_selftest_timeout, la_gemm_schedule, la_destroy, la_strerror, load_library, LIB_PATH)
+                 la_selftest_timeout, la_gemm_schedule, la_step_tables, la_destroy, la_strerror, load_library, LIB_PATH)
 
 __all__ = ["LaError", "Decoder", "DeviceWeights", "la_create", "la_prefill", "la_step", "la_ar_step", "la_generate", "la_stats",
            "la_export_state", "la_import_state", "la_debug_logits", "la_gemm_bf16", "la_gemm_bf16_noalloc", "la_gemm_status",
-           "la_selftest_timeout", "la_gemm_schedule", "la_destroy",
+           "la_selftest_timeout", "la_gemm_schedule", "la_step_tables", "la_destroy",
            "la_strerror", "load_library", "LIB_PATH"]

@@ -281,6 +281,24 @@ void step_structure(int N, int W, int G, std::vector<int> &parent, std::vector<i
         }
 }
 
+// Static tables of a step's rows: depth (position offset from the prefix
+// length), the 256-bit visibility word of each row (bit s of word s / 32: the
+// row attends to step row s, i.e. s is the row itself or one of its
+// ancestors) and the rows whose logits the step reads (row 0, the top window
+// level, every candidate row).
+void step_tables(int N, int W, int G, std::vector<int> &depth, std::vector<uint32_t> &bits, std::vector<int> &used) {
+    std::vector<int> parent;
+    step_structure(N, W, G, parent, depth);
+    const int M = static_cast<int>(parent.size());
+    bits.assign(static_cast<size_t>(M) * 8, 0u);
+    for (int r = 0; r < M; ++r)
+        for (int x = r; x >= 0; x = parent[x]) bits[static_cast<size_t>(r) * 8 + x / 32] |= 1u << (x % 32);
+    used.assign(1, 0);
+    for (int j = 0; j < W; ++j) used.push_back(1 + (N - 2) * W + j);
+    for (int c = 0; c < G; ++c)
+        for (int m = 1; m < N; ++m) used.push_back(1 + (N - 1) * W + c * (N - 1) + (m - 1));
+}
+
 uint64_t splitmix64(uint64_t x) {
     x += 0x9E3779B97F4A7C15ull;
     x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
@@ -933,8 +951,10 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
                 rope[static_cast<size_t>(p) * (h->hd / 2) + i] =
                     make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
             }
-        std::vector<int> parent, depth;
+        std::vector<int> parent, depth, used;
+        std::vector<uint32_t> bits;
         step_structure(h->N, h->W, h->G, parent, depth);
+        step_tables(h->N, h->W, h->G, depth, bits, used);
         std::vector<int> anc(static_cast<size_t>(M) * h->anc_stride, 0), cnt(M, 0);
         for (int r = 0; r < M; ++r) {
             std::vector<int> chain;
@@ -943,17 +963,6 @@ static int la_create_body(const la_model_dims *dims, const la_weights *w, const 
             cnt[r] = static_cast<int>(chain.size());
             for (size_t i = 0; i < chain.size(); ++i) anc[static_cast<size_t>(r) * h->anc_stride + i] = chain[i];
         }
-        std::vector<uint32_t> bits(static_cast<size_t>(M) * 8, 0u);
-        for (int r = 0; r < M; ++r)
-            for (int i = 0; i < cnt[r]; ++i) {
-                const int a = anc[static_cast<size_t>(r) * h->anc_stride + i];
-                bits[static_cast<size_t>(r) * 8 + a / 32] |= 1u << (a % 32);
-            }
-        std::vector<int> used;
-        used.push_back(0);
-        for (int j = 0; j < h->W; ++j) used.push_back(1 + (h->N - 2) * h->W + j);
-        for (int c = 0; c < h->G; ++c)
-            for (int m = 1; m < h->N; ++m) used.push_back(1 + (h->N - 1) * h->W + c * (h->N - 1) + (m - 1));
         std::vector<int> iota(R);
         for (int i = 0; i < R; ++i) iota[i] = i;
         if (cudaMemcpy(h->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -1468,6 +1477,23 @@ static int la_selftest_timeout_body(la_handle *h, int64_t limit_ns, void *stream
     return LA_OK;
 }
 
+static int la_step_tables_body(int32_t N, int32_t W, int32_t G, int32_t *depth, uint32_t *vis, int32_t *used,
+                               int32_t max_rows, int32_t *m_out, int32_t *u_out) {
+    if (N < 2 || W < 1 || G < 0 || !depth || !vis || !used || !m_out || !u_out)
+        return fail(LA_ERR_INVALID_ARG, "la_step_tables: N >= 2, W >= 1, G >= 0 and non-null pointers");
+    const long long M = 1 + static_cast<long long>(W + G) * (N - 1);
+    if (M > 256 || M > max_rows) return fail(LA_ERR_CAPACITY, "la_step_tables: %lld rows (at most 256 and max_rows)", M);
+    std::vector<int> dp, us;
+    std::vector<uint32_t> bits;
+    step_tables(N, W, G, dp, bits, us);
+    std::copy(dp.begin(), dp.end(), depth);
+    std::copy(bits.begin(), bits.end(), vis);
+    std::copy(us.begin(), us.end(), used);
+    *m_out = static_cast<int32_t>(dp.size());
+    *u_out = static_cast<int32_t>(us.size());
+    return LA_OK;
+}
+
 static int la_gemm_schedule_body(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,
                                  int32_t max_segs, int32_t *cta_first, int32_t *ctas_used, int32_t *planes) {
     if (tiles < 1 || n_kb < 1 || ctas < 1 || max_segs < 0 || !segs || !cta_first || !ctas_used || !planes)
@@ -1531,6 +1557,12 @@ int la_gemm_status(void *stream) {
 
 int la_selftest_timeout(la_handle *h, int64_t limit_ns, void *stream) {
     return abi_guard("la_selftest_timeout", [&] { return la_selftest_timeout_body(h, limit_ns, stream); });
+}
+
+int la_step_tables(int32_t N, int32_t W, int32_t G, int32_t *depth, uint32_t *vis, int32_t *used, int32_t max_rows,
+                   int32_t *m_out, int32_t *u_out) {
+    return abi_guard("la_step_tables",
+                     [&] { return la_step_tables_body(N, W, G, depth, vis, used, max_rows, m_out, u_out); });
 }
 
 int la_gemm_schedule(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,

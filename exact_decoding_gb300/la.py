@@ -95,6 +95,8 @@ def load_library():
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
     lib.la_gemm_status.argtypes = [ctypes.c_void_p]
     lib.la_selftest_timeout.argtypes = [H, ctypes.c_int64, ctypes.c_void_p]
+    lib.la_step_tables.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I32P,
+                                   ctypes.POINTER(ctypes.c_uint32), _I32P, ctypes.c_int32, _I32P, _I32P]
     lib.la_gemm_schedule.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I32P,
                                      ctypes.c_int32, _I32P, _I32P, _I32P]
     lib.la_destroy.argtypes = [H]
@@ -105,7 +107,7 @@ def load_library():
     lib.la_last_error.restype = ctypes.c_char_p
     for name in ("la_create", "la_prefill", "la_step", "la_ar_step", "la_generate", "la_stats", "la_export_state",
                  "la_import_state", "la_debug_logits", "la_gemm_bf16", "la_gemm_bf16_noalloc", "la_gemm_status",
-                 "la_selftest_timeout", "la_gemm_schedule"):
+                 "la_selftest_timeout", "la_gemm_schedule", "la_step_tables"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -232,6 +234,23 @@ def la_selftest_timeout(h, limit_ns: int, stream: Optional[int] = None) -> None:
     limit_ns and sets a timeout bit in h's error word, or with h None in the
     standalone GEMMs' words)."""
     _check(load_library().la_selftest_timeout(h, limit_ns, stream), "la_selftest_timeout")
+
+
+def la_step_tables(N: int, W: int, G: int):
+    """The static tables of a step's rows, from the library's host code:
+    (depth [M], visibility words [M][8] as uint32, used rows [U]) as numpy
+    arrays.  No GPU is touched."""
+    import numpy as np
+    lib = load_library()
+    depth = np.zeros(256, dtype=np.int32)
+    vis = np.zeros((256, 8), dtype=np.uint32)
+    used = np.zeros(256, dtype=np.int32)
+    m = np.zeros(1, dtype=np.int32)
+    u = np.zeros(1, dtype=np.int32)
+    rc = lib.la_step_tables(N, W, G, depth.ctypes.data_as(_I32P), vis.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)),
+                            used.ctypes.data_as(_I32P), 256, m.ctypes.data_as(_I32P), u.ctypes.data_as(_I32P))
+    _check(rc, "la_step_tables")
+    return depth[:m[0]].copy(), vis[:m[0]].copy(), used[:u[0]].copy()
 
 
 def la_gemm_schedule(tiles: int, n_kb: int, ctas: int, whole_first: bool):

@@ -311,6 +311,21 @@ int la_gemm_status(void *stream);
  * Asynchronous.  Errors: INVALID_ARG (limit), CUDA. */
 int la_selftest_timeout(la_handle *h, int64_t limit_ns, void *stream);
 
+/* Test support: the static tables of a step's rows for (N, W, G), as the
+ * library builds them at la_create (the mask of section 3.4 "Integrated
+ * Forward Pass", Figure 2b, with row 0 the last committed token, window row
+ * 1 + k W + j for level k and column j, candidate row 1 + (N-1) W + c (N-1)
+ * + m - 1 for candidate c and depth m).  Host only; no GPU is touched.
+ * Writes, with M = 1 + (W + G)(N - 1) and U = 1 + W + G (N - 1):
+ *   depth[M]     position offset of each row from the prefix length
+ *   vis[M][8]    bit s % 32 of word s / 32: row r attends to step row s
+ *   used[U]      the rows whose logits the step reads (row 0, the top
+ *                window level, every candidate row)
+ * and *m_out = M, *u_out = U.  Errors: INVALID_ARG (N < 2, W < 1, G < 0, a
+ * null pointer), CAPACITY (M > 256 or M > max_rows; nothing written). */
+int la_step_tables(int32_t N, int32_t W, int32_t G, int32_t *depth, uint32_t *vis, int32_t *used, int32_t max_rows,
+                   int32_t *m_out, int32_t *u_out);
+
 /* Test support (no passage): the work split of the projection GEMMs,
  * computed on the host; no GPU is touched.  `tiles` output tiles of n_kb
  * k-units each over `ctas` persistent CTAs (CTA pairs on the GPU).
