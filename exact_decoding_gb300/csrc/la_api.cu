@@ -1495,8 +1495,9 @@ static int la_step_tables_body(int32_t N, int32_t W, int32_t G, int32_t *depth, 
 }
 
 static int la_gemm_schedule_body(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,
-                                 int32_t max_segs, int32_t *cta_first, int32_t *ctas_used, int32_t *planes) {
-    if (tiles < 1 || n_kb < 1 || ctas < 1 || max_segs < 0 || !segs || !cta_first || !ctas_used || !planes)
+                                 int32_t max_segs, int32_t *nseg_out, int32_t *cta_first, int32_t *ctas_used,
+                                 int32_t *planes) {
+    if (tiles < 1 || n_kb < 1 || ctas < 1 || max_segs < 0 || !segs || !nseg_out || !cta_first || !ctas_used || !planes)
         return fail(LA_ERR_INVALID_ARG, "la_gemm_schedule: sizes must be >= 1 and pointers non-null");
     std::vector<int> sg, first, tp;
     if (whole_first) hybrid_schedule(tiles, n_kb, ctas, sg, first, tp);
@@ -1507,7 +1508,8 @@ static int la_gemm_schedule_body(int32_t tiles, int32_t n_kb, int32_t ctas, int3
     std::copy(first.begin(), first.end(), cta_first);
     std::copy(tp.begin(), tp.end(), planes);
     *ctas_used = static_cast<int32_t>(first.size()) - 1;
-    return nseg;
+    *nseg_out = nseg;
+    return LA_OK;
 }
 
 // Exported entry points: each runs its body under abi_guard, so no C++
@@ -1566,9 +1568,10 @@ int la_step_tables(int32_t N, int32_t W, int32_t G, int32_t *depth, uint32_t *vi
 }
 
 int la_gemm_schedule(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,
-                     int32_t max_segs, int32_t *cta_first, int32_t *ctas_used, int32_t *planes) {
+                     int32_t max_segs, int32_t *nseg, int32_t *cta_first, int32_t *ctas_used, int32_t *planes) {
     return abi_guard("la_gemm_schedule", [&] {
-        return la_gemm_schedule_body(tiles, n_kb, ctas, whole_first, segs, max_segs, cta_first, ctas_used, planes);
+        return la_gemm_schedule_body(tiles, n_kb, ctas, whole_first, segs, max_segs, nseg, cta_first, ctas_used,
+                                     planes);
     });
 }
 

@@ -98,7 +98,7 @@ def load_library():
     lib.la_step_tables.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I32P,
                                    ctypes.POINTER(ctypes.c_uint32), _I32P, ctypes.c_int32, _I32P, _I32P]
     lib.la_gemm_schedule.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I32P,
-                                     ctypes.c_int32, _I32P, _I32P, _I32P]
+                                     ctypes.c_int32, _I32P, _I32P, _I32P, _I32P]
     lib.la_destroy.argtypes = [H]
     lib.la_destroy.restype = None
     lib.la_strerror.argtypes = [ctypes.c_int]
@@ -264,15 +264,16 @@ def la_gemm_schedule(tiles: int, n_kb: int, ctas: int, whole_first: bool):
         segs = np.zeros((cap, 4), dtype=np.int32)
         first = np.zeros(ctas + 1, dtype=np.int32)
         used = np.zeros(1, dtype=np.int32)
+        nseg = np.zeros(1, dtype=np.int32)
         planes = np.zeros(tiles, dtype=np.int32)
         ptr = lambda a: a.ctypes.data_as(_I32P)
-        n = lib.la_gemm_schedule(tiles, n_kb, ctas, int(bool(whole_first)), ptr(segs), cap, ptr(first), ptr(used),
-                                 ptr(planes))
-        if n == LA_ERR_CAPACITY:
+        rc = lib.la_gemm_schedule(tiles, n_kb, ctas, int(bool(whole_first)), ptr(segs), cap, ptr(nseg), ptr(first),
+                                  ptr(used), ptr(planes))
+        if rc == LA_ERR_CAPACITY:
             cap *= 2
             continue
-        _check(n if n < 0 else 0, "la_gemm_schedule")
-        return segs[:n].copy(), first[:used[0] + 1].copy(), planes
+        _check(rc, "la_gemm_schedule")
+        return segs[:nseg[0]].copy(), first[:used[0] + 1].copy(), planes
 
 
 def la_destroy(h) -> None:

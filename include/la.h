@@ -336,11 +336,11 @@ int la_step_tables(int32_t N, int32_t W, int32_t G, int32_t *depth, uint32_t *vi
  * (tile, kb0, kb1, plane) quadruples to segs, cta_first[0 .. *ctas_used]
  * (CTA c runs segments cta_first[c] .. cta_first[c + 1] - 1; cta_first must
  * hold ctas + 1 entries) and planes[0 .. tiles) (partial planes per tile;
- * plane p of a tile is its p-th segment in CTA order).  Returns the number
- * of segments.  Errors: INVALID_ARG (a size < 1 or a null pointer),
+ * plane p of a tile is its p-th segment in CTA order), and the number of
+ * segments to *nseg.  Errors: INVALID_ARG (a size < 1 or a null pointer),
  * CAPACITY (more than max_segs segments; nothing written to segs). */
 int la_gemm_schedule(int32_t tiles, int32_t n_kb, int32_t ctas, int32_t whole_first, int32_t *segs,
-                     int32_t max_segs, int32_t *cta_first, int32_t *ctas_used, int32_t *planes);
+                     int32_t max_segs, int32_t *nseg, int32_t *cta_first, int32_t *ctas_used, int32_t *planes);
 
 void la_destroy(la_handle *h);
 const char *la_strerror(int code);
